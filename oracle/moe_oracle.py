@@ -1,0 +1,283 @@
+"""CPU oracle of the W4A16 routed-expert MoE layer — TEST INFRASTRUCTURE.
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+import this module. The product path (the CUDA library and its binding) never
+calls it and shares no code with it; this file imports nothing from the
+package.
+
+Plain, slow, obviously-correct NumPy in float64, one function per step of the
+layer, each step written in the order the layer defines it:
+
+1. router logits ``L = x W_r^T (+ b)``                       -> router_logits
+2. softmax over all E experts                                -> softmax_rows
+3. top-k, ties to the lowest expert id, rank order            -> select_topk
+4. routing weights (softmax value, optionally renormalised)   -> routing_weights
+5. counting-sort permutation by expert                        -> counting_sort
+6. expert FFN ``y = W_d (silu(W_g x) * (W_u x))`` on dequantised INT4 weights
+                                                              -> expert_ffn
+7. weighted combine ``out = sum_j w_j y_j (+ y_shared)``     -> moe_forward
+
+Sources (page title, section):
+* Horizon RunMap report, "Architecture invariants" / "What is implemented" /
+  "The complete execution path" step 2: routed experts stored as INT4 qpacked
+  data with FP16 scales, executed with FP16 activations; routing selects the
+  experts each token needs.
+* moe-stream, "Terms used here" and "Method": a router picks 8 of 64 experts
+  per token at each layer (the OLMoE shape).
+* F51 Nitro-MoE, "The thesis": 10 routed experts plus one shared expert.
+The pages give no formulas for the layer; where they are silent this oracle
+takes the plain readings that the layer's specification states: zero point 8,
+one FP16 scale per G codes along K, SwiGLU ``silu(g) * u``, softmax over all
+experts, ties to the lowest id, shared expert with weight 1.
+
+Record layout (its own reading of the canonical format): sections gate_q,
+up_q, down_q, gate_s, up_s, down_s, each starting on a 256-byte boundary;
+codes row-major with K contiguous, low nibble = even k.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------
+# expert record
+# ----------------------------------------------------------------------------
+
+def _align256(v: int) -> int:
+    return -(-v // 256) * 256
+
+
+def record_layout(H: int, I: int, G: int):
+    """Section offsets of one expert record and the padded record size."""
+    groups_h = -(-H // G)
+    groups_i = -(-I // G)
+    order = (("gate_q", I * (H // 2)), ("up_q", I * (H // 2)), ("down_q", H * (I // 2)),
+             ("gate_s", 2 * I * groups_h), ("up_s", 2 * I * groups_h), ("down_s", 2 * H * groups_i))
+    offs = {}
+    cur = 0
+    for name, nbytes in order:
+        cur = _align256(cur)
+        offs[name] = (cur, nbytes)
+        cur += nbytes
+    return offs, _align256(cur)
+
+
+def unpack_codes(raw: np.ndarray, N: int, K: int) -> np.ndarray:
+    """Bytes of an [N][K] code matrix -> integer codes 0..15.
+
+    Byte b of a row holds code k = 2b in its low four bits and k = 2b + 1 in
+    its high four bits."""
+    raw = np.asarray(raw, dtype=np.uint8).reshape(N, K // 2).astype(np.int64)
+    q = np.empty((N, K), dtype=np.int64)
+    q[:, 0::2] = raw % 16
+    q[:, 1::2] = raw // 16
+    return q
+
+
+def dequantize(q: np.ndarray, scales: np.ndarray, G: int) -> np.ndarray:
+    """w[n, k] = (q[n, k] - 8) * s[n, k // G] in float64."""
+    N, K = q.shape
+    s = np.asarray(scales, dtype=np.float16).astype(np.float64)
+    group_of_k = np.arange(K) // G
+    return (q.astype(np.float64) - 8.0) * s[:, group_of_k]
+
+
+def expert_matrices(record: np.ndarray, H: int, I: int, G: int):
+    """Dequantised (W_gate [I][H], W_up [I][H], W_down [H][I]) of one record."""
+    offs, _ = record_layout(H, I, G)
+    rec = np.asarray(record, dtype=np.uint8).reshape(-1)
+
+    def sect(name):
+        o, n = offs[name]
+        return rec[o:o + n]
+
+    gh, gi = -(-H // G), -(-I // G)
+    wg = dequantize(unpack_codes(sect("gate_q"), I, H), sect("gate_s").view(np.float16).reshape(I, gh), G)
+    wu = dequantize(unpack_codes(sect("up_q"), I, H), sect("up_s").view(np.float16).reshape(I, gh), G)
+    wd = dequantize(unpack_codes(sect("down_q"), H, I), sect("down_s").view(np.float16).reshape(H, gi), G)
+    return wg, wu, wd
+
+
+# ----------------------------------------------------------------------------
+# routing
+# ----------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, router_w: np.ndarray, router_bias=None) -> np.ndarray:
+    """L[t, e] = sum_h x[t, h] * W_r[e, h]  (+ b[e]) in float64."""
+    L = np.asarray(x, dtype=np.float64) @ np.asarray(router_w, dtype=np.float64).T
+    if router_bias is not None:
+        L = L + np.asarray(router_bias, dtype=np.float64)[None, :]
+    return L
+
+
+def softmax_rows(L: np.ndarray) -> np.ndarray:
+    """Softmax over all experts of each row, with the row max subtracted."""
+    m = L.max(axis=1, keepdims=True)
+    z = np.exp(L - m)
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def select_topk(L: np.ndarray, k: int) -> np.ndarray:
+    """k rounds of selection: each round takes the largest remaining logit,
+    the lowest expert id among equal logits. Result in rank order."""
+    T, E = L.shape
+    ids = np.empty((T, k), dtype=np.int64)
+    for t in range(T):
+        taken = np.zeros(E, dtype=bool)
+        for j in range(k):
+            best = -1
+            for e in range(E):
+                if taken[e]:
+                    continue
+                if best < 0 or L[t, e] > L[t, best]:
+                    best = e
+            ids[t, j] = best
+            taken[best] = True
+    return ids
+
+
+def select_topk_fast(L: np.ndarray, k: int) -> np.ndarray:
+    """Same selection as select_topk, vectorised over tokens (np.argmax
+    returns the first, i.e. lowest, index among equal maxima)."""
+    work = np.array(L, dtype=np.float64, copy=True)
+    T = work.shape[0]
+    ids = np.empty((T, k), dtype=np.int64)
+    rows = np.arange(T)
+    for j in range(k):
+        best = np.argmax(work, axis=1)
+        ids[:, j] = best
+        work[rows, best] = -np.inf
+    return ids
+
+
+def routing_weights(p: np.ndarray, ids: np.ndarray, renormalize: bool) -> np.ndarray:
+    """w[t, j] = p[t, ids[t, j]], divided by the sum over the selected experts
+    when renormalising."""
+    w = np.take_along_axis(p, ids, axis=1)
+    if renormalize:
+        w = w / w.sum(axis=1, keepdims=True)
+    return w
+
+
+def counting_sort(ids: np.ndarray, E: int):
+    """Counting sort of the flat (token, rank) pairs f = t*k + j by expert.
+
+    counts[e]   = number of pairs routed to e
+    offsets     = exclusive prefix sum of counts, offsets[E] = T*k
+    perm[p]     = flat index at sorted position p (ascending f within an expert)
+    inv_perm[f] = sorted position of flat index f
+    """
+    flat = np.asarray(ids, dtype=np.int64).reshape(-1)
+    n = flat.size
+    counts = np.zeros(E, dtype=np.int64)
+    for e in flat:
+        counts[e] += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    cursor = offsets[:E].copy()
+    perm = np.empty(n, dtype=np.int64)
+    inv_perm = np.empty(n, dtype=np.int64)
+    for f in range(n):
+        e = flat[f]
+        perm[cursor[e]] = f
+        inv_perm[f] = cursor[e]
+        cursor[e] += 1
+    return counts, offsets, perm, inv_perm
+
+
+# ----------------------------------------------------------------------------
+# expert FFN and combine
+# ----------------------------------------------------------------------------
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z / (1 + exp(-z))."""
+    return z / (1.0 + np.exp(-z))
+
+
+def expert_ffn(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, xrows: np.ndarray) -> np.ndarray:
+    """SwiGLU expert: y = W_d (silu(W_g x) * (W_u x)) for each row of xrows."""
+    x64 = np.asarray(xrows, dtype=np.float64)
+    g = x64 @ wg.T
+    u = x64 @ wu.T
+    h = silu(g) * u
+    return h @ wd.T
+
+
+def moe_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k, G,
+                renormalize, has_shared=False, tokens=None):
+    """Whole layer for the tokens in ``tokens`` (default: all).
+
+    Routing (logits, softmax, selection, weights, permutation) is computed for
+    every token of the batch; expert outputs and the combine only for the
+    requested tokens. Returns a dict of float64 / int64 arrays."""
+    x = np.asarray(x)
+    T = x.shape[0]
+    L = router_logits(x, router_w, router_bias)
+    p = softmax_rows(L)
+    ids = select_topk_fast(L, k)
+    w = routing_weights(p, ids, renormalize)
+    counts, offsets, perm, inv_perm = counting_sort(ids, E)
+    if tokens is None:
+        tokens = np.arange(T)
+    tokens = np.asarray(tokens, dtype=np.int64)
+    out = np.zeros((tokens.size, H), dtype=np.float64)
+    used = sorted(set(int(e) for e in ids[tokens].reshape(-1)))
+    for e in used:
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[e])], H, I, G)
+        for j in range(k):
+            rows = np.nonzero(ids[tokens, j] == e)[0]
+            if rows.size == 0:
+                continue
+            y = expert_ffn(wg, wu, wd, x[tokens[rows]])
+            out[rows] += w[tokens[rows], j][:, None] * y
+    if has_shared:
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[E])], H, I, G)
+        out += expert_ffn(wg, wu, wd, x[tokens])
+    return dict(out=out, logits=L, probs=p, ids=ids, weights=w, counts=counts,
+                offsets=offsets, perm=perm, inv_perm=inv_perm)
+
+
+def dense_masked_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k, G,
+                         renormalize, has_shared=False):
+    """Brute force: every expert runs on every token; a [T][E] mask-weight
+    matrix (zero for experts a token did not select) combines them."""
+    x = np.asarray(x)
+    T = x.shape[0]
+    L = router_logits(x, router_w, router_bias)
+    p = softmax_rows(L)
+    # full descending order of each row, lower id first among equals
+    order = np.lexsort((np.broadcast_to(np.arange(E), (T, E)), -L), axis=1)
+    sel = order[:, :k]
+    M = np.zeros((T, E), dtype=np.float64)
+    for t in range(T):
+        ps = p[t, sel[t]]
+        if renormalize:
+            ps = ps / ps.sum()
+        M[t, sel[t]] = ps
+    Y = np.zeros((E, T, H), dtype=np.float64)
+    for e in range(E):
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[e])], H, I, G)
+        Y[e] = expert_ffn(wg, wu, wd, x)
+    out = np.einsum("te,eth->th", M, Y)
+    if has_shared:
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[E])], H, I, G)
+        out = out + expert_ffn(wg, wu, wd, x)
+    return out, sel
+
+
+def residual_add(x_fp16: np.ndarray, out_fp16: np.ndarray) -> np.ndarray:
+    """Residual stream update between stacked layers: fp16(x + moe(x)), with
+    the layer output taken at its FP16 value."""
+    return (np.asarray(x_fp16, dtype=np.float64) + np.asarray(out_fp16, dtype=np.float64)).astype(np.float16)
+
+
+def near_tie_tokens(L: np.ndarray, k: int, eps: float = 1e-3) -> np.ndarray:
+    """Tokens whose routing is not decided beyond eps: the gap between the
+    k-th and (k+1)-th largest logits, or between two adjacent selected
+    logits, is at most eps."""
+    s = -np.sort(-np.asarray(L, dtype=np.float64), axis=1)
+    E = s.shape[1]
+    upto = min(k + 1, E)
+    gaps = s[:, :upto - 1] - s[:, 1:upto]
+    return np.nonzero((gaps <= eps).any(axis=1))[0]

@@ -1,0 +1,218 @@
+"""Seeded synthetic inputs for the W4A16 routed-expert MoE layer.
+
+This module is the one piece shared by the CPU oracle's tests and the CUDA
+path: it draws activations, router weights and expert weights, quantises the
+expert weights to unsigned INT4 codes with FP16 group scales (an offline
+preparation step, not part of the layer's forward computation) and packs them
+into the canonical qpacked expert record. It performs none of the layer's own
+arithmetic (no router logits, softmax, selection, permutation, expert FFN or
+combine).
+
+Canonical expert record (one contiguous record per expert, so that one copy
+moves everything an expert needs — the "one read brings everything it needs"
+file layout of the moe-stream page, section "Method"):
+
+    gate_q | up_q | down_q | gate_s | up_s | down_s
+
+* ``gate_q``/``up_q``: INT4 codes of the [I][H] gate and up projections,
+  ``down_q``: codes of the [H][I] down projection. Row-major, K (the
+  reduction axis) contiguous, two codes per byte: the low nibble holds the even
+  k, the high nibble the odd k. Row stride K/2 bytes.
+* ``*_s``: FP16 scales, [N][ceil(K/G)] row-major, one per G consecutive codes
+  along K; the last group of a row covers the remaining K mod G codes.
+* The dequantised weight is ``(q - 8) * s`` (unsigned 4-bit, zero point 8).
+* Each section starts on a 256-byte boundary; the record size is rounded up to
+  a multiple of 256 bytes.
+
+Horizon RunMap report, "Architecture invariants" and "What is implemented":
+routed experts are kept compact as INT4 qpacked data with FP16 scales and run
+with FP16 activations; the pages do not print a byte layout, so the layout
+above is this library's own definition.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+SECTION_ALIGN = 256
+
+
+def _round_up(v: int, a: int) -> int:
+    return (v + a - 1) // a * a
+
+
+@dataclasses.dataclass(frozen=True)
+class LayerShape:
+    hidden: int
+    intermediate: int
+    num_experts: int
+    top_k: int
+    group_size: int
+    renormalize: bool
+    has_shared: bool = False
+    router_std: float = 0.02
+    expert_std: float = 0.02
+    zipf_s: float = 0.0  # >0: add -zipf_s*ln(e+1) to expert e's logit
+
+    @property
+    def n_records(self) -> int:
+        return self.num_experts + (1 if self.has_shared else 0)
+
+
+# Workloads named by what they are (shapes from the pages plus the stated
+# synthetic recipe).
+TINY = LayerShape(256, 128, 8, 2, 64, True, router_std=0.05)
+OLMOE = LayerShape(2048, 1024, 64, 8, 128, False)
+MANY_EXPERTS = LayerShape(2048, 512, 512, 10, 128, True, has_shared=True, zipf_s=1.1)
+GPTOSS_LIKE = LayerShape(2880, 2880, 128, 4, 128, True)
+
+
+def section_layout(H: int, I: int, G: int) -> dict:
+    """Byte offset and size of each section of the canonical record."""
+    ng_h = -(-H // G)
+    ng_i = -(-I // G)
+    sizes = [
+        ("gate_q", I * H // 2),
+        ("up_q", I * H // 2),
+        ("down_q", H * I // 2),
+        ("gate_s", I * ng_h * 2),
+        ("up_s", I * ng_h * 2),
+        ("down_s", H * ng_i * 2),
+    ]
+    out = {}
+    off = 0
+    for name, size in sizes:
+        off = _round_up(off, SECTION_ALIGN)
+        out[name] = (off, size)
+        off += size
+    out["record_bytes"] = _round_up(off, SECTION_ALIGN)
+    out["payload_bytes"] = sum(s for _, s in sizes)
+    return out
+
+
+def record_bytes(H: int, I: int, G: int) -> int:
+    return section_layout(H, I, G)["record_bytes"]
+
+
+def quantize_int4(w: np.ndarray, G: int):
+    """Symmetric-range INT4 quantisation with zero point 8 (data preparation).
+
+    scale = fp16(max|w| / 7) per group of G along K (1.0 for an all-zero
+    group); code = clip(rint(w / scale) + 8, 0, 15).
+    """
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    ng = -(-K // G)
+    pad = ng * G - K
+    wp = np.pad(w, ((0, 0), (0, pad))) if pad else w
+    wg = wp.reshape(N, ng, G)
+    amax = np.abs(wg).max(axis=2)
+    s16 = (amax / np.float32(7.0)).astype(np.float16)
+    s16[amax == 0] = np.float16(1.0)
+    s32 = s16.astype(np.float32)
+    q = np.rint(wg / s32[:, :, None]) + 8.0
+    q = np.clip(q, 0, 15).astype(np.uint8).reshape(N, ng * G)[:, :K]
+    return np.ascontiguousarray(q), s16
+
+
+def pack_nibbles(q: np.ndarray) -> np.ndarray:
+    """[N][K] codes in 0..15 -> [N][K/2] bytes, low nibble = even k."""
+    q = np.asarray(q, dtype=np.uint8)
+    assert q.shape[1] % 2 == 0
+    return np.ascontiguousarray((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+
+
+def pack_record(H, I, G, gate_q, up_q, down_q, gate_s, up_s, down_s) -> np.ndarray:
+    lay = section_layout(H, I, G)
+    rec = np.zeros(lay["record_bytes"], dtype=np.uint8)
+    parts = {
+        "gate_q": pack_nibbles(gate_q),
+        "up_q": pack_nibbles(up_q),
+        "down_q": pack_nibbles(down_q),
+        "gate_s": np.ascontiguousarray(gate_s, dtype=np.float16).view(np.uint8),
+        "up_s": np.ascontiguousarray(up_s, dtype=np.float16).view(np.uint8),
+        "down_s": np.ascontiguousarray(down_s, dtype=np.float16).view(np.uint8),
+    }
+    for name, arr in parts.items():
+        off, size = lay[name]
+        flat = arr.reshape(-1)
+        assert flat.size == size, (name, flat.size, size)
+        rec[off:off + size] = flat
+    return rec
+
+
+def _expert_codes(shape: LayerShape, rng: np.random.Generator, codes: str):
+    H, I, G = shape.hidden, shape.intermediate, shape.group_size
+    mats = []
+    for (n, k) in ((I, H), (I, H), (H, I)):
+        if codes == "quantized":
+            w = rng.standard_normal((n, k), dtype=np.float32) * np.float32(shape.expert_std)
+            mats.append(quantize_int4(w, G))
+        elif codes == "uniform":
+            # every code 0..15 equally likely; scales spread over a range so
+            # that no single scale dominates (exercises q = 0 and q = 15).
+            q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
+            ng = -(-k // G)
+            s = (rng.uniform(0.5, 1.5, size=(n, ng)) * (shape.expert_std / 4.6)).astype(np.float16)
+            mats.append((q, s))
+        else:
+            raise ValueError(codes)
+    (gq, gs), (uq, us), (dq, ds) = mats
+    return gq, uq, dq, gs, us, ds
+
+
+@dataclasses.dataclass
+class Layer:
+    shape: LayerShape
+    router_w: np.ndarray            # fp32 [E][H]
+    router_bias: Optional[np.ndarray]  # fp32 [E] or None
+    records: np.ndarray             # uint8 [n_slots][record_bytes], in slot order
+    expert_to_slot: np.ndarray      # int32 [n_records]
+
+
+def make_layer(shape: LayerShape, seed: int, codes: str = "quantized",
+               shuffle_slots: bool = True, extra_slots: int = 0) -> Layer:
+    """Draw one layer. Expert e's draws come from its own child seed, so any
+    expert can be regenerated alone. Records are stored in slot order through
+    a random expert_to_slot permutation (identity if shuffle_slots is False);
+    ``extra_slots`` appends unused slots filled with 0xFF bytes."""
+    E = shape.num_experts
+    nrec = shape.n_records
+    children = np.random.SeedSequence(seed).spawn(3 + nrec)
+    rng_router = np.random.default_rng(children[1])
+    router_w = rng_router.standard_normal((E, shape.hidden), dtype=np.float32) * np.float32(shape.router_std)
+    bias = None
+    if shape.zipf_s > 0:
+        bias = (-shape.zipf_s * np.log(np.arange(1, E + 1, dtype=np.float64))).astype(np.float32)
+    n_slots = nrec + extra_slots
+    if shuffle_slots:
+        slot_of = np.random.default_rng(children[2]).permutation(n_slots)[:nrec].astype(np.int32)
+    else:
+        slot_of = np.arange(nrec, dtype=np.int32)
+    rb = record_bytes(shape.hidden, shape.intermediate, shape.group_size)
+    records = np.full((n_slots, rb), 0xFF, dtype=np.uint8)
+    for e in range(nrec):
+        rng = np.random.default_rng(children[3 + e])
+        parts = _expert_codes(shape, rng, codes)
+        records[slot_of[e]] = pack_record(shape.hidden, shape.intermediate, shape.group_size, *parts)
+    return Layer(shape, router_w, bias, records, slot_of)
+
+
+def make_tokens(H: int, T: int, seed: int, std: float = 1.0) -> np.ndarray:
+    """FP16 activations ~ N(0, std), [T][H]."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x70C5]))
+    return (rng.standard_normal((T, H), dtype=np.float32) * np.float32(std)).astype(np.float16)
+
+
+def make_noise(H: int, T: int, seed: int, step: int, std: float = 0.1) -> np.ndarray:
+    """Per-step residual-stream noise for the stacked-layer decode workload."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 1000 + step]))
+    return (rng.standard_normal((T, H), dtype=np.float32) * np.float32(std))
+
+
+def stack_layer_seed(seed: int, layer: int) -> int:
+    """Seed of layer ``layer`` in the stacked workload (distinct per layer)."""
+    return int(np.random.SeedSequence([seed, layer]).generate_state(1)[0])
