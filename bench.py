@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 routed-expert MoE layer on GB300.
+
+One step = one forward of the whole layer (routing, permutation, gate/up +
+SwiGLU, down, weighted combine) over one batch of synthetic tokens. Prints
+one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+
+Timing: W untimed warm-up steps, then exactly K steps replayed from a CUDA
+graph, bracketed by a barrier and device synchronisation, timed with CUDA
+events on the launching stream; the max over ranks is reported. Steps rotate
+over several independently allocated copies of the expert table (and
+distinct token batches) so that the bytes a step reads are not in L2 from an
+earlier step.
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU-baseline leg times the oracle single-threaded
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import threading  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from w4a16_routed_expert_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (decode b=1 and prefill) + HBM GB/s and TC util vs roofline"
+
+WORKLOADS = {
+    # name: (shape, tokens, seed, description)
+    "olmoe-decode-t1": (synth.OLMOE, 1, 1, "OLMoE-shaped layer, decode batch 1, all 64 experts resident"),
+    "olmoe-decode-t4": (synth.OLMOE, 4, 1, "OLMoE-shaped layer, decode batch 4"),
+    "olmoe-decode-t16": (synth.OLMOE, 16, 1, "OLMoE-shaped layer, decode batch 16"),
+    "many-experts-t1": (synth.MANY_EXPERTS, 1, 3, "512 routed + 1 shared expert, Zipf-biased router, batch 1"),
+    "many-experts-t16": (synth.MANY_EXPERTS, 16, 3, "512 routed + 1 shared expert, batch 16"),
+    "many-experts-t256": (synth.MANY_EXPERTS, 256, 3, "512 routed + 1 shared expert, batch 256"),
+    "olmoe-prefill-t8192": (synth.OLMOE, 8192, 1, "OLMoE-shaped layer, 8192-token prefill"),
+}
+DEFAULT_WORKLOAD = "olmoe-decode-t1"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=p["hbm_gbs"], bf16_tflops=p["bf16_tflops"],
+                    bf16_tflops_sustained=p.get("bf16_tflops_sustained"), source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (reported baseline and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample(lay, shape, T, seed, budget_s):
+    """Time the oracle, as it stands, on bounded samples of the workload:
+    whole forwards of the workload's batch size (decode), or of a leading
+    slice of the batch (large batches). Returns (tokens/s, description)."""
+    from oracle import moe_oracle as O
+    kw = dict(H=shape.hidden, I=shape.intermediate, E=shape.num_experts, k=shape.top_k, G=shape.group_size,
+              renormalize=shape.renormalize, has_shared=shape.has_shared)
+    batch = T if T <= 16 else 64
+    t0 = time.perf_counter()
+    tokens = 0
+    calls = 0
+    while True:
+        x = synth.make_tokens(shape.hidden, batch, seed=seed * 7919 + calls)
+        O.moe_forward(x, lay.router_w, lay.router_bias, lay.records, lay.expert_to_slot, **kw)
+        tokens += batch
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or calls >= 200:
+            break
+    desc = (f"{calls} oracle forwards of {batch} token(s)"
+            + ("" if batch == T else f" (a {batch}-token slice of the {T}-token batch)")
+            + f", {el:.1f} s")
+    return tokens / el, desc, el
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled while the GPU is under load
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.samples = []
+        self.proc = None
+        self.index = index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for p in inside for n, v in zip(names, p[3:]) if v.strip().lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def algorithmic(shape, T, eu):
+    """Bytes the method must move and FLOPs it must do for one forward with
+    eu distinct routed experts selected."""
+    H, I, E, k, G = shape.hidden, shape.intermediate, shape.num_experts, shape.top_k, shape.group_size
+    sh = 1 if shape.has_shared else 0
+    ngh, ngi = -(-H // G), -(-I // G)
+    gate_up = 2 * I * H // 2 + 2 * I * ngh * 2
+    down = H * I // 2 + H * ngi * 2
+    n_exp = eu + sh
+    pairs = T * k + T * sh
+    b = dict(
+        gate_up=n_exp * gate_up + T * H * 2 + pairs * I * 2,
+        down=n_exp * down + pairs * I * 2 + pairs * H * 4,
+        layer=n_exp * (gate_up + down) + E * H * 4 + 2 * T * H * 2,
+    )
+    f = dict(layer=2 * T * H * E + pairs * 6 * H * I)
+    return b, f, dict(gate_up_per_expert=gate_up, down_per_expert=down)
+
+
+def source_hash(*files):
+    h = hashlib.sha256()
+    for fn in files:
+        with open(os.path.join(ROOT, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def run_ours(args):
+    import torch
+
+    from w4a16_routed_expert_gb300 import build as B
+    from w4a16_routed_expert_gb300 import capi
+    from w4a16_routed_expert_gb300.layer import MoELayer
+
+    world, rank, local = _dist()
+    shape, T, seed, desc = WORKLOADS[args.workload]
+    lay = synth.make_layer(shape, seed=seed)
+
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sdesc, el = oracle_sample(lay, shape, T, seed, args.cpu_seconds)
+        cpu_base = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sdesc}
+
+    if not os.path.exists(capi.LIB_PATH):
+        B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2**20
+    rec = lay.records.shape[1]
+    max_eu = min(shape.num_experts, T * shape.top_k) + (1 if shape.has_shared else 0)
+    touched = max_eu * rec
+    R = int(min(16, max(2, math.ceil(2 * l2 / touched) + 1)))
+
+    pools, routers, biases, e2ss, layers, xs, outs = [], [], [], [], [], [], []
+    for r in range(R):
+        pools.append(torch.from_numpy(lay.records).to(dev))
+        routers.append(torch.from_numpy(lay.router_w).to(dev))
+        biases.append(torch.from_numpy(lay.router_bias).to(dev) if lay.router_bias is not None else None)
+        e2ss.append(torch.from_numpy(lay.expert_to_slot.astype(np.int32)).to(dev))
+        layers.append(MoELayer(hidden=shape.hidden, intermediate=shape.intermediate, num_experts=shape.num_experts,
+                               top_k=shape.top_k, group_size=shape.group_size, renormalize=shape.renormalize,
+                               has_shared=shape.has_shared, max_tokens=T, router_w=routers[r],
+                               router_bias=biases[r], pool=pools[r], expert_to_slot=e2ss[r]))
+        xs.append(torch.from_numpy(synth.make_tokens(shape.hidden, T, seed=1000 * (rank + 1) + r)).to(dev))
+        outs.append(torch.empty_like(xs[-1]))
+
+    K, W = args.steps, args.warmup
+    launches_per_forward = (1 if T <= 16 else 3) + 3
+    for i in range(max(W, R)):
+        layers[i % R].forward(xs[i % R], out=outs[i % R])
+    for l in layers:
+        l.sync()
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cs):
+            for r in range(n):
+                layers[r].forward(xs[r], out=outs[r])
+        torch.cuda.synchronize()
+        return g
+
+    g_full = capture(R)
+    g_rem = capture(K % R) if K % R else None
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    start.record()
+    for _ in range(K // R):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
+    barrier()
+    el_ms = start.elapsed_time(end)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([el_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el_ms = float(t.item())
+    # keep the GPU loaded long enough for the clock sampler to see it
+    soak_t0 = time.perf_counter()
+    while time.perf_counter() - soak_t0 < max(0.0, 1.5 - (t_wall1 - t_wall0)):
+        for _ in range(20):
+            g_full.replay()
+        torch.cuda.synchronize()
+    soak_t1 = time.perf_counter()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, max(t_wall1, soak_t1))
+    clocks["window"] = "timed region" if soak_t1 - soak_t0 < 0.01 else "timed region + untimed replay of the same graph"
+
+    ms_per_step = el_ms / K
+    value = T * world / (ms_per_step / 1e3)
+
+    # per-stage CUDA events (profiling graph of the same R forwards)
+    for l in layers:
+        l.set_profiling(True)
+    g_prof = capture(R)
+    stage = np.zeros(5)
+    eu_sum = 0
+    nprof = 0
+    for _ in range(max(1, min(K // R, 25))):
+        g_prof.replay()
+        torch.cuda.synchronize()
+        for l in layers:
+            p = l.profile()
+            stage += [p.route_ms, p.gate_up_ms, p.down_ms, p.combine_ms, p.total_ms]
+            eu_sum += p.active_experts
+            nprof += 1
+    for l in layers:
+        l.set_profiling(False)
+    stage /= nprof
+    eu = eu_sum / nprof
+    peaks = _peaks()
+    b, f, per = algorithmic(shape, T, eu)
+    kern = "gate_up" if stage[1] >= stage[2] else "down"
+    kern_ms = stage[1] if kern == "gate_up" else stage[2]
+    achieved = b[kern] / (kern_ms / 1e3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as ftr:
+            tr = json.load(ftr)
+        ent = tr.get(args.workload, {}).get(kern)
+        if ent and ent.get("source_sha") == source_hash("w4a16_routed_expert_gb300/csrc/gemv.cu"):
+            traffic = ent["dram_bytes_per_launch"]
+    except Exception:
+        traffic = None
+    roofline = {"bound": "hbm", "kernel": f"k_gemv ({kern.replace('_', '/')})", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": peaks["source"], "traffic": traffic,
+                "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms,
+                "active_experts": eu}
+    layer_bytes_gbs = b["layer"] / (ms_per_step / 1e3) / 1e9
+    layer_tflops = f["layer"] / (ms_per_step / 1e3) / 1e12
+    layer_roof = {"bytes_per_step": b["layer"], "flops_per_step": f["layer"], "achieved_gbs": layer_bytes_gbs,
+                  "hbm_frac": layer_bytes_gbs / peaks["hbm_gbs"], "achieved_tflops": layer_tflops,
+                  "tensor_frac": layer_tflops / peaks["bf16_tflops"],
+                  "roofline_ms": max(b["layer"] / (peaks["hbm_gbs"] * 1e9), f["layer"] / (peaks["bf16_tflops"] * 1e12)) * 1e3}
+    layer_roof["frac_of_roofline"] = layer_roof["roofline_ms"] / ms_per_step
+
+    # end to end through the C ABI with host buffers (pinned), copies inside
+    xh = [x.cpu().pin_memory() for x in xs]
+    oh = [torch.empty_like(x) .pin_memory() for x in xh]
+    ih = [torch.empty((T, shape.top_k), dtype=torch.int32).pin_memory() for _ in xs]
+    wh = [torch.empty((T, shape.top_k), dtype=torch.float32).pin_memory() for _ in xs]
+    for i in range(R):
+        layers[i].forward_host(xh[i], oh[i], ih[i], wh[i])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(K):
+        layers[i % R].forward_host(xh[i % R], oh[i % R], ih[i % R], wh[i % R])
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": T * K * world / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": T * shape.hidden * 2,
+           "d2h_bytes_per_step": T * shape.hidden * 2 + T * shape.top_k * 8,
+           "path": "moe_layer_forward_host (pinned host x -> device, forward, out/ids/weights -> host)"}
+
+    for l in layers:
+        l.close()
+    if rank != 0:
+        return None
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded; INT4 codes quantised from N(0,0.02) weights)",
+        "config": {"workload": args.workload, "description": desc, "hidden": shape.hidden,
+                   "intermediate": shape.intermediate, "experts": shape.num_experts, "top_k": shape.top_k,
+                   "shared_expert": shape.has_shared, "group_size": shape.group_size,
+                   "renormalize": shape.renormalize, "tokens_per_step": T, "global_batch": T * world,
+                   "arithmetic": "INT4 codes (zero point 8) x FP16 scales x FP16 activations, FP32 accumulation",
+                   "l2": f"inputs larger than L2: steps rotate over {R} device copies of the "
+                         f"{lay.records.nbytes / 1e6:.1f} MB expert table and {R} token batches",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline, "layer_roofline": layer_roof,
+        "stage_ms": {"route": stage[0], "gate_up": stage[1], "down": stage[2], "combine": stage[3],
+                     "total": stage[4]},
+        "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": K * launches_per_forward,
+    }
+
+
+def run_reference(args):
+    world, rank, local = _dist()
+    if rank != 0:
+        return None
+    shape, T, seed, desc = WORKLOADS[args.workload]
+    lay = synth.make_layer(shape, seed=seed)
+    # warm-up steps, then K timed steps, each a bounded sample of the workload
+    budget = max(0.5, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(lay, shape, T, seed, 0.0)
+    tot_tokens, tot_s, descs = 0.0, 0.0, []
+    for i in range(args.steps):
+        v, d, el = oracle_sample(lay, shape, T, seed + 17 * i, budget)
+        tot_tokens += v * el
+        tot_s += el
+        descs.append(d)
+    value = tot_tokens / tot_s
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "description": desc, "tokens_per_step": T},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "sample": descs[0], "value": value, "unit": "tokens/s"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * moe_layer.h — C ABI of the GB300 (sm_103a) W4A16 routed-expert MoE layer.
+ *
+ * The layer (Horizon RunMap report, "The complete execution path", steps 1-3;
+ * "Architecture invariants"): routed experts are stored compact as INT4
+ * qpacked codes with FP16 group scales and executed with FP16 activations
+ * (W4A16). For T tokens x[T][H] the layer computes
+ *
+ *   logits  L[t][e] = sum_h x[t][h] * Wr[e][h] (+ bias[e])        FP32
+ *   p[t]    = softmax over all E experts of L[t]                  FP32
+ *   ids[t]  = the top_k experts of L[t], ties to the lower id,
+ *             in rank order (descending logit, then ascending id)
+ *   w[t][j] = p[t][ids[t][j]]  (divided by sum_j p[t][ids[t][j]] when
+ *             renormalising)
+ *   y_e(x)  = Wd_e (silu(Wg_e x) * (Wu_e x)),  silu(z) = z / (1 + e^-z),
+ *             W = (q - 8) * s dequantised from expert e's record
+ *   out[t]  = sum_j w[t][j] * y_{ids[t][j]}(x[t])  (+ y_shared(x[t]))
+ *
+ * with an optional always-on shared expert (F51 Nitro-MoE, "The thesis": the
+ * documented model routes each token to ten experts and also runs one shared
+ * expert) applied to every token with weight 1.
+ *
+ * Expert records (canonical format, one contiguous record per expert so a
+ * single copy moves everything an expert needs — moe-stream, "Method"):
+ *   gate_q | up_q | down_q | gate_s | up_s | down_s
+ * codes row-major with K contiguous, two codes per byte (low nibble = even k),
+ * gate/up [I][H], down [H][I]; FP16 scales [N][ceil(K/G)], one per G codes
+ * along K; w = (q - 8) * s. Each section starts on a 256-byte boundary and
+ * the record size is a multiple of 256 bytes (moe_record_bytes).
+ *
+ * Records are addressed through expert_to_slot (F51 Nitro-MoE, "Layer 1 -
+ * expert persistence cache": an expert_to_slot map over a fixed pool of GPU
+ * slots), so a fully resident table and a partially resident slot pool run
+ * the same kernels.
+ *
+ * Conventions
+ *  - Every call returns a moe_status_t; nothing aborts and no C++ exception
+ *    crosses the ABI. moe_layer_last_error() describes the last failure of
+ *    the calling thread.
+ *  - Device pointers passed in are borrowed: the caller owns them and they
+ *    must stay valid until moe_layer_destroy.
+ *  - moe_layer_forward is asynchronous on the given CUDA stream (NULL = the
+ *    legacy default stream). Its outputs, including ids and weights, are
+ *    valid only once that stream has been synchronised.
+ *  - One forward at a time per handle: two forwards of one handle that
+ *    overlap on the GPU share its workspace and race.
+ *  - Kernels never trap. A device-side wait that runs out of time (a
+ *    bounded spin of about two seconds) records an error word in the
+ *    workspace; moe_layer_sync reports it as MOE_ERR_TIMEOUT.
+ *  - The library never writes host_backing and never copies an expert
+ *    record from the device to the host.
+ */
+#ifndef MOE_LAYER_H
+#define MOE_LAYER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* a NULL handle/pointer, a size out of range, T > max_tokens */
+  MOE_ERR_OOM = 2,         /* a device or pinned allocation failed in create */
+  MOE_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the CUDA error) */
+  MOE_ERR_UNSUPPORTED = 4, /* a shape or mode this build does not run (e.g. H % 32 != 0) */
+  MOE_ERR_CAPACITY = 5,    /* partial residency: not enough slots for one expert group */
+  MOE_ERR_TIMEOUT = 6,     /* a device-side bounded wait gave up (reported by moe_layer_sync) */
+  MOE_ERR_INTERNAL = 7     /* an internal consistency check failed */
+} moe_status_t;
+
+typedef enum {
+  MOE_RESIDENCY_FULL = 0,   /* every record resident in a caller-owned device pool */
+  MOE_RESIDENCY_PARTIAL = 1 /* library-owned pool of num_slots records filled from pinned host backing */
+} moe_residency_t;
+
+typedef struct {
+  int32_t hidden;            /* H, multiple of 32 */
+  int32_t intermediate;      /* I, multiple of 32 */
+  int32_t num_experts;       /* E routed experts, 1..1024 */
+  int32_t top_k;             /* k, 1..min(E, 32) */
+  int32_t group_size;        /* G, 64 or 128 (codes per FP16 scale along K) */
+  int32_t renormalize;       /* 0: w = softmax over all E; 1: w renormalised over the top k */
+  int32_t has_shared_expert; /* 1: record index E is a shared expert run on every token, weight 1 */
+  int32_t max_tokens;        /* upper bound of T; workspace is sized for it at create */
+  int32_t num_slots;         /* FULL: records in slot_pool; PARTIAL: slots of the library's pool */
+  int32_t residency;         /* moe_residency_t */
+  int32_t add_residual;      /* 1: out = fp16(x + fp16(layer(x))) (residual stream of stacked layers) */
+} moe_layer_config_t;
+
+typedef struct {
+  const float* router_w;         /* device, FP32 [E][H] row-major */
+  const float* router_bias;      /* device, FP32 [E] added to the logits, or NULL */
+  const void* slot_pool;         /* FULL: device, num_slots * moe_record_bytes bytes, 256-byte aligned.
+                                    PARTIAL: must be NULL (the library allocates the pool). */
+  const int32_t* expert_to_slot; /* FULL: device int32 [E (+1 if shared)], values in [0, num_slots).
+                                    PARTIAL: must be NULL (the library owns the map). */
+  const void* host_backing;      /* PARTIAL: host memory, [E (+1)] records back to back, registered
+                                    (pinned) by the library for the handle's lifetime and never
+                                    written. FULL: must be NULL. */
+} moe_layer_weights_t;
+
+typedef struct moe_layer moe_layer_t;
+
+typedef struct {
+  uint64_t forward_calls;    /* forwards run (T > 0) */
+  uint64_t tokens;           /* tokens processed */
+  uint64_t expert_hits;      /* PARTIAL: demanded experts found resident */
+  uint64_t expert_misses;    /* PARTIAL: demanded experts copied host -> device */
+  uint64_t h2d_bytes;        /* PARTIAL: expert bytes copied host -> device */
+  uint64_t d2h_expert_bytes; /* expert bytes copied device -> host: 0 by construction */
+  uint64_t waves;            /* PARTIAL: expert-compute waves (one per pool refill) */
+} moe_layer_stats_t;
+
+typedef struct {
+  float route_ms;         /* routing kernels (logits, top-k, permutation) */
+  float gate_up_ms;       /* gate/up + SwiGLU expert kernel */
+  float down_ms;          /* down-projection expert kernel */
+  float combine_ms;       /* weighted combine */
+  float total_ms;         /* whole forward */
+  int32_t active_experts; /* distinct routed experts selected (E_u) */
+  int32_t tokens;         /* T of the profiled forward */
+} moe_layer_profile_t;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION of its build). */
+int32_t moe_abi_version(void);
+
+/* Padded size in bytes of one canonical expert record; 0 for an invalid shape. */
+size_t moe_record_bytes(int32_t hidden, int32_t intermediate, int32_t group_size);
+
+/* Byte offset and size of section `section` (0 gate_q, 1 up_q, 2 down_q,
+ * 3 gate_s, 4 up_s, 5 down_s) inside one record. */
+moe_status_t moe_record_section(int32_t hidden, int32_t intermediate, int32_t group_size,
+                                int32_t section, size_t* offset, size_t* bytes);
+
+/* Validates the configuration, records the borrowed pointers and allocates
+ * the workspace for max_tokens tokens on the current CUDA device. Fails with
+ * INVALID_ARG / UNSUPPORTED / OOM / CAPACITY; *out is NULL on failure. No
+ * allocation happens in moe_layer_forward afterwards. */
+moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_weights_t* weights,
+                              moe_layer_t** out);
+
+/* One forward of T tokens on `stream` (a cudaStream_t, NULL = default).
+ *   x        device FP16 [T][H], read only
+ *   out      device FP16 [T][H]; must not overlap x
+ *   topk_ids device int32 [T][k] or NULL; rank order
+ *   topk_w   device FP32 [T][k] or NULL
+ * T = 0 returns MOE_OK without launching. T > max_tokens -> INVALID_ARG.
+ * FULL residency: enqueues kernels only, no synchronisation and no
+ * allocation. PARTIAL residency: synchronises the stream once to read the
+ * demanded expert set, copies missing records into the pool on a side
+ * stream and runs the experts in waves (not capturable in a CUDA graph). */
+moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, void* out,
+                               int32_t* topk_ids, float* topk_w, void* stream);
+
+/* Same computation for callers whose tokens live in host memory: copies x
+ * (host FP16 [T][H]) to a device staging buffer, runs the forward and copies
+ * out / ids / weights back into host buffers (ids, weights may be NULL).
+ * Asynchronous on `stream`; page-locked host buffers make the copies
+ * overlap-capable. Synchronise the stream before reading the results. */
+moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* x_host, int32_t T, void* out_host,
+                                    int32_t* topk_ids_host, float* topk_w_host, void* stream);
+
+/* Copies the routing of the last forward on this handle into device buffers
+ * (any may be NULL): counts int32 [E], offsets int32 [E+1] (exclusive prefix
+ * sum of counts), perm int32 [T*k] (flat index t*k+j at each sorted position,
+ * ascending flat index inside an expert), inv_perm int32 [T*k]. Asynchronous
+ * on `stream`. */
+moe_status_t moe_layer_routing(const moe_layer_t* layer, int32_t* counts, int32_t* offsets, int32_t* perm,
+                               int32_t* inv_perm, void* stream);
+
+/* Synchronises `stream` and reports (then clears) a device-side error word:
+ * MOE_ERR_TIMEOUT if a bounded wait gave up, MOE_ERR_CUDA on a CUDA error. */
+moe_status_t moe_layer_sync(moe_layer_t* layer, void* stream);
+
+/* Tracing: when enabled, each forward records CUDA events between its
+ * stages on the forward's stream (also inside a captured CUDA graph).
+ * moe_layer_get_profile waits for the last forward's events and reports the
+ * stage times and the number of distinct experts it selected. */
+moe_status_t moe_layer_set_profiling(moe_layer_t* layer, int32_t enable);
+moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* profile);
+
+/* Copies the handle's counters into *stats. */
+moe_status_t moe_layer_get_stats(const moe_layer_t* layer, moe_layer_stats_t* stats);
+
+/* Frees the workspace (and, in PARTIAL mode, the pool and the host
+ * registration). NULL is accepted and returns MOE_OK. Call after the last
+ * forward has completed. */
+moe_status_t moe_layer_destroy(moe_layer_t* layer);
+
+/* Message of the calling thread's last failed call ("" if none). The pointer
+ * stays valid until the thread's next call into the library. */
+const char* moe_layer_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYER_H */

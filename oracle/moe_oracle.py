@@ -220,6 +220,20 @@ def moe_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k
     counts, offsets, perm, inv_perm = counting_sort(ids, E)
     if tokens is None:
         tokens = np.arange(T)
+    out = expert_combine(x, ids, w, records, expert_to_slot, H=H, I=I, E=E, k=k, G=G,
+                         has_shared=has_shared, tokens=tokens)
+    return dict(out=out, logits=L, probs=p, ids=ids, weights=w, counts=counts,
+                offsets=offsets, perm=perm, inv_perm=inv_perm)
+
+
+def expert_combine(x, ids, w, records, expert_to_slot, *, H, I, E, k, G, has_shared=False, tokens=None):
+    """out[t] = sum_j w[t, j] * y_{ids[t, j]}(x[t]) (+ y_shared(x[t])) for the
+    requested tokens, given the routing (ids, w) of the whole batch."""
+    x = np.asarray(x)
+    ids = np.asarray(ids)
+    w = np.asarray(w, dtype=np.float64)
+    if tokens is None:
+        tokens = np.arange(x.shape[0])
     tokens = np.asarray(tokens, dtype=np.int64)
     out = np.zeros((tokens.size, H), dtype=np.float64)
     used = sorted(set(int(e) for e in ids[tokens].reshape(-1)))
@@ -234,8 +248,7 @@ def moe_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k
     if has_shared:
         wg, wu, wd = expert_matrices(records[int(expert_to_slot[E])], H, I, G)
         out += expert_ffn(wg, wu, wd, x[tokens])
-    return dict(out=out, logits=L, probs=p, ids=ids, weights=w, counts=counts,
-                offsets=offsets, perm=perm, inv_perm=inv_perm)
+    return out
 
 
 def dense_masked_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k, G,

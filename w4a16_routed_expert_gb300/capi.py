@@ -1,0 +1,158 @@
+"""ctypes binding of include/moe_layer.h — argument marshalling only.
+
+Every entry point has the same name as in the header. The library is loaded
+on first use; if it has not been built this raises instead of falling back
+to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_w4a16.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_OOM = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_UNSUPPORTED = 4
+MOE_ERR_CAPACITY = 5
+MOE_ERR_TIMEOUT = 6
+MOE_ERR_INTERNAL = 7
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_OOM", 3: "MOE_ERR_CUDA",
+                4: "MOE_ERR_UNSUPPORTED", 5: "MOE_ERR_CAPACITY", 6: "MOE_ERR_TIMEOUT",
+                7: "MOE_ERR_INTERNAL"}
+
+MOE_RESIDENCY_FULL = 0
+MOE_RESIDENCY_PARTIAL = 1
+
+
+class moe_layer_config_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "hidden", "intermediate", "num_experts", "top_k", "group_size", "renormalize",
+        "has_shared_expert", "max_tokens", "num_slots", "residency", "add_residual")]
+
+
+class moe_layer_weights_t(ctypes.Structure):
+    _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("slot_pool", ctypes.c_void_p), ("expert_to_slot", ctypes.c_void_p),
+                ("host_backing", ctypes.c_void_p)]
+
+
+class moe_layer_stats_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "forward_calls", "tokens", "expert_hits", "expert_misses", "h2d_bytes",
+        "d2h_expert_bytes", "waves")]
+
+
+class moe_layer_profile_t(ctypes.Structure):
+    _fields_ = [("route_ms", ctypes.c_float), ("gate_up_ms", ctypes.c_float), ("down_ms", ctypes.c_float),
+                ("combine_ms", ctypes.c_float), ("total_ms", ctypes.c_float),
+                ("active_experts", ctypes.c_int32), ("tokens", ctypes.c_int32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {message}")
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+
+# name -> (restype, argtypes)
+PROTOTYPES = {
+    "moe_abi_version": (_I32, []),
+    "moe_record_bytes": (ctypes.c_size_t, [_I32, _I32, _I32]),
+    "moe_record_section": (_I32, [_I32, _I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t),
+                                  ctypes.POINTER(ctypes.c_size_t)]),
+    "moe_layer_create": (_I32, [ctypes.POINTER(moe_layer_config_t), ctypes.POINTER(moe_layer_weights_t),
+                                ctypes.POINTER(_P)]),
+    "moe_layer_forward": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
+    "moe_layer_forward_host": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
+    "moe_layer_routing": (_I32, [_P, _P, _P, _P, _P, _P]),
+    "moe_layer_sync": (_I32, [_P, _P]),
+    "moe_layer_get_stats": (_I32, [_P, ctypes.POINTER(moe_layer_stats_t)]),
+    "moe_layer_set_profiling": (_I32, [_P, _I32]),
+    "moe_layer_get_profile": (_I32, [_P, ctypes.POINTER(moe_layer_profile_t)]),
+    "moe_layer_destroy": (_I32, [_P]),
+    "moe_layer_last_error": (ctypes.c_char_p, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run w4a16_routed_expert_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in PROTOTYPES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def last_error() -> str:
+    return lib().moe_layer_last_error().decode()
+
+
+def check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoEError(status, where, last_error())
+
+
+def record_bytes(hidden: int, intermediate: int, group_size: int) -> int:
+    return int(lib().moe_record_bytes(hidden, intermediate, group_size))
+
+
+def record_section(hidden: int, intermediate: int, group_size: int, section: int):
+    off, size = ctypes.c_size_t(), ctypes.c_size_t()
+    check(lib().moe_record_section(hidden, intermediate, group_size, section, ctypes.byref(off),
+                                   ctypes.byref(size)), "moe_record_section")
+    return off.value, size.value
+
+
+def moe_layer_create(config: moe_layer_config_t, weights: moe_layer_weights_t) -> int:
+    h = _P()
+    check(lib().moe_layer_create(ctypes.byref(config), ctypes.byref(weights), ctypes.byref(h)),
+          "moe_layer_create")
+    return h.value
+
+
+def moe_layer_forward(h, x, T, out, ids, w, stream) -> int:
+    return lib().moe_layer_forward(h, x, T, out, ids, w, stream)
+
+
+def moe_layer_forward_host(h, x, T, out, ids, w, stream) -> int:
+    return lib().moe_layer_forward_host(h, x, T, out, ids, w, stream)
+
+
+def moe_layer_routing(h, counts, offsets, perm, inv_perm, stream) -> int:
+    return lib().moe_layer_routing(h, counts, offsets, perm, inv_perm, stream)
+
+
+def moe_layer_sync(h, stream) -> int:
+    return lib().moe_layer_sync(h, stream)
+
+
+def moe_layer_get_stats(h) -> moe_layer_stats_t:
+    st = moe_layer_stats_t()
+    check(lib().moe_layer_get_stats(h, ctypes.byref(st)), "moe_layer_get_stats")
+    return st
+
+
+def moe_layer_set_profiling(h, enable: bool) -> None:
+    check(lib().moe_layer_set_profiling(h, int(bool(enable))), "moe_layer_set_profiling")
+
+
+def moe_layer_get_profile(h) -> moe_layer_profile_t:
+    p = moe_layer_profile_t()
+    check(lib().moe_layer_get_profile(h, ctypes.byref(p)), "moe_layer_get_profile")
+    return p
+
+
+def moe_layer_destroy(h) -> int:
+    return lib().moe_layer_destroy(h)

@@ -1,0 +1,571 @@
+// Runtime behind the C ABI declared in include/moe_layer.h: validates the
+// configuration, owns the workspace, and enqueues the layer's kernels on the
+// caller's stream (routing -> gate/up+SwiGLU -> down -> weighted combine).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <string>
+#include <unordered_map>
+
+#include "kernels.h"
+#include "moe_layer.h"
+#include "residency.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status_t fail(moe_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+moe_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t off[6];
+  size_t size[6];
+  size_t record;
+  size_t payload;
+};
+
+bool record_layout(int H, int I, int G, Layout* L) {
+  if (H <= 0 || I <= 0 || G <= 0 || (H % 2) || (I % 2)) return false;
+  const size_t gh = (size_t)(H + G - 1) / G, gi = (size_t)(I + G - 1) / G;
+  const size_t sizes[6] = {(size_t)I * H / 2, (size_t)I * H / 2, (size_t)H * I / 2,
+                           2 * (size_t)I * gh,  2 * (size_t)I * gh,  2 * (size_t)H * gi};
+  size_t cur = 0, payload = 0;
+  for (int i = 0; i < 6; ++i) {
+    cur = align256(cur);
+    L->off[i] = cur;
+    L->size[i] = sizes[i];
+    cur += sizes[i];
+    payload += sizes[i];
+  }
+  L->record = align256(cur);
+  L->payload = payload;
+  return true;
+}
+
+}  // namespace
+
+struct moe_layer {
+  moe_layer_config_t cfg;
+  moe_layer_weights_t w;
+  int device = 0;
+  int num_sms = 0;
+  Layout lay;
+  int n_records = 0;
+  bool pdl = true;
+  // workspace (one allocation)
+  void* ws = nullptr;
+  float* logits = nullptr;
+  int32_t* ids = nullptr;
+  float* wts = nullptr;
+  int32_t* chunk_hist = nullptr;
+  int32_t* chunk_base = nullptr;
+  int32_t* counts = nullptr;
+  int32_t* offsets = nullptr;
+  int32_t* perm = nullptr;
+  int32_t* inv_perm = nullptr;
+  int32_t* seg_expert = nullptr;
+  int32_t* seg_start = nullptr;
+  int32_t* seg_count = nullptr;
+  int32_t* num_seg = nullptr;
+  uint32_t* ticket = nullptr;
+  uint32_t* err = nullptr;
+  __half* hbuf = nullptr;
+  float* ypart = nullptr;
+  __half* x_stage = nullptr;
+  __half* out_stage = nullptr;
+  int32_t* ids_stage = nullptr;
+  float* w_stage = nullptr;
+  int last_T = 0;
+  bool profiling = false;
+  cudaEvent_t ev[5] = {};
+  moe::Residency* res = nullptr;  // partial residency state
+  moe_layer_stats_t stats = {};
+};
+
+namespace {
+
+moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w) {
+  if (!c || !w) return fail(MOE_ERR_INVALID_ARG, "config and weights must not be NULL");
+  if (c->hidden < 128 || c->hidden > 4096 || c->hidden % 32)
+    return fail(MOE_ERR_UNSUPPORTED, "hidden=%d: supported 128..4096, multiple of 32", c->hidden);
+  if (c->intermediate < 128 || c->intermediate > 4096 || c->intermediate % 32)
+    return fail(MOE_ERR_UNSUPPORTED, "intermediate=%d: supported 128..4096, multiple of 32", c->intermediate);
+  if (c->group_size != 64 && c->group_size != 128)
+    return fail(MOE_ERR_UNSUPPORTED, "group_size=%d: supported 64 or 128", c->group_size);
+  if (c->num_experts < 1 || c->num_experts > 1024)
+    return fail(MOE_ERR_INVALID_ARG, "num_experts=%d out of 1..1024", c->num_experts);
+  if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->num_experts)
+    return fail(MOE_ERR_INVALID_ARG, "top_k=%d out of 1..min(32, E)", c->top_k);
+  if (c->max_tokens < 1 || c->max_tokens > (1 << 20))
+    return fail(MOE_ERR_INVALID_ARG, "max_tokens=%d out of 1..2^20", c->max_tokens);
+  if ((long long)c->max_tokens * (c->top_k + 1) > (1LL << 30))
+    return fail(MOE_ERR_INVALID_ARG, "max_tokens * (top_k + 1) too large");
+  if (c->renormalize != 0 && c->renormalize != 1) return fail(MOE_ERR_INVALID_ARG, "renormalize must be 0 or 1");
+  if (c->has_shared_expert != 0 && c->has_shared_expert != 1)
+    return fail(MOE_ERR_INVALID_ARG, "has_shared_expert must be 0 or 1");
+  if (c->add_residual != 0 && c->add_residual != 1) return fail(MOE_ERR_INVALID_ARG, "add_residual must be 0 or 1");
+  if (!w->router_w) return fail(MOE_ERR_INVALID_ARG, "router_w must not be NULL");
+  const int n_records = c->num_experts + c->has_shared_expert;
+  if (c->residency == MOE_RESIDENCY_FULL) {
+    if (!w->slot_pool || !w->expert_to_slot)
+      return fail(MOE_ERR_INVALID_ARG, "full residency needs slot_pool and expert_to_slot");
+    if (w->host_backing) return fail(MOE_ERR_INVALID_ARG, "full residency takes no host_backing");
+    if (c->num_slots < 1) return fail(MOE_ERR_INVALID_ARG, "num_slots=%d", c->num_slots);
+    if (reinterpret_cast<uintptr_t>(w->slot_pool) % 256)
+      return fail(MOE_ERR_INVALID_ARG, "slot_pool must be 256-byte aligned");
+  } else if (c->residency == MOE_RESIDENCY_PARTIAL) {
+    if (w->slot_pool || w->expert_to_slot)
+      return fail(MOE_ERR_INVALID_ARG, "partial residency owns its pool: slot_pool/expert_to_slot must be NULL");
+    if (!w->host_backing) return fail(MOE_ERR_INVALID_ARG, "partial residency needs host_backing");
+    if (c->num_slots < 1 || c->num_slots > n_records)
+      return fail(MOE_ERR_INVALID_ARG, "num_slots=%d out of 1..%d", c->num_slots, n_records);
+    if (c->num_slots < c->top_k + c->has_shared_expert)
+      return fail(MOE_ERR_CAPACITY, "num_slots=%d cannot hold one token's %d experts", c->num_slots,
+                  c->top_k + c->has_shared_expert);
+  } else {
+    return fail(MOE_ERR_INVALID_ARG, "residency=%d unknown", c->residency);
+  }
+  return MOE_OK;
+}
+
+template <typename T>
+T* carve(char*& p, size_t count) {
+  T* r = reinterpret_cast<T*>(p);
+  p += align256(count * sizeof(T));
+  return r;
+}
+
+size_t workspace_bytes(const moe_layer_config_t& c) {
+  const size_t T = c.max_tokens, k = c.top_k, E = c.num_experts, H = c.hidden, I = c.intermediate;
+  const size_t nchunks = (T + moe::kRouteChunkTokens - 1) / moe::kRouteChunkTokens;
+  const size_t P = T * k + T;  // sorted positions incl. the shared segment
+  size_t b = 0;
+  b += align256(T * E * 4);             // logits
+  b += 2 * align256(T * k * 4);         // ids, wts
+  b += 2 * align256(nchunks * E * 4);   // chunk_hist, chunk_base
+  b += align256(E * 4);                 // counts
+  b += align256((E + 1) * 4);           // offsets
+  b += 2 * align256(T * k * 4);         // perm, inv_perm
+  b += 3 * align256((E + 1) * 4);       // segments
+  b += 4 * align256(4);                 // num_seg, ticket, err, pad
+  b += align256(P * I * 2);             // h
+  b += align256(P * H * 4);             // ypart
+  b += 2 * align256(T * H * 2);         // x/out staging
+  b += align256(T * k * 4) * 2;         // ids/w staging
+  return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+size_t moe_record_bytes(int32_t hidden, int32_t intermediate, int32_t group_size) {
+  Layout L;
+  if (!record_layout(hidden, intermediate, group_size, &L)) return 0;
+  return L.record;
+}
+
+moe_status_t moe_record_section(int32_t hidden, int32_t intermediate, int32_t group_size, int32_t section,
+                                size_t* offset, size_t* bytes) {
+  Layout L;
+  if (!record_layout(hidden, intermediate, group_size, &L)) return fail(MOE_ERR_INVALID_ARG, "invalid shape");
+  if (section < 0 || section > 5) return fail(MOE_ERR_INVALID_ARG, "section %d out of 0..5", section);
+  if (offset) *offset = L.off[section];
+  if (bytes) *bytes = L.size[section];
+  return MOE_OK;
+}
+
+const char* moe_layer_last_error(void) { return g_last_error.c_str(); }
+
+moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_weights_t* weights,
+                              moe_layer_t** out) {
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out must not be NULL");
+  *out = nullptr;
+  moe_status_t st = validate(config, weights);
+  if (st != MOE_OK) return st;
+  moe_layer* L = new (std::nothrow) moe_layer();
+  if (!L) return fail(MOE_ERR_OOM, "host allocation failed");
+  L->cfg = *config;
+  L->w = *weights;
+  record_layout(config->hidden, config->intermediate, config->group_size, &L->lay);
+  L->n_records = config->num_experts + config->has_shared_expert;
+  const char* pdl_env = getenv("MOE_PDL");
+  L->pdl = !(pdl_env && pdl_env[0] == '0');
+  cudaError_t e = cudaGetDevice(&L->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+  if (e != cudaSuccess) {
+    delete L;
+    return cuda_fail(e, "device query");
+  }
+  const size_t wsb = workspace_bytes(L->cfg);
+  e = cudaMalloc(&L->ws, wsb);
+  if (e != cudaSuccess) {
+    delete L;
+    cudaGetLastError();
+    return fail(MOE_ERR_OOM, "workspace allocation of %zu bytes failed: %s", wsb, cudaGetErrorString(e));
+  }
+  {
+    const size_t T = L->cfg.max_tokens, k = L->cfg.top_k, E = L->cfg.num_experts;
+    const size_t H = L->cfg.hidden, I = L->cfg.intermediate;
+    const size_t nchunks = (T + moe::kRouteChunkTokens - 1) / moe::kRouteChunkTokens;
+    const size_t P = T * k + T;
+    char* p = static_cast<char*>(L->ws);
+    L->logits = carve<float>(p, T * E);
+    L->ids = carve<int32_t>(p, T * k);
+    L->wts = carve<float>(p, T * k);
+    L->chunk_hist = carve<int32_t>(p, nchunks * E);
+    L->chunk_base = carve<int32_t>(p, nchunks * E);
+    L->counts = carve<int32_t>(p, E);
+    L->offsets = carve<int32_t>(p, E + 1);
+    L->perm = carve<int32_t>(p, T * k);
+    L->inv_perm = carve<int32_t>(p, T * k);
+    L->seg_expert = carve<int32_t>(p, E + 1);
+    L->seg_start = carve<int32_t>(p, E + 1);
+    L->seg_count = carve<int32_t>(p, E + 1);
+    L->num_seg = carve<int32_t>(p, 1);
+    L->ticket = carve<uint32_t>(p, 1);
+    L->err = carve<uint32_t>(p, 1);
+    carve<uint32_t>(p, 1);
+    L->hbuf = carve<__half>(p, P * I);
+    L->ypart = carve<float>(p, P * H);
+    L->x_stage = carve<__half>(p, T * H);
+    L->out_stage = carve<__half>(p, T * H);
+    L->ids_stage = carve<int32_t>(p, T * k);
+    L->w_stage = carve<float>(p, T * k);
+  }
+  // zero the small control words (ticket, error word, segment count)
+  e = cudaMemset(L->num_seg, 0, 4 * 256);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(L->ws);
+    delete L;
+    return cuda_fail(e, "workspace init");
+  }
+  if (config->residency == MOE_RESIDENCY_PARTIAL) {
+    st = moe::residency_create(L->cfg, L->lay.record, L->n_records, weights->host_backing, &L->res);
+    if (st != MOE_OK) {
+      cudaFree(L->ws);
+      delete L;
+      return fail(st, "%s", moe::residency_last_error());
+    }
+  }
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_destroy(moe_layer_t* layer) {
+  if (!layer) return MOE_OK;
+  for (cudaEvent_t& ev : layer->ev)
+    if (ev) cudaEventDestroy(ev);
+  if (layer->res) moe::residency_destroy(layer->res);
+  if (layer->ws) cudaFree(layer->ws);
+  delete layer;
+  return MOE_OK;
+}
+
+namespace {
+
+// Enqueue routing + experts + combine for one batch whose tokens are on the
+// device. pool/e2s/num_slots select the record table.
+moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s,
+                             const uint8_t* pool, const int32_t* e2s, int num_slots) {
+  const moe_layer_config_t& c = L->cfg;
+  const int H = c.hidden, I = c.intermediate, E = c.num_experts, k = c.top_k, G = c.group_size;
+  const int max_seg = std::min(E, T * k) + c.has_shared_expert;
+
+  const moe::GemvPlan pd = moe::plan_gemv(I, H, G, true, T);
+  const moe::GemvPlan ps = moe::plan_gemv(H, I, G, false, T);
+  if (!moe::gemv_plan_supported(pd) || !moe::gemv_plan_supported(ps))
+    return fail(MOE_ERR_UNSUPPORTED, "no GEMV variant for H=%d I=%d", H, I);
+
+  moe::GemvArgs gd = {};
+  gd.pool = pool;
+  gd.record_bytes = (long long)L->lay.record;
+  gd.expert_to_slot = e2s;
+  gd.num_slots = num_slots;
+  gd.q_off0 = L->lay.off[0];
+  gd.q_off1 = L->lay.off[1];
+  gd.s_off0 = L->lay.off[3];
+  gd.s_off1 = L->lay.off[4];
+  gd.N = I;
+  gd.K = H;
+  gd.G = G;
+  gd.ng = (H + G - 1) / G;
+  gd.lpr = pd.lpr;
+  gd.rb = pd.rb;
+  gd.num_seg = L->num_seg;
+  gd.seg_expert = L->seg_expert;
+  gd.seg_start = L->seg_start;
+  gd.seg_count = L->seg_count;
+  gd.act = x;
+  gd.act_gather = 1;
+  gd.perm = L->perm;
+  gd.Tk = T * k;
+  gd.k = k;
+  gd.h_out = L->hbuf;
+  gd.y_out = nullptr;
+  gd.stages = pd.stages;
+  gd.stage_bytes = pd.stage_bytes;
+  gd.err = L->err;
+  const int nrb_d = (I + pd.rb - 1) / pd.rb;
+  const int grid_d = std::max(1, std::min(L->num_sms, max_seg * nrb_d));
+  cudaError_t e = moe::launch_gemv(gd, true, pd, grid_d, s, L->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[2], s, cudaEventRecordExternal);
+
+  moe::GemvArgs gs = gd;
+  gs.q_off0 = L->lay.off[2];
+  gs.q_off1 = 0;
+  gs.s_off0 = L->lay.off[5];
+  gs.s_off1 = 0;
+  gs.N = H;
+  gs.K = I;
+  gs.ng = (I + G - 1) / G;
+  gs.lpr = ps.lpr;
+  gs.rb = ps.rb;
+  gs.act = L->hbuf;
+  gs.act_gather = 0;
+  gs.h_out = nullptr;
+  gs.y_out = L->ypart;
+  gs.stages = ps.stages;
+  gs.stage_bytes = ps.stage_bytes;
+  const int nrb_s = (H + ps.rb - 1) / ps.rb;
+  const int grid_s = std::max(1, std::min(L->num_sms, max_seg * nrb_s));
+  e = moe::launch_gemv(gs, false, ps, grid_s, s, L->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "down launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[3], s, cudaEventRecordExternal);
+
+  moe::CombineArgs ca = {};
+  ca.ypart = L->ypart;
+  ca.w = L->wts;
+  ca.x = c.add_residual ? x : nullptr;
+  ca.out = out;
+  ca.T = T;
+  ca.H = H;
+  ca.k = k;
+  ca.has_shared = c.has_shared_expert;
+  e = moe::launch_combine(ca, s, L->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
+  return MOE_OK;
+}
+
+moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_user, float* w_user,
+                           cudaStream_t s) {
+  const moe_layer_config_t& c = L->cfg;
+  moe::RouteArgs ra = {};
+  ra.x = x;
+  ra.wr = L->w.router_w;
+  ra.bias = L->w.router_bias;
+  ra.T = T;
+  ra.H = c.hidden;
+  ra.E = c.num_experts;
+  ra.k = c.top_k;
+  ra.renorm = c.renormalize;
+  ra.has_shared = c.has_shared_expert;
+  ra.logits = L->logits;
+  ra.ids = L->ids;
+  ra.w = L->wts;
+  ra.ids_user = ids_user;
+  ra.w_user = w_user;
+  ra.chunk_hist = L->chunk_hist;
+  ra.chunk_base = L->chunk_base;
+  ra.counts = L->counts;
+  ra.offsets = L->offsets;
+  ra.perm = L->perm;
+  ra.inv_perm = L->inv_perm;
+  ra.seg_expert = L->seg_expert;
+  ra.seg_start = L->seg_start;
+  ra.seg_count = L->seg_count;
+  ra.num_seg = L->num_seg;
+  ra.ticket = L->ticket;
+  ra.err = L->err;
+  const bool small = T <= moe::kSmallRouteMaxT && (size_t)T * c.hidden * 2 <= 200 * 1024;
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
+  cudaError_t e = small ? moe::launch_route_small(ra, s, L->pdl) : moe::launch_route_large(ra, s, L->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "routing launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[1], s, cudaEventRecordExternal);
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, void* out, int32_t* topk_ids,
+                               float* topk_w, void* stream) {
+  if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");
+  if (T < 0 || T > layer->cfg.max_tokens)
+    return fail(MOE_ERR_INVALID_ARG, "T=%d out of 0..max_tokens=%d", T, layer->cfg.max_tokens);
+  if (T == 0) return MOE_OK;
+  if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out must not be NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __half* xh = static_cast<const __half*>(x);
+  __half* oh = static_cast<__half*>(out);
+  // programmatic dependent launch only on explicitly created streams
+  const bool pdl_saved = layer->pdl;
+  if (s == nullptr) layer->pdl = false;
+  moe_status_t st = enqueue_route(layer, xh, T, topk_ids, topk_w, s);
+  if (st != MOE_OK) {
+    layer->pdl = pdl_saved;
+    return st;
+  }
+  if (layer->cfg.residency == MOE_RESIDENCY_FULL) {
+    st = enqueue_experts(layer, xh, T, oh, s, static_cast<const uint8_t*>(layer->w.slot_pool),
+                         layer->w.expert_to_slot, layer->cfg.num_slots);
+  } else {
+    st = moe::residency_forward(layer->res, layer, xh, T, oh, s);
+  }
+  layer->pdl = pdl_saved;
+  if (st != MOE_OK) return st;
+  layer->last_T = T;
+  layer->stats.forward_calls += 1;
+  layer->stats.tokens += (uint64_t)T;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* x_host, int32_t T, void* out_host,
+                                    int32_t* topk_ids_host, float* topk_w_host, void* stream) {
+  if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");
+  if (T < 0 || T > layer->cfg.max_tokens)
+    return fail(MOE_ERR_INVALID_ARG, "T=%d out of 0..max_tokens=%d", T, layer->cfg.max_tokens);
+  if (T == 0) return MOE_OK;
+  if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must not be NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t xb = (size_t)T * layer->cfg.hidden * 2, kb = (size_t)T * layer->cfg.top_k * 4;
+  cudaError_t e = cudaMemcpyAsync(layer->x_stage, x_host, xb, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "x host->device");
+  moe_status_t st = moe_layer_forward(layer, layer->x_stage, T, layer->out_stage,
+                                      topk_ids_host ? layer->ids_stage : nullptr,
+                                      topk_w_host ? layer->w_stage : nullptr, stream);
+  if (st != MOE_OK) return st;
+  e = cudaMemcpyAsync(out_host, layer->out_stage, xb, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && topk_ids_host)
+    e = cudaMemcpyAsync(topk_ids_host, layer->ids_stage, kb, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && topk_w_host) e = cudaMemcpyAsync(topk_w_host, layer->w_stage, kb, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "result device->host");
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_routing(const moe_layer_t* layer, int32_t* counts, int32_t* offsets, int32_t* perm,
+                               int32_t* inv_perm, void* stream) {
+  if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t E = layer->cfg.num_experts, n = (size_t)layer->last_T * layer->cfg.top_k;
+  cudaError_t e = cudaSuccess;
+  if (counts) e = cudaMemcpyAsync(counts, layer->counts, E * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && offsets) e = cudaMemcpyAsync(offsets, layer->offsets, (E + 1) * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && perm && n) e = cudaMemcpyAsync(perm, layer->perm, n * 4, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && inv_perm && n)
+    e = cudaMemcpyAsync(inv_perm, layer->inv_perm, n * 4, cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "routing copy");
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_sync(moe_layer_t* layer, void* stream) {
+  if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t word = 0;
+  e = cudaMemcpy(&word, layer->err, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "error word read");
+  if (word != 0u) {
+    cudaMemset(layer->err, 0, 4);
+    cudaDeviceSynchronize();
+    if (word == 1) return fail(MOE_ERR_TIMEOUT, "a device-side wait gave up (error word %u)", word);
+    return fail(MOE_ERR_INTERNAL, "device-side check failed (error word %u)", word);
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_set_profiling(moe_layer_t* layer, int32_t enable) {
+  if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");
+  if (enable && !layer->ev[0]) {
+    for (cudaEvent_t& ev : layer->ev) {
+      cudaError_t e = cudaEventCreate(&ev);
+      if (e != cudaSuccess) return cuda_fail(e, "event create");
+    }
+  }
+  layer->profiling = enable != 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* p) {
+  if (!layer || !p) return fail(MOE_ERR_INVALID_ARG, "layer and profile must not be NULL");
+  if (!layer->ev[0]) return fail(MOE_ERR_INVALID_ARG, "profiling was never enabled");
+  cudaError_t e = cudaEventSynchronize(layer->ev[4]);
+  float ms[4] = {0, 0, 0, 0}, tot = 0;
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&ms[i], layer->ev[i], layer->ev[i + 1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&tot, layer->ev[0], layer->ev[4]);
+  int32_t nseg = 0;
+  if (e == cudaSuccess) e = cudaMemcpy(&nseg, layer->num_seg, 4, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "profile read");
+  p->route_ms = ms[0];
+  p->gate_up_ms = ms[1];
+  p->down_ms = ms[2];
+  p->combine_ms = ms[3];
+  p->total_ms = tot;
+  p->active_experts = nseg - layer->cfg.has_shared_expert;
+  p->tokens = layer->last_T;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_get_stats(const moe_layer_t* layer, moe_layer_stats_t* stats) {
+  if (!layer || !stats) return fail(MOE_ERR_INVALID_ARG, "layer and stats must not be NULL");
+  *stats = layer->stats;
+  if (layer->res) moe::residency_fill_stats(layer->res, stats);
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- internal
+namespace moe {
+
+cudaError_t ensure_smem_ptr(const void* kern, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void*, size_t> set_bytes;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = set_bytes.find(kern);
+  if (it != set_bytes.end() && it->second >= bytes) return cudaSuccess;
+  if (bytes <= 48 * 1024 && it == set_bytes.end()) {
+    set_bytes[kern] = 48 * 1024;
+    return cudaSuccess;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) set_bytes[kern] = bytes;
+  return e;
+}
+
+moe_status_t layer_enqueue_experts(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s,
+                                   const uint8_t* pool, const int32_t* e2s, int num_slots) {
+  return enqueue_experts(L, x, T, out, s, pool, e2s, num_slots);
+}
+
+const int32_t* layer_counts(const moe_layer* L) { return L->counts; }
+const moe_layer_config_t& layer_config(const moe_layer* L) { return L->cfg; }
+size_t layer_record_bytes(const moe_layer* L) { return L->lay.record; }
+int32_t* layer_num_seg(moe_layer* L) { return L->num_seg; }
+int32_t* layer_seg_expert(moe_layer* L) { return L->seg_expert; }
+int32_t* layer_seg_start(moe_layer* L) { return L->seg_start; }
+int32_t* layer_seg_count(moe_layer* L) { return L->seg_count; }
+
+}  // namespace moe

@@ -1,0 +1,22 @@
+// Partial residency (library-owned slot pool filled from pinned host backing).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "moe_layer.h"
+
+struct moe_layer;
+
+namespace moe {
+
+struct Residency;
+
+moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes, int n_records,
+                              const void* host_backing, Residency** out);
+void residency_destroy(Residency* r);
+const char* residency_last_error();
+moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s);
+void residency_fill_stats(const Residency* r, moe_layer_stats_t* st);
+
+}  // namespace moe

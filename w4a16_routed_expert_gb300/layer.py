@@ -1,0 +1,100 @@
+"""MoELayer: a torch-tensor convenience wrapper over the C ABI.
+
+PyTorch only provides device memory and streams here; every step of the
+layer runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import capi
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class MoELayer:
+    """One routed-expert layer bound to device-resident weights.
+
+    router_w: cuda fp32 [E][H]; router_bias: cuda fp32 [E] or None;
+    pool: cuda uint8 [num_slots][record_bytes] (full residency) ;
+    expert_to_slot: cuda int32 [E (+1)];
+    host_backing: pinned cpu uint8 [E (+1)][record_bytes] (partial residency).
+    """
+
+    def __init__(self, *, hidden, intermediate, num_experts, top_k, group_size, renormalize,
+                 has_shared=False, max_tokens, router_w, router_bias=None, pool=None,
+                 expert_to_slot=None, num_slots=None, host_backing=None, add_residual=False):
+        partial = host_backing is not None
+        self.cfg = capi.moe_layer_config_t(
+            hidden=hidden, intermediate=intermediate, num_experts=num_experts, top_k=top_k,
+            group_size=group_size, renormalize=int(bool(renormalize)), has_shared_expert=int(bool(has_shared)),
+            max_tokens=max_tokens,
+            num_slots=int(num_slots if num_slots is not None else (pool.shape[0] if pool is not None else 0)),
+            residency=capi.MOE_RESIDENCY_PARTIAL if partial else capi.MOE_RESIDENCY_FULL,
+            add_residual=int(bool(add_residual)))
+        self.weights = capi.moe_layer_weights_t(
+            router_w=_ptr(router_w), router_bias=_ptr(router_bias),
+            slot_pool=None if partial else _ptr(pool), expert_to_slot=None if partial else _ptr(expert_to_slot),
+            host_backing=_ptr(host_backing) if partial else None)
+        # keep the borrowed buffers alive for the handle's lifetime
+        self._keep = (router_w, router_bias, pool, expert_to_slot, host_backing)
+        self.hidden, self.top_k, self.num_experts = hidden, top_k, num_experts
+        self.handle = capi.moe_layer_create(self.cfg, self.weights)
+
+    def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, ids: Optional[torch.Tensor] = None,
+                w: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        capi.check(capi.moe_layer_forward(self.handle, _ptr(x), T, _ptr(out), _ptr(ids), _ptr(w),
+                                          _stream_handle(stream)), "moe_layer_forward")
+        return out
+
+    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, ids_host=None, w_host=None, stream=None):
+        capi.check(capi.moe_layer_forward_host(self.handle, _ptr(x_host), x_host.shape[0], _ptr(out_host),
+                                               _ptr(ids_host), _ptr(w_host), _stream_handle(stream)),
+                   "moe_layer_forward_host")
+        return out_host
+
+    def routing(self, T: int, stream=None):
+        dev = torch.device("cuda")
+        E, k = self.num_experts, self.top_k
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        perm = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+        inv = torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)
+        capi.check(capi.moe_layer_routing(self.handle, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+                                          _stream_handle(stream)), "moe_layer_routing")
+        return counts, offsets, perm[:T * k], inv[:T * k]
+
+    def sync(self, stream=None):
+        capi.check(capi.moe_layer_sync(self.handle, _stream_handle(stream)), "moe_layer_sync")
+
+    def set_profiling(self, enable: bool = True):
+        capi.moe_layer_set_profiling(self.handle, enable)
+
+    def profile(self):
+        return capi.moe_layer_get_profile(self.handle)
+
+    def stats(self):
+        return capi.moe_layer_get_stats(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            capi.moe_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -32,7 +32,7 @@ above is this library's own definition.
 from __future__ import annotations
 
 import dataclasses
-import math
+import os
 from typing import Optional
 
 import numpy as np
@@ -173,12 +173,20 @@ class Layer:
     expert_to_slot: np.ndarray      # int32 [n_records]
 
 
+def _expert_record(args):
+    shape, child, codes = args
+    rng = np.random.default_rng(child)
+    return pack_record(shape.hidden, shape.intermediate, shape.group_size, *_expert_codes(shape, rng, codes))
+
+
 def make_layer(shape: LayerShape, seed: int, codes: str = "quantized",
-               shuffle_slots: bool = True, extra_slots: int = 0) -> Layer:
+               shuffle_slots: bool = True, extra_slots: int = 0, workers: Optional[int] = None) -> Layer:
     """Draw one layer. Expert e's draws come from its own child seed, so any
-    expert can be regenerated alone. Records are stored in slot order through
-    a random expert_to_slot permutation (identity if shuffle_slots is False);
-    ``extra_slots`` appends unused slots filled with 0xFF bytes."""
+    expert can be regenerated alone (and records can be drawn in parallel
+    worker processes with identical results). Records are stored in slot
+    order through a random expert_to_slot permutation (identity if
+    shuffle_slots is False); ``extra_slots`` appends unused slots filled with
+    0xFF bytes."""
     E = shape.num_experts
     nrec = shape.n_records
     children = np.random.SeedSequence(seed).spawn(3 + nrec)
@@ -194,10 +202,20 @@ def make_layer(shape: LayerShape, seed: int, codes: str = "quantized",
         slot_of = np.arange(nrec, dtype=np.int32)
     rb = record_bytes(shape.hidden, shape.intermediate, shape.group_size)
     records = np.full((n_slots, rb), 0xFF, dtype=np.uint8)
-    for e in range(nrec):
-        rng = np.random.default_rng(children[3 + e])
-        parts = _expert_codes(shape, rng, codes)
-        records[slot_of[e]] = pack_record(shape.hidden, shape.intermediate, shape.group_size, *parts)
+    jobs = [(shape, children[3 + e], codes) for e in range(nrec)]
+    weights_per_layer = nrec * 3 * shape.hidden * shape.intermediate
+    if workers is None:
+        workers = min(os.cpu_count() or 1, 16) if weights_per_layer > 64 * 2**20 else 1
+    if workers > 1:
+        import concurrent.futures
+        import multiprocessing
+        ctx = multiprocessing.get_context("spawn")
+        with concurrent.futures.ProcessPoolExecutor(max_workers=workers, mp_context=ctx) as ex:
+            for e, rec in enumerate(ex.map(_expert_record, jobs, chunksize=max(1, nrec // (4 * workers)))):
+                records[slot_of[e]] = rec
+    else:
+        for e, job in enumerate(jobs):
+            records[slot_of[e]] = _expert_record(job)
     return Layer(shape, router_w, bias, records, slot_of)
 
 
