@@ -1,0 +1,87 @@
+"""Partially resident slot pool on the GPU: same results as full residency
+(bit-exact) and as the oracle, the pool bookkeeping counters, the host copy
+never written, and a host-side injected copy failure."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+from w4a16_routed_expert_gb300 import capi, synth  # noqa: E402
+from w4a16_routed_expert_gb300.layer import MoELayer  # noqa: E402
+
+import gpu_harness as GH  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    capi.lib()
+
+
+def _partial(lay, slots, max_tokens):
+    s = lay.shape
+    host = torch.from_numpy(lay.records[lay.expert_to_slot]).contiguous()  # expert order
+    dev = torch.device("cuda")
+    ml = MoELayer(hidden=s.hidden, intermediate=s.intermediate, num_experts=s.num_experts, top_k=s.top_k,
+                  group_size=s.group_size, renormalize=s.renormalize, has_shared=s.has_shared,
+                  max_tokens=max_tokens, router_w=torch.from_numpy(lay.router_w).to(dev),
+                  router_bias=torch.from_numpy(lay.router_bias).to(dev) if lay.router_bias is not None else None,
+                  num_slots=slots, host_backing=host)
+    return ml, host
+
+
+@pytest.mark.parametrize("shape,slots,T", [
+    (synth.LayerShape(256, 256, 16, 2, 64, True), 4, 8),
+    (synth.LayerShape(512, 384, 24, 3, 128, True, has_shared=True), 5, 12),
+    (synth.LayerShape(2880, 2880, 12, 4, 128, True), 4, 6),
+])
+def test_partial_matches_full_and_oracle(shape, slots, T):
+    lay = synth.make_layer(shape, seed=21, codes="uniform")
+    x = synth.make_tokens(shape.hidden, T, seed=21)
+    full = GH.upload(lay, max_tokens=T)
+    gf = GH.run(full, x)
+    full.close()
+    ml, host = _partial(lay, slots, T)
+    before = host.numpy().copy()
+    g1 = GH.run(ml, x)
+    g2 = GH.run(ml, x)
+    st = ml.stats()
+    for key in ("out", "ids", "w", "perm", "counts"):
+        assert np.array_equal(g1[key], gf[key]) and np.array_equal(g2[key], gf[key]), key
+    GH.compare(lay, x, g1)
+    demanded = int((g1["counts"] > 0).sum()) + (1 if shape.has_shared else 0)
+    assert st.forward_calls == 2 and st.tokens == 2 * T
+    assert st.expert_hits + st.expert_misses == 2 * demanded
+    assert st.h2d_bytes == st.expert_misses * lay.records.shape[1]
+    assert st.d2h_expert_bytes == 0
+    assert st.waves >= 2 * -(-demanded // slots)
+    # the second call finds at least the previous call's last wave resident
+    assert st.expert_hits >= min(slots, demanded) - 0
+    assert np.array_equal(host.numpy(), before), "host backing was written"
+    ml.close()
+
+
+def test_injected_copy_failure_keeps_a_consistent_pool(monkeypatch):
+    shape = synth.LayerShape(256, 256, 16, 2, 64, True)
+    lay = synth.make_layer(shape, seed=22, codes="uniform")
+    x = synth.make_tokens(shape.hidden, 8, seed=22)
+    monkeypatch.setenv("MOE_FAULT_INJECT", "h2d_fail")
+    ml, host = _partial(lay, 4, 8)
+    with pytest.raises(capi.MoEError) as ei:
+        GH.run(ml, x)
+    assert ei.value.status == capi.MOE_ERR_CUDA and "injected" in str(ei.value)
+    # the injection is one-shot; the next forward is correct
+    g = GH.run(ml, x)
+    GH.compare(lay, x, g)
+    ml.close()
+
+
+def test_capacity_shortfall_fails_at_create():
+    shape = synth.LayerShape(256, 256, 16, 4, 64, True)
+    lay = synth.make_layer(shape, seed=23)
+    with pytest.raises(capi.MoEError) as ei:
+        _partial(lay, 3, 4)
+    assert ei.value.status == capi.MOE_ERR_CAPACITY

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w4a16.so")
-SOURCES = ["route.cu", "gemv.cu", "moe_layer.cu", "residency.cu"]
+SOURCES = ["route.cu", "gemv.cu", "gemm.cu", "moe_layer.cu", "residency.cu", "slot_planner.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + [
@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers):
             jobs.append([nvcc] + FLAGS + ["-c", s, "-o", o])

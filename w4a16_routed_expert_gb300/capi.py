@@ -78,7 +78,57 @@ PROTOTYPES = {
     "moe_layer_get_profile": (_I32, [_P, ctypes.POINTER(moe_layer_profile_t)]),
     "moe_layer_destroy": (_I32, [_P]),
     "moe_layer_last_error": (ctypes.c_char_p, []),
+    # include/moe_residency.h
+    "moe_slot_planner_create": (_P, [_I32, _I32]),
+    "moe_slot_planner_plan": (_I32, [_P, ctypes.POINTER(_I32), _I32, _I32, ctypes.POINTER(_I32),
+                                     ctypes.POINTER(_I32), ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "moe_slot_planner_slot_of": (_I32, [_P, _I32]),
+    "moe_slot_planner_invalidate": (None, [_P, _I32]),
+    "moe_slot_planner_destroy": (None, [_P]),
 }
+
+MOE_PLAN_HITS_FIRST = 0
+MOE_PLAN_FIXED_ORDER_LRU = 1
+
+
+class SlotPlanner:
+    """Host-side slot planner of the partially resident pool (no GPU)."""
+
+    def __init__(self, n_records: int, num_slots: int):
+        self.n_records = n_records
+        self.h = lib().moe_slot_planner_create(n_records, num_slots)
+        if not self.h:
+            raise ValueError("invalid planner size")
+
+    def plan(self, demanded, policy=MOE_PLAN_HITS_FIRST):
+        d = sorted(int(e) for e in demanded)
+        n = len(d)
+        arr = (_I32 * max(n, 1))(*d)
+        wave = (_I32 * max(n, 1))()
+        slot = (_I32 * max(n, 1))()
+        hit = (_I32 * max(n, 1))()
+        nw = _I32()
+        rc = lib().moe_slot_planner_plan(self.h, arr, n, policy, wave, slot, hit, ctypes.byref(nw))
+        if rc != 0:
+            raise ValueError("invalid plan request")
+        return dict(experts=d, wave=list(wave)[:n], slot=list(slot)[:n], hit=list(hit)[:n], n_waves=nw.value)
+
+    def slot_of(self, e: int) -> int:
+        return lib().moe_slot_planner_slot_of(self.h, e)
+
+    def invalidate(self, slot: int) -> None:
+        lib().moe_slot_planner_invalidate(self.h, slot)
+
+    def close(self):
+        if self.h:
+            lib().moe_slot_planner_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def lib() -> ctypes.CDLL:

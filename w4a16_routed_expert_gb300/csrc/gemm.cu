@@ -1,0 +1,494 @@
+// Prefill-regime grouped W4A16 GEMM on the 5th-generation tensor cores.
+//
+// Horizon RunMap report, "What is implemented": the INT4 experts stay compact
+// in GPU memory and run with FP16 activations; here a weight tile is expanded
+// to FP16 only inside shared memory, for the MMAs that consume it.
+//
+// Tile = 128 weight rows x 128 tokens of one expert segment; the weights are
+// the MMA's A operand (M = 128) and the tokens its B operand (N = 128), so
+// each dequantised weight tile serves 128 tokens and the accumulator's TMEM
+// lane is the output unit, its column the token.
+//
+// Warp roles of a persistent CTA (one per SM):
+//   warp 0      TMA producer: INT4 code tiles (3-D tensor map over the slot
+//               pool: bytes x rows x slot) and token tiles (gate/up: four-row
+//               gathers of x through the permutation; down: 2-D tiles of h,
+//               which is already in expert-sorted order)
+//   warp 1      TMEM allocation and the single MMA-issuing thread
+//   warps 2-9   dequantisers: codes -> (q - 8) * s in FP16, written in the
+//               128-byte-swizzled K-major layout the MMA reads
+//   warps 10-13 epilogue: TMEM -> registers; gate/up: h = silu(g) * u -> FP16
+//               h rows; down: FP32 partial rows at the pair's flat index
+// Rings: codes (TMA -> dequant), A (dequant -> MMA), B (TMA -> MMA), and two
+// TMEM accumulator buffers (MMA -> epilogue), each with full/empty mbarriers.
+// Every wait is bounded; a wait that gives up records an error, the CTA
+// drains its in-flight copies and MMAs, frees TMEM and exits.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;  // weight rows per tile
+constexpr int BN = 128;  // tokens per tile
+constexpr int BK = 64;   // K per pipeline step (128 bytes of FP16)
+constexpr int kCodeStages = 4;
+constexpr int kAStages = 3;
+constexpr int kBStages = 4;
+constexpr int kDequantWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpDequant0 = 2;
+constexpr int kWarpEpi0 = kWarpDequant0 + kDequantWarps;
+constexpr int kGemmThreads = (kWarpEpi0 + kEpiWarps) * 32;
+constexpr int kMaxSeg = 1025;
+
+template <bool DUAL>
+struct Smem {
+  static constexpr int mats = DUAL ? 2 : 1;
+  static constexpr uint32_t a_tile = BM * BK * 2;
+  static constexpr uint32_t b_tile = BN * BK * 2;
+  static constexpr uint32_t code_tile = BM * BK / 2;
+  static constexpr uint32_t off_a = 0;
+  static constexpr uint32_t off_b = off_a + kAStages * mats * a_tile;
+  static constexpr uint32_t off_codes = off_b + kBStages * b_tile;
+  static constexpr uint32_t off_bar = off_codes + kCodeStages * mats * code_tile;
+  // codes_full/empty, a_full/empty, b_full/empty, acc_full/empty, drain
+  static constexpr uint32_t n_bars = 2 * kCodeStages + 2 * kAStages + 2 * kBStages + 4 + 1;
+  static constexpr uint32_t off_misc = off_bar + n_bars * 8;
+  static constexpr uint32_t off_prefix = off_misc + 64;
+  static constexpr uint32_t bytes = off_prefix + (kMaxSeg + 1) * 4;
+  static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
+  static constexpr uint32_t tmem_cols = DUAL ? 512 : 256;
+  static constexpr uint32_t acc_stride = DUAL ? 256 : 128;
+};
+
+struct Bars {
+  uint64_t* codes_full;
+  uint64_t* codes_empty;
+  uint64_t* a_full;
+  uint64_t* a_empty;
+  uint64_t* b_full;
+  uint64_t* b_empty;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* drain;
+};
+
+struct Misc {
+  uint32_t tmem_base;
+  int abort_flag;
+  int total_tiles;
+  int codes_issued;
+  int b_issued;
+  int mma_issued;
+};
+
+__device__ __forceinline__ int find_segment(const int* prefix, int nseg, int t) {
+  int lo = 0, hi = nseg - 1;  // largest s with prefix[s] <= t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// (q - 8) * s for the 8 codes of one word (k = 8i .. 8i+7), as 8 FP16 in
+// k order. Codes k=2b (low nibble) and 2b+1 (high nibble) of byte b become
+// the half pair {1024 + q_lo, 1024 + q_hi} via the exponent-bias trick, then
+// (h - 1032) is exact and one multiply by the FP16 scale rounds once.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
+  const uint32_t hi = w >> 4;
+  const __half2 bias = __half2half2(__ushort_as_half(0x6408));  // 1032
+  uint32_t out[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    // byte b of w in bits 0..7, byte b of (w >> 4) in bits 16..23
+    const uint32_t p = __byte_perm(w, hi, (uint32_t)(b | ((4 + b) << 8)) | 0x5400u);
+    uint32_t v;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(p), "r"(0x000F000Fu), "r"(0x64006400u));
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    h = __hmul2(__hsub2(h, bias), s2);
+    out[b] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+template <bool DUAL>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tm_codes0, const __grid_constant__ CUtensorMap tm_codes1,
+           const __grid_constant__ CUtensorMap tm_act, GemmArgs a) {
+  using L = Smem<DUAL>;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::off_bar);
+  Bars B;
+  B.codes_full = bars;
+  B.codes_empty = B.codes_full + kCodeStages;
+  B.a_full = B.codes_empty + kCodeStages;
+  B.a_empty = B.a_full + kAStages;
+  B.b_full = B.a_empty + kAStages;
+  B.b_empty = B.b_full + kBStages;
+  B.acc_full = B.b_empty + kBStages;
+  B.acc_empty = B.acc_full + 2;
+  B.drain = B.acc_empty + 2;
+  Misc* misc = reinterpret_cast<Misc*>(smem + L::off_misc);
+  int* prefix = reinterpret_cast<int*>(smem + L::off_prefix);
+
+  if (tid == 0) {
+    for (int i = 0; i < kCodeStages; ++i) {
+      mbar_init(&B.codes_full[i], 1);
+      mbar_init(&B.codes_empty[i], kDequantWarps);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&B.a_full[i], kDequantWarps);
+      mbar_init(&B.a_empty[i], 1);
+    }
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(&B.b_full[i], 1);
+      mbar_init(&B.b_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&B.acc_full[i], 1);
+      mbar_init(&B.acc_empty[i], kEpiWarps);
+    }
+    mbar_init(B.drain, 1);
+    misc->abort_flag = 0;
+    misc->codes_issued = 0;
+    misc->b_issued = 0;
+    misc->mma_issued = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    prefetch_tmap(&tm_codes0);
+    if (DUAL) prefetch_tmap(&tm_codes1);
+    prefetch_tmap(&tm_act);
+  }
+  if (warp == kWarpMma) tmem_alloc(&misc->tmem_base, L::tmem_cols);
+  pdl_trigger();
+  pdl_wait();
+
+  // tile prefix over the segments (segment s has m_tiles * ceil(count/BN) tiles)
+  const int nseg = min(*a.num_seg, kMaxSeg);
+  const int m_tiles = (a.N + BM - 1) / BM;
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 0; base < nseg; base += 32) {
+      const int s = base + lane;
+      const int c = s < nseg ? a.seg_count[s] : 0;
+      int v = m_tiles * ((c + BN - 1) / BN);
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (s < nseg) prefix[s] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      prefix[nseg] = run;
+      misc->total_tiles = run;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const int total = misc->total_tiles;
+  const uint32_t tbase = misc->tmem_base;
+  const int nK = a.K / BK;
+  volatile int* abort_flag = &misc->abort_flag;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    uint32_t g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const int s = find_segment(prefix, nseg, t);
+      const int local = t - prefix[s];
+      const int cnt = a.seg_count[s];
+      const int ntl = (cnt + BN - 1) / BN;
+      const int m0 = (local / ntl) * BM, n0 = (local % ntl) * BN;
+      const int e = a.seg_expert[s];
+      int slot = a.expert_to_slot[e];
+      if (slot < 0 || slot >= a.num_slots) {
+        if (lane == 0) record_error(a.err, MOE_DEV_ERR_BOUNDS);
+        slot = 0;
+      }
+      const int pos0 = a.seg_start[s];
+      int rows[4] = {0, 0, 0, 0};
+      if (DUAL) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int tok = min(n0 + 4 * lane + i, cnt - 1);
+          const int p = pos0 + tok;
+          rows[i] = (p < a.Tk) ? (__ldg(a.perm + p) / a.k) : (p - a.Tk);
+        }
+      }
+      for (int kk = 0; kk < nK; ++kk, ++g) {
+        const int sc = g % kCodeStages, sb = g % kBStages;
+        int good = 1;
+        if (lane == 0) {
+          good = mbar_wait(&B.codes_empty[sc], ((g / kCodeStages) & 1u) ^ 1u, abort_flag, a.err);
+          if (good) {
+            unsigned char* cdst = smem + L::off_codes + (uint32_t)sc * L::mats * L::code_tile;
+            mbar_arrive_expect_tx(&B.codes_full[sc], L::mats * L::code_tile);
+            tma_load_3d(cdst, &tm_codes0, kk * (BK / 2), m0, slot, &B.codes_full[sc]);
+            if (DUAL) tma_load_3d(cdst + L::code_tile, &tm_codes1, kk * (BK / 2), m0, slot, &B.codes_full[sc]);
+            misc->codes_issued = (int)g + 1;
+            good = mbar_wait(&B.b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err);
+            if (good) mbar_arrive_expect_tx(&B.b_full[sb], L::b_tile);
+          }
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        unsigned char* bdst = smem + L::off_b + (uint32_t)sb * L::b_tile;
+        if (DUAL) {
+          tma_gather4(bdst + lane * 4 * (BK * 2), &tm_act, kk * BK, rows[0], rows[1], rows[2], rows[3], &B.b_full[sb]);
+        } else if (lane == 0) {
+          tma_load_2d(bdst, &tm_act, kk * BK, pos0 + n0, &B.b_full[sb]);
+        }
+        if (lane == 0) misc->b_issued = (int)g + 1;
+        __syncwarp();
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+      uint32_t g = 0;
+      int j = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++j) {
+        const int ab = j & 1;
+        if (!mbar_wait(&B.acc_empty[ab], ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, a.err)) break;
+        tc_fence_after();
+        const uint32_t d0 = tbase + (uint32_t)ab * L::acc_stride;
+        for (int kk = 0; kk < nK; ++kk, ++g) {
+          const int sa = g % kAStages, sb = g % kBStages;
+          if (!mbar_wait(&B.a_full[sa], (g / kAStages) & 1u, abort_flag, a.err) ||
+              !mbar_wait(&B.b_full[sb], (g / kBStages) & 1u, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + L::off_a + (uint32_t)sa * L::mats * L::a_tile);
+          const uint32_t bb = smem_u32(smem + L::off_b + (uint32_t)sb * L::b_tile);
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint32_t acc = (kk > 0 || k16 > 0) ? 1u : 0u;
+            const uint64_t bdesc = smem_desc_sw128(bb + k16 * 32);
+            mma_f16(d0, smem_desc_sw128(a0 + k16 * 32), bdesc, idesc, acc);
+            if (DUAL) mma_f16(d0 + 128, smem_desc_sw128(a0 + L::a_tile + k16 * 32), bdesc, idesc, acc);
+          }
+          misc->mma_issued = 1;
+          mma_commit(&B.a_empty[sa]);
+          mma_commit(&B.b_empty[sb]);
+        }
+        if (!ok) break;
+        mma_commit(&B.acc_full[ab]);
+      }
+    }
+  } else if (warp < kWarpEpi0) {
+    // ------------------------------------------------------------ dequant
+    const int dt = tid - kWarpDequant0 * 32;
+    const int r = dt >> 1, hsel = dt & 1;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const int s = find_segment(prefix, nseg, t);
+      const int local = t - prefix[s];
+      const int cnt = a.seg_count[s];
+      const int ntl = (cnt + BN - 1) / BN;
+      const int m0 = (local / ntl) * BM;
+      const int e = a.seg_expert[s];
+      int slot = a.expert_to_slot[e];
+      if (slot < 0 || slot >= a.num_slots) slot = 0;
+      const bool rvalid = m0 + r < a.N;
+      const __half* sp0 = reinterpret_cast<const __half*>(a.pool + (size_t)slot * a.record_bytes + a.s_off0) +
+                          (size_t)(m0 + r) * a.ng;
+      const __half* sp1 = reinterpret_cast<const __half*>(a.pool + (size_t)slot * a.record_bytes + a.s_off1) +
+                          (size_t)(m0 + r) * a.ng;
+      for (int kk = 0; kk < nK; ++kk, ++g) {
+        const int sc = g % kCodeStages, sa = g % kAStages;
+        const int grp = (kk * BK) / a.G;
+        const __half s0 = rvalid ? __ldg(sp0 + grp) : __float2half(0.f);
+        const __half s1 = (DUAL && rvalid) ? __ldg(sp1 + grp) : __float2half(0.f);
+        if (!mbar_wait(&B.codes_full[sc], (g / kCodeStages) & 1u, abort_flag, a.err) ||
+            !mbar_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
+        const unsigned char* csrc = smem + L::off_codes + (uint32_t)sc * L::mats * L::code_tile;
+        unsigned char* adst = smem + L::off_a + (uint32_t)sa * L::mats * L::a_tile;
+#pragma unroll
+        for (int mat = 0; mat < L::mats; ++mat) {
+          const uint4 w = *reinterpret_cast<const uint4*>(csrc + mat * L::code_tile + r * (BK / 2) + hsel * 16);
+          const __half2 s2 = __half2half2(mat == 0 ? s0 : s1);
+          const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+          unsigned char* rowp = adst + mat * L::a_tile + r * (BK * 2);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = hsel * 4 + i;  // 16-byte chunk (8 halves) of the 128-byte row
+            const uint4 v = dequant8(words[i], s2);
+            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = v;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&B.a_full[sa]);
+          mbar_arrive(&B.codes_empty[sc]);
+        }
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row = 32 * q + lane;
+    int j = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++j) {
+      const int s = find_segment(prefix, nseg, t);
+      const int local = t - prefix[s];
+      const int cnt = a.seg_count[s];
+      const int ntl = (cnt + BN - 1) / BN;
+      const int m0 = (local / ntl) * BM, n0 = (local % ntl) * BN;
+      const int pos0 = a.seg_start[s];
+      const int ab = j & 1;
+      if (!mbar_wait(&B.acc_full[ab], (uint32_t)(j >> 1) & 1u, abort_flag, a.err)) break;
+      tc_fence_after();
+      const int grow = m0 + row;
+      const bool rvalid = grow < a.N;
+      const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * L::acc_stride;
+#pragma unroll 1
+      for (int cb = 0; cb < BN / 32; ++cb) {
+        uint32_t gv[32];
+        tmem_ld32(tacc + cb * 32, gv);
+        if (DUAL) {
+          uint32_t uv[32];
+          tmem_ld32(tacc + 128 + cb * 32, uv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int tok = n0 + cb * 32 + c;
+            if (rvalid && tok < cnt) {
+              const float h = silu_f(__uint_as_float(gv[c])) * __uint_as_float(uv[c]);
+              a.h_out[(size_t)(pos0 + tok) * a.N + grow] = __float2half_rn(h);
+            }
+          }
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const int tok = n0 + cb * 32 + c;
+            if (rvalid && tok < cnt) {
+              const int pos = pos0 + tok;
+              const int f = (pos < a.Tk) ? __ldg(a.perm + pos) : pos;
+              a.y_out[(size_t)f * a.N + grow] = __uint_as_float(gv[c]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.acc_empty[ab]);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (misc->abort_flag) {
+    if (warp == kWarpProducer && lane == 0) {
+      // let issued copies land before shared memory is released
+      const int ci = misc->codes_issued, bi = misc->b_issued;
+      for (int s = 0; s < kCodeStages && s < ci; ++s)
+        mbar_wait(&B.codes_full[s], (uint32_t)((ci - 1 - s) / kCodeStages) & 1u, nullptr, nullptr);
+      for (int s = 0; s < kBStages && s < bi; ++s)
+        mbar_wait(&B.b_full[s], (uint32_t)((bi - 1 - s) / kBStages) & 1u, nullptr, nullptr);
+    }
+    if (warp == kWarpMma && lane == 0 && misc->mma_issued) {
+      mma_commit(B.drain);
+      mbar_wait(B.drain, 0, nullptr, nullptr);
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tbase, L::tmem_cols);
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(bool dual) { return dual ? Smem<true>::alloc : Smem<false>::alloc; }
+
+cudaError_t launch_gemm(bool dual, const CUtensorMap& codes0, const CUtensorMap& codes1, const CUtensorMap& act,
+                        const GemmArgs& a, int grid, cudaStream_t s, bool pdl) {
+  if (dual) {
+    cudaError_t e = ensure_smem(k_gemm<true>, Smem<true>::alloc);
+    if (e != cudaSuccess) return e;
+    return launch_ex(k_gemm<true>, dim3(grid), dim3(kGemmThreads), Smem<true>::alloc, s, pdl, codes0, codes1, act, a);
+  }
+  cudaError_t e = ensure_smem(k_gemm<false>, Smem<false>::alloc);
+  if (e != cudaSuccess) return e;
+  return launch_ex(k_gemm<false>, dim3(grid), dim3(kGemmThreads), Smem<false>::alloc, s, pdl, codes0, codes1, act, a);
+}
+
+// ---------------------------------------------------------------- tensor maps
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+}  // namespace
+
+bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)N, (cuuint64_t)num_slots};
+  const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)record_bytes};
+  const cuuint32_t box[3] = {BK / 2, BM, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool_section), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_tile_n() { return BN; }
+int gemm_tile_k() { return BK; }
+
+}  // namespace moe

@@ -2,10 +2,12 @@
 // kernel files. Not part of the public ABI.
 #pragma once
 
-#include <cstddef>
-#include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
 
 namespace moe {
 
@@ -71,6 +73,32 @@ struct GemvArgs {
   uint32_t* err;
 };
 
+// Grouped W4A16 GEMM over expert segments (prefill regime, tensor cores).
+struct GemmArgs {
+  const uint8_t* pool;
+  long long record_bytes;
+  const int32_t* expert_to_slot;
+  int num_slots;
+  long long s_off0, s_off1;     // scale sections (gate, up) or (down, -)
+  int N, K, G, ng;
+  const int32_t* num_seg;
+  const int32_t* seg_expert;
+  const int32_t* seg_start;
+  const int32_t* seg_count;
+  const int32_t* perm;
+  int Tk;
+  int k;
+  __half* h_out;                // DUAL: [P][N]
+  float* y_out;                 // single: [Tk + T][N]
+  uint32_t* err;
+};
+
+// Tensor maps of the three code sections of a slot pool.
+struct CodeMaps {
+  CUtensorMap gate, up, down;
+  bool valid;
+};
+
 struct CombineArgs {
   const float* ypart;   // [Tk + T][H]
   const float* w;       // [T][k]
@@ -124,5 +152,12 @@ int gemv_kch(int K, int lpr);
 int gemv_lanes_per_row(int K);
 size_t gemv_smem_bytes(int stages, uint32_t stage_bytes);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
+cudaError_t launch_gemm(bool dual, const CUtensorMap& codes0, const CUtensorMap& codes1, const CUtensorMap& act,
+                        const GemmArgs& a, int grid, cudaStream_t s, bool pdl);
+size_t gemm_smem_bytes(bool dual);
+bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes);
+bool encode_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, int box_rows);
+int gemm_tile_n();
+int gemm_tile_k();
 
 }  // namespace moe

@@ -1,0 +1,110 @@
+// Internal definition of the layer handle, shared by the runtime
+// (moe_layer.cu) and the partial-residency driver (residency.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "moe_layer.h"
+
+namespace moe {
+struct Residency;
+}
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t off[6];
+  size_t size[6];
+  size_t record;
+  size_t payload;
+};
+
+inline bool record_layout(int H, int I, int G, Layout* L) {
+  if (H <= 0 || I <= 0 || G <= 0 || (H % 2) || (I % 2)) return false;
+  const size_t gh = (size_t)(H + G - 1) / G, gi = (size_t)(I + G - 1) / G;
+  const size_t sizes[6] = {(size_t)I * H / 2, (size_t)I * H / 2, (size_t)H * I / 2,
+                           2 * (size_t)I * gh,  2 * (size_t)I * gh,  2 * (size_t)H * gi};
+  size_t cur = 0, payload = 0;
+  for (int i = 0; i < 6; ++i) {
+    cur = align256(cur);
+    L->off[i] = cur;
+    L->size[i] = sizes[i];
+    cur += sizes[i];
+    payload += sizes[i];
+  }
+  L->record = align256(cur);
+  L->payload = payload;
+  return true;
+}
+
+struct moe_layer {
+  moe_layer_config_t cfg;
+  moe_layer_weights_t w;
+  int device = 0;
+  int num_sms = 0;
+  Layout lay;
+  int n_records = 0;
+  bool pdl = true;
+  // workspace (one allocation)
+  void* ws = nullptr;
+  float* logits = nullptr;
+  int32_t* ids = nullptr;
+  float* wts = nullptr;
+  int32_t* chunk_hist = nullptr;
+  int32_t* chunk_base = nullptr;
+  int32_t* counts = nullptr;
+  int32_t* offsets = nullptr;
+  int32_t* perm = nullptr;
+  int32_t* inv_perm = nullptr;
+  int32_t* seg_expert = nullptr;
+  int32_t* seg_start = nullptr;
+  int32_t* seg_count = nullptr;
+  int32_t* num_seg = nullptr;
+  uint32_t* ticket = nullptr;
+  uint32_t* err = nullptr;
+  __half* hbuf = nullptr;
+  float* ypart = nullptr;
+  __half* x_stage = nullptr;
+  __half* out_stage = nullptr;
+  int32_t* ids_stage = nullptr;
+  float* w_stage = nullptr;
+  int last_T = 0;
+  // prefill (tensor-core) path
+  int gemm_min_tokens = 256;
+  bool gemm_ok = false;         // shapes suit the GEMM (H, I multiples of 64)
+  moe::CodeMaps pool_maps = {};  // code sections of the caller's pool (full residency)
+  CUtensorMap h_map = {};        // h workspace rows
+  CUtensorMap x_map = {};        // tokens of the current forward
+  bool profiling = false;
+  cudaEvent_t ev[5] = {};
+  moe::Residency* res = nullptr;  // partial residency state
+  moe_layer_stats_t stats = {};
+};
+
+
+namespace moe {
+
+// Device pointers of an expert-segment list (see RouteArgs).
+struct SegPtrs {
+  const int32_t* num_seg;
+  const int32_t* seg_expert;
+  const int32_t* seg_start;
+  const int32_t* seg_count;
+};
+
+// Enqueue gate/up + down over the given segments (no combine).
+moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t s, const uint8_t* pool,
+                             const int32_t* e2s, int num_slots, const SegPtrs& seg, int max_seg,
+                             const CodeMaps* maps);
+// Encode the three code-section tensor maps of a slot pool.
+bool encode_pool_maps(const moe_layer* L, const uint8_t* pool, int num_slots, CodeMaps* maps);
+// Enqueue the weighted combine of the expert outputs into out.
+moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s);
+// Record the calling thread's error message; returns st.
+moe_status_t set_error(moe_status_t st, const char* fmt, ...);
+
+}  // namespace moe

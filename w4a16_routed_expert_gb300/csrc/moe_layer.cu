@@ -11,8 +11,7 @@
 #include <string>
 #include <unordered_map>
 
-#include "kernels.h"
-#include "moe_layer.h"
+#include "layer_internal.h"
 #include "residency.h"
 
 namespace {
@@ -33,72 +32,7 @@ moe_status_t cuda_fail(cudaError_t e, const char* what) {
   return fail(MOE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
-
-struct Layout {
-  size_t off[6];
-  size_t size[6];
-  size_t record;
-  size_t payload;
-};
-
-bool record_layout(int H, int I, int G, Layout* L) {
-  if (H <= 0 || I <= 0 || G <= 0 || (H % 2) || (I % 2)) return false;
-  const size_t gh = (size_t)(H + G - 1) / G, gi = (size_t)(I + G - 1) / G;
-  const size_t sizes[6] = {(size_t)I * H / 2, (size_t)I * H / 2, (size_t)H * I / 2,
-                           2 * (size_t)I * gh,  2 * (size_t)I * gh,  2 * (size_t)H * gi};
-  size_t cur = 0, payload = 0;
-  for (int i = 0; i < 6; ++i) {
-    cur = align256(cur);
-    L->off[i] = cur;
-    L->size[i] = sizes[i];
-    cur += sizes[i];
-    payload += sizes[i];
-  }
-  L->record = align256(cur);
-  L->payload = payload;
-  return true;
-}
-
 }  // namespace
-
-struct moe_layer {
-  moe_layer_config_t cfg;
-  moe_layer_weights_t w;
-  int device = 0;
-  int num_sms = 0;
-  Layout lay;
-  int n_records = 0;
-  bool pdl = true;
-  // workspace (one allocation)
-  void* ws = nullptr;
-  float* logits = nullptr;
-  int32_t* ids = nullptr;
-  float* wts = nullptr;
-  int32_t* chunk_hist = nullptr;
-  int32_t* chunk_base = nullptr;
-  int32_t* counts = nullptr;
-  int32_t* offsets = nullptr;
-  int32_t* perm = nullptr;
-  int32_t* inv_perm = nullptr;
-  int32_t* seg_expert = nullptr;
-  int32_t* seg_start = nullptr;
-  int32_t* seg_count = nullptr;
-  int32_t* num_seg = nullptr;
-  uint32_t* ticket = nullptr;
-  uint32_t* err = nullptr;
-  __half* hbuf = nullptr;
-  float* ypart = nullptr;
-  __half* x_stage = nullptr;
-  __half* out_stage = nullptr;
-  int32_t* ids_stage = nullptr;
-  float* w_stage = nullptr;
-  int last_T = 0;
-  bool profiling = false;
-  cudaEvent_t ev[5] = {};
-  moe::Residency* res = nullptr;  // partial residency state
-  moe_layer_stats_t stats = {};
-};
 
 namespace {
 
@@ -261,6 +195,16 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     delete L;
     return cuda_fail(e, "workspace init");
   }
+  {
+    const char* gm = getenv("MOE_GEMM_MIN_TOKENS");
+    if (gm) L->gemm_min_tokens = atoi(gm);
+    const int H = config->hidden, I = config->intermediate;
+    const size_t P = (size_t)config->max_tokens * (config->top_k + 1);
+    L->gemm_ok = (H % 64 == 0) && (I % 64 == 0) && P < (1u << 31) &&
+                 moe::encode_rows_map(&L->h_map, L->hbuf, I, (int)P, moe::gemm_tile_n());
+    if (L->gemm_ok && config->residency == MOE_RESIDENCY_FULL)
+      moe::encode_pool_maps(L, static_cast<const uint8_t*>(weights->slot_pool), config->num_slots, &L->pool_maps);
+  }
   if (config->residency == MOE_RESIDENCY_PARTIAL) {
     st = moe::residency_create(L->cfg, L->lay.record, L->n_records, weights->host_backing, &L->res);
     if (st != MOE_OK) {
@@ -283,22 +227,97 @@ moe_status_t moe_layer_destroy(moe_layer_t* layer) {
   return MOE_OK;
 }
 
+}  // extern "C"
+
 namespace {
 
-// Enqueue routing + experts + combine for one batch whose tokens are on the
-// device. pool/e2s/num_slots select the record table.
-moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s,
-                             const uint8_t* pool, const int32_t* e2s, int num_slots) {
-  const moe_layer_config_t& c = L->cfg;
-  const int H = c.hidden, I = c.intermediate, E = c.num_experts, k = c.top_k, G = c.group_size;
-  const int max_seg = std::min(E, T * k) + c.has_shared_expert;
+}  // namespace
 
-  const moe::GemvPlan pd = moe::plan_gemv(I, H, G, true, T);
-  const moe::GemvPlan ps = moe::plan_gemv(H, I, G, false, T);
-  if (!moe::gemv_plan_supported(pd) || !moe::gemv_plan_supported(ps))
+namespace moe {
+
+moe_status_t set_error(moe_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+// Gate/up + SwiGLU and down over the experts of the given segment list;
+// pool/e2s/num_slots select the record table.
+bool encode_pool_maps(const moe_layer* L, const uint8_t* pool, int num_slots, CodeMaps* maps) {
+  const int H = L->cfg.hidden, I = L->cfg.intermediate;
+  const size_t rb = L->lay.record;
+  maps->valid = encode_codes_map(&maps->gate, pool + L->lay.off[0], H, I, num_slots, rb) &&
+                encode_codes_map(&maps->up, pool + L->lay.off[1], H, I, num_slots, rb) &&
+                encode_codes_map(&maps->down, pool + L->lay.off[2], I, H, num_slots, rb);
+  return maps->valid;
+}
+
+namespace {
+
+// Tensor-core path: gate/up + SwiGLU GEMM, then the down GEMM.
+moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, const uint8_t* pool,
+                          const int32_t* e2s, int num_slots, const SegPtrs& seg, const CodeMaps* maps) {
+  const moe_layer_config_t& c = L->cfg;
+  const int H = c.hidden, I = c.intermediate, k = c.top_k, G = c.group_size;
+  if (!encode_rows_map(&L->x_map, x, H, T, 1)) return fail(MOE_ERR_CUDA, "token tensor map encoding failed");
+  GemmArgs ga = {};
+  ga.pool = pool;
+  ga.record_bytes = (long long)L->lay.record;
+  ga.expert_to_slot = e2s;
+  ga.num_slots = num_slots;
+  ga.s_off0 = L->lay.off[3];
+  ga.s_off1 = L->lay.off[4];
+  ga.N = I;
+  ga.K = H;
+  ga.G = G;
+  ga.ng = (H + G - 1) / G;
+  ga.num_seg = seg.num_seg;
+  ga.seg_expert = seg.seg_expert;
+  ga.seg_start = seg.seg_start;
+  ga.seg_count = seg.seg_count;
+  ga.perm = L->perm;
+  ga.Tk = T * k;
+  ga.k = k;
+  ga.h_out = L->hbuf;
+  ga.y_out = nullptr;
+  ga.err = L->err;
+  cudaError_t e = launch_gemm(true, maps->gate, maps->up, L->x_map, ga, L->num_sms, s, L->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[2], s, cudaEventRecordExternal);
+  GemmArgs gb = ga;
+  gb.s_off0 = L->lay.off[5];
+  gb.s_off1 = L->lay.off[5];
+  gb.N = H;
+  gb.K = I;
+  gb.ng = (I + G - 1) / G;
+  gb.h_out = nullptr;
+  gb.y_out = L->ypart;
+  e = launch_gemm(false, maps->down, maps->down, L->h_map, gb, L->num_sms, s, L->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[3], s, cudaEventRecordExternal);
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t s, const uint8_t* pool,
+                             const int32_t* e2s, int num_slots, const SegPtrs& seg, int max_seg,
+                             const CodeMaps* maps) {
+  const moe_layer_config_t& c = L->cfg;
+  const int H = c.hidden, I = c.intermediate, k = c.top_k, G = c.group_size;
+  if (L->gemm_ok && maps && maps->valid && T >= L->gemm_min_tokens)
+    return enqueue_gemm(L, x, T, s, pool, e2s, num_slots, seg, maps);
+
+  const GemvPlan pd = plan_gemv(I, H, G, true, T);
+  const GemvPlan ps = plan_gemv(H, I, G, false, T);
+  if (!gemv_plan_supported(pd) || !gemv_plan_supported(ps))
     return fail(MOE_ERR_UNSUPPORTED, "no GEMV variant for H=%d I=%d", H, I);
 
-  moe::GemvArgs gd = {};
+  GemvArgs gd = {};
   gd.pool = pool;
   gd.record_bytes = (long long)L->lay.record;
   gd.expert_to_slot = e2s;
@@ -313,10 +332,10 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, __half* out, 
   gd.ng = (H + G - 1) / G;
   gd.lpr = pd.lpr;
   gd.rb = pd.rb;
-  gd.num_seg = L->num_seg;
-  gd.seg_expert = L->seg_expert;
-  gd.seg_start = L->seg_start;
-  gd.seg_count = L->seg_count;
+  gd.num_seg = seg.num_seg;
+  gd.seg_expert = seg.seg_expert;
+  gd.seg_start = seg.seg_start;
+  gd.seg_count = seg.seg_count;
   gd.act = x;
   gd.act_gather = 1;
   gd.perm = L->perm;
@@ -329,11 +348,11 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, __half* out, 
   gd.err = L->err;
   const int nrb_d = (I + pd.rb - 1) / pd.rb;
   const int grid_d = std::max(1, std::min(L->num_sms, max_seg * nrb_d));
-  cudaError_t e = moe::launch_gemv(gd, true, pd, grid_d, s, L->pdl);
+  cudaError_t e = launch_gemv(gd, true, pd, grid_d, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[2], s, cudaEventRecordExternal);
 
-  moe::GemvArgs gs = gd;
+  GemvArgs gs = gd;
   gs.q_off0 = L->lay.off[2];
   gs.q_off1 = 0;
   gs.s_off0 = L->lay.off[5];
@@ -351,24 +370,32 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, __half* out, 
   gs.stage_bytes = ps.stage_bytes;
   const int nrb_s = (H + ps.rb - 1) / ps.rb;
   const int grid_s = std::max(1, std::min(L->num_sms, max_seg * nrb_s));
-  e = moe::launch_gemv(gs, false, ps, grid_s, s, L->pdl);
+  e = launch_gemv(gs, false, ps, grid_s, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[3], s, cudaEventRecordExternal);
+  return MOE_OK;
+}
 
-  moe::CombineArgs ca = {};
+moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s) {
+  const moe_layer_config_t& c = L->cfg;
+  CombineArgs ca = {};
   ca.ypart = L->ypart;
   ca.w = L->wts;
   ca.x = c.add_residual ? x : nullptr;
   ca.out = out;
   ca.T = T;
-  ca.H = H;
-  ca.k = k;
+  ca.H = c.hidden;
+  ca.k = c.top_k;
   ca.has_shared = c.has_shared_expert;
-  e = moe::launch_combine(ca, s, L->pdl);
+  cudaError_t e = launch_combine(ca, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
   return MOE_OK;
 }
+
+}  // namespace moe
+
+namespace {
 
 moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_user, float* w_user,
                            cudaStream_t s) {
@@ -410,6 +437,8 @@ moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_us
 
 }  // namespace
 
+extern "C" {
+
 moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, void* out, int32_t* topk_ids,
                                float* topk_w, void* stream) {
   if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");
@@ -429,8 +458,11 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
     return st;
   }
   if (layer->cfg.residency == MOE_RESIDENCY_FULL) {
-    st = enqueue_experts(layer, xh, T, oh, s, static_cast<const uint8_t*>(layer->w.slot_pool),
-                         layer->w.expert_to_slot, layer->cfg.num_slots);
+    const moe::SegPtrs seg = {layer->num_seg, layer->seg_expert, layer->seg_start, layer->seg_count};
+    const int max_seg = std::min(layer->cfg.num_experts, T * layer->cfg.top_k) + layer->cfg.has_shared_expert;
+    st = moe::enqueue_experts(layer, xh, T, s, static_cast<const uint8_t*>(layer->w.slot_pool),
+                              layer->w.expert_to_slot, layer->cfg.num_slots, seg, max_seg, &layer->pool_maps);
+    if (st == MOE_OK) st = moe::enqueue_combine(layer, xh, T, oh, s);
   } else {
     st = moe::residency_forward(layer->res, layer, xh, T, oh, s);
   }
@@ -554,18 +586,5 @@ cudaError_t ensure_smem_ptr(const void* kern, size_t bytes) {
   if (e == cudaSuccess) set_bytes[kern] = bytes;
   return e;
 }
-
-moe_status_t layer_enqueue_experts(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s,
-                                   const uint8_t* pool, const int32_t* e2s, int num_slots) {
-  return enqueue_experts(L, x, T, out, s, pool, e2s, num_slots);
-}
-
-const int32_t* layer_counts(const moe_layer* L) { return L->counts; }
-const moe_layer_config_t& layer_config(const moe_layer* L) { return L->cfg; }
-size_t layer_record_bytes(const moe_layer* L) { return L->lay.record; }
-int32_t* layer_num_seg(moe_layer* L) { return L->num_seg; }
-int32_t* layer_seg_expert(moe_layer* L) { return L->seg_expert; }
-int32_t* layer_seg_start(moe_layer* L) { return L->seg_start; }
-int32_t* layer_seg_count(moe_layer* L) { return L->seg_count; }
 
 }  // namespace moe
