@@ -177,7 +177,7 @@ def algorithmic(shape, T, eu):
         down=n_exp * down + pairs * I * 2 + pairs * H * 4,
         layer=n_exp * (gate_up + down) + E * H * 4 + 2 * T * H * 2,
     )
-    f = dict(layer=2 * T * H * E + pairs * 6 * H * I)
+    f = dict(layer=2 * T * H * E + pairs * 6 * H * I, gate_up=pairs * 4 * H * I, down=pairs * 2 * H * I)
     return b, f, dict(gate_up_per_expert=gate_up, down_per_expert=down)
 
 
@@ -318,21 +318,32 @@ def run_ours(args):
     b, f, per = algorithmic(shape, T, eu)
     kern = "gate_up" if stage[1] >= stage[2] else "down"
     kern_ms = stage[1] if kern == "gate_up" else stage[2]
-    achieved = b[kern] / (kern_ms / 1e3) / 1e9
+    tensor_path = T >= args.gemm_min_tokens and shape.hidden % 64 == 0 and shape.intermediate % 64 == 0
     traffic = None
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as ftr:
             tr = json.load(ftr)
+        src = "gemm.cu" if tensor_path else "gemv.cu"
         ent = tr.get(args.workload, {}).get(kern)
-        if ent and ent.get("source_sha") == source_hash("w4a16_routed_expert_gb300/csrc/gemv.cu"):
+        if ent and ent.get("source_sha") == source_hash(f"w4a16_routed_expert_gb300/csrc/{src}"):
             traffic = ent["dram_bytes_per_launch"]
     except Exception:
         traffic = None
-    roofline = {"bound": "hbm", "kernel": f"k_gemv ({kern.replace('_', '/')})", "achieved": achieved,
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "peak_source": peaks["source"], "traffic": traffic,
-                "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms,
-                "active_experts": eu}
+    if tensor_path:
+        achieved = f[kern] / (kern_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roofline = {"bound": "tensor", "kernel": f"k_gemm ({kern.replace('_', '/')})", "achieved": achieved,
+                    "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": peaks["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
+                    "traffic": traffic, "algorithmic_flops_per_launch": f[kern],
+                    "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms, "active_experts": eu}
+    else:
+        achieved = b[kern] / (kern_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "kernel": f"k_gemv ({kern.replace('_', '/')})", "achieved": achieved,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "peak_source": peaks["source"], "traffic": traffic,
+                    "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms,
+                    "active_experts": eu}
     layer_bytes_gbs = b["layer"] / (ms_per_step / 1e3) / 1e9
     layer_tflops = f["layer"] / (ms_per_step / 1e3) / 1e12
     layer_roof = {"bytes_per_step": b["layer"], "flops_per_step": f["layer"], "achieved_gbs": layer_bytes_gbs,
@@ -430,6 +441,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-min-tokens", type=int, default=256,
+                    help="batch size from which the library takes the tensor-core path (its default)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -194,39 +194,103 @@ __device__ void warp_segments(const RouteArgs& a, const int* s_counts, const int
 }
 
 // ------------------------------------------------------------ small path
-template <int NV>
-__global__ void __launch_bounds__(kRouteThreads) k_route_small(RouteArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_scan[33];
-  __shared__ int s_last;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = a.T, H = a.H, E = a.E, k = a.k;
-
-  pdl_wait();
-  __half* sx = reinterpret_cast<__half*>(smem);
-  {
-    const int nvec = T * H / 8;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    uint4* dst = reinterpret_cast<uint4*>(sx);
-    for (int i = tid; i < nvec; i += kRouteThreads) dst[i] = __ldg(src + i);
+// Single-warp finish for n = T*k <= 32 (token, rank) pairs: lane f holds pair
+// f; its sorted position is the number of pairs with a lower expert id, or
+// the same id and a lower flat index (a stable counting sort by rank). Also
+// writes the segment list and the per-expert counts / offsets (by binary
+// search over the sorted ids, all threads).
+__device__ void finish_tiny(const RouteArgs& a, int32_t* s_ids, int32_t* s_sorted, int* s_nseg) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n = a.T * a.k;
+  if (tid < 32) {
+    const int e = lane < n ? s_ids[lane] : 0x7fffffff;
+    int rank = 0;
+    for (int o = 0; o < n; ++o) {
+      const int eo = __shfl_sync(0xffffffffu, e, o);
+      rank += (eo < e || (eo == e && o < lane)) ? 1 : 0;
+    }
+    if (lane < n) {
+      a.perm[rank] = lane;
+      a.inv_perm[lane] = rank;
+      s_sorted[rank] = e;
+    }
+    __syncwarp();
+    const int se = lane < n ? s_sorted[lane] : -1;
+    const bool start = lane < n && (lane == 0 || s_sorted[lane - 1] != se);
+    const uint32_t mask = __ballot_sync(0xffffffffu, start);
+    if (start) {
+      const int idx = __popc(mask & lanemask_lt());
+      const uint32_t later = mask & ~((2u << lane) - 1u);
+      const int next = later ? (__ffs(later) - 1) : n;
+      a.seg_expert[idx] = se;
+      a.seg_start[idx] = lane;
+      a.seg_count[idx] = next - lane;
+    }
+    if (lane == 0) {
+      int ns = __popc(mask);
+      if (a.has_shared) {
+        a.seg_expert[ns] = a.E;
+        a.seg_start[ns] = n;
+        a.seg_count[ns] = a.T;
+        ++ns;
+      }
+      *a.num_seg = ns;
+      *s_nseg = ns;
+    }
   }
   __syncthreads();
+  // offsets[e] = number of pairs with expert < e
+  for (int e = tid; e <= a.E; e += blockDim.x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_sorted[mid] < e)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    a.offsets[e] = lo;
+    s_ids[32 + e] = lo;  // scratch copy for the counts
+  }
+  __syncthreads();
+  for (int e = tid; e < a.E; e += blockDim.x) a.counts[e] = s_ids[32 + e + 1] - s_ids[32 + e];
+}
 
-  const int e = blockIdx.x * (kRouteThreads / 32) + warp;
-  if (e < E) {
-    float acc[kSmallRouteMaxT];
+// Router logits for T <= kSmallRouteMaxT tokens: each CTA (4 warps) owns EPC
+// experts; a warp covers 1/(4/EPC) of an expert row, FP32 FMA from the FP32
+// router row and FP16 tokens, lane partials reduced by shuffles and shared
+// memory. The last CTA to finish (atomic ticket, no spinning) runs top-k and
+// the permutation for the whole batch.
+template <int NV, int EPC>
+__global__ void __launch_bounds__(128) k_route_small(RouteArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ float s_part[4][kSmallRouteMaxT];
+  __shared__ int s_scan[33];
+  __shared__ int s_last;
+  __shared__ int s_nseg;
+  constexpr int WPE = 4 / EPC;  // warps per expert
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.T, H = a.H, E = a.E, k = a.k;
+  pdl_wait();
+
+  const int e = blockIdx.x * EPC + warp / WPE;
+  const int part = warp % WPE;
+  float acc[kSmallRouteMaxT];
 #pragma unroll
-    for (int t = 0; t < kSmallRouteMaxT; ++t) acc[t] = 0.f;
-    const float4* wr4 = reinterpret_cast<const float4*>(a.wr + (size_t)e * H);
+  for (int t = 0; t < kSmallRouteMaxT; ++t) acc[t] = 0.f;
+  if (e < E) {
+    const int span = H / WPE;  // multiple of 4 * 32 / 4 ... H % 128 == 0
+    const float4* wr4 = reinterpret_cast<const float4*>(a.wr + (size_t)e * H + part * span);
+    const uint2* x2 = reinterpret_cast<const uint2*>(a.x + part * span);
 #pragma unroll 4
-    for (int h4 = lane; h4 < H / 4; h4 += 32) {
+    for (int h4 = lane; h4 < span / 4; h4 += 32) {
       const float4 wv = __ldg(wr4 + h4);
 #pragma unroll
       for (int t = 0; t < kSmallRouteMaxT; ++t) {
         if (t < T) {
-          const __half2* xp = reinterpret_cast<const __half2*>(sx + (size_t)t * H + 4 * h4);
-          const float2 x01 = __half22float2(xp[0]);
-          const float2 x23 = __half22float2(xp[1]);
+          const uint2 raw = __ldg(x2 + (size_t)t * (H / 4) + h4);
+          const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+          const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
           acc[t] = fmaf(wv.x, x01.x, acc[t]);
           acc[t] = fmaf(wv.y, x01.y, acc[t]);
           acc[t] = fmaf(wv.z, x23.x, acc[t]);
@@ -234,17 +298,26 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_small(RouteArgs a) {
         }
       }
     }
-    const float b = a.bias ? __ldg(a.bias + e) : 0.f;
+  }
 #pragma unroll
-    for (int t = 0; t < kSmallRouteMaxT; ++t) {
-      if (t < T) {
-        const float s = warp_sum(acc[t]);
-        if (lane == 0) a.logits[(size_t)t * E + e] = s + b;
-      }
+  for (int t = 0; t < kSmallRouteMaxT; ++t)
+    if (t < T) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0) s_part[warp][t] = v;
+    }
+  __syncthreads();
+  if (tid < EPC * T) {
+    const int ee = tid / T, t = tid % T;
+    const int eg = blockIdx.x * EPC + ee;
+    if (eg < E) {
+      float v = 0.f;
+#pragma unroll
+      for (int p = 0; p < WPE; ++p) v += s_part[ee * WPE + p][t];
+      a.logits[(size_t)t * E + eg] = v + (a.bias ? __ldg(a.bias + eg) : 0.f);
     }
   }
 
-  // The last CTA to finish its logits runs the rest of the routing.
+  // the last CTA to finish its logits runs the rest of the routing
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
@@ -252,34 +325,40 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_small(RouteArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  // shared memory reuse: ids [T*k], counts [E], offsets [E+1], cursor [E+1]
-  int32_t* s_ids = reinterpret_cast<int32_t*>(smem);
-  int* s_counts = s_ids + T * k;
-  int* s_off = s_counts + E;
-  int* s_cur = s_off + E + 1;
-  __syncthreads();
-  for (int t = warp; t < T; t += kRouteThreads / 32) warp_softmax_topk<NV>(a, t, s_ids + t * k);
-  for (int i = tid; i < E; i += kRouteThreads) s_counts[i] = 0;
-  __syncthreads();
-  for (int f = tid; f < T * k; f += kRouteThreads) atomicAdd(&s_counts[s_ids[f]], 1);
-  __syncthreads();
-  for (int i = tid; i < E; i += kRouteThreads) {
-    s_off[i] = s_counts[i];
-    a.counts[i] = s_counts[i];
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem);  // [T*k] (+ scratch)
+  if (T * k <= 32) {
+    int32_t* s_sorted = s_ids + 32 + E + 1;
+    if (warp == 0)
+      for (int t = 0; t < T; ++t) warp_softmax_topk<NV>(a, t, s_ids + t * k);
+    __syncthreads();
+    finish_tiny(a, s_ids, s_sorted, &s_nseg);
+  } else {
+    int* s_counts = s_ids + T * k;
+    int* s_off = s_counts + E;
+    int* s_cur = s_off + E + 1;
+    for (int t = warp; t < T; t += 4) warp_softmax_topk<NV>(a, t, s_ids + t * k);
+    for (int i = tid; i < E; i += 128) s_counts[i] = 0;
+    __syncthreads();
+    for (int f = tid; f < T * k; f += 128) atomicAdd(&s_counts[s_ids[f]], 1);
+    __syncthreads();
+    for (int i = tid; i < E; i += 128) {
+      s_off[i] = s_counts[i];
+      a.counts[i] = s_counts[i];
+    }
+    __syncthreads();
+    block_exclusive_scan(s_off, E, s_scan);
+    for (int i = tid; i < E; i += 128) {
+      s_cur[i] = s_off[i];
+      a.offsets[i] = s_off[i];
+    }
+    if (tid == 0) {
+      s_off[E] = T * k;
+      a.offsets[E] = T * k;
+    }
+    __syncthreads();
+    if (warp == 0) warp_stable_scatter(a, s_ids, 0, T * k, s_cur);
+    if (warp == 1) warp_segments(a, s_counts, s_off);
   }
-  __syncthreads();
-  block_exclusive_scan(s_off, E, s_scan);
-  for (int i = tid; i < E; i += kRouteThreads) {
-    s_cur[i] = s_off[i];
-    a.offsets[i] = s_off[i];
-  }
-  if (tid == 0) {
-    s_off[E] = T * k;
-    a.offsets[E] = T * k;
-  }
-  __syncthreads();
-  if (warp == 0) warp_stable_scatter(a, s_ids, 0, T * k, s_cur);
-  if (warp == 1) warp_segments(a, s_counts, s_off);
   if (tid == 0) *a.ticket = 0u;
 }
 
@@ -432,13 +511,18 @@ __global__ void __launch_bounds__(32) k_scatter(RouteArgs a) {
 
 template <int NV>
 cudaError_t launch_route_small_nv(const RouteArgs& a, cudaStream_t s, bool pdl) {
-  const int grid = (a.E + 7) / 8;
-  const size_t xbytes = (size_t)a.T * a.H * sizeof(__half);
-  const size_t fbytes = ((size_t)a.T * a.k + 3 * (size_t)a.E + 2) * sizeof(int);
-  const size_t smem = xbytes > fbytes ? xbytes : fbytes;
-  cudaError_t e = ensure_smem(k_route_small<NV>, smem);
-  if (e != cudaSuccess) return e;
-  return launch_ex(k_route_small<NV>, dim3(grid), dim3(kRouteThreads), smem, s, pdl, a);
+  // one expert per CTA up to 128 experts, then 2 or 4 per CTA
+  const size_t fbytes = ((size_t)a.T * a.k + 3 * (size_t)a.E + 64) * sizeof(int);
+  if (a.E <= 128) {
+    ensure_smem(k_route_small<NV, 1>, fbytes);
+    return launch_ex(k_route_small<NV, 1>, dim3(a.E), dim3(128), fbytes, s, pdl, a);
+  }
+  if (a.E <= 256) {
+    ensure_smem(k_route_small<NV, 2>, fbytes);
+    return launch_ex(k_route_small<NV, 2>, dim3((a.E + 1) / 2), dim3(128), fbytes, s, pdl, a);
+  }
+  ensure_smem(k_route_small<NV, 4>, fbytes);
+  return launch_ex(k_route_small<NV, 4>, dim3((a.E + 3) / 4), dim3(128), fbytes, s, pdl, a);
 }
 
 template <int NV>
