@@ -192,6 +192,28 @@ moe_status_t moe_layer_get_stats(const moe_layer_t* layer, moe_layer_stats_t* st
  * forward has completed. */
 moe_status_t moe_layer_destroy(moe_layer_t* layer);
 
+/* Routing without any device allocation, for callers that must not allocate
+ * device memory (a host runtime that owns every device byte and forbids
+ * allocation after start-up, a fixed-arena process, a plug-in handed only
+ * input and output buffers). The pages describe no such entry point; it is
+ * this library's addition. It runs the small-batch routing kernel (FP32
+ * logits, softmax over all E, top-k with ties to the lower id, weights) with
+ * its scratch in a static device array of 192 KiB that every GPU loading the
+ * library keeps until exit.
+ *   x          device FP16 [T][H]; router_w device FP32 [E][H];
+ *   router_bias device FP32 [E] or NULL; renormalize 0 or 1
+ *   topk_ids   device int32 [T][k] (rank order); topk_w device FP32 [T][k]
+ * Limits: 0 <= T <= 16, 1 <= E <= 1024, 1 <= k <= min(32, E), H a multiple
+ * of 32 in 128..4096; anything else returns MOE_ERR_INVALID_ARG with a
+ * message. The first call on a device (with that device current) looks up
+ * the scratch array's address and caches it: make that first call before any
+ * stream capture. All calls share the array and it keeps the last call's
+ * contents; calls that overlap on the GPU race. Asynchronous on `stream`;
+ * results are valid once it is synchronised. Calls no allocating routine. */
+moe_status_t moe_route_topk_static(const void* x, int32_t T, int32_t H, const float* router_w,
+                                   const float* router_bias, int32_t E, int32_t k, int32_t renormalize,
+                                   int32_t* topk_ids, float* topk_w, void* stream);
+
 /* Message of the calling thread's last failed call ("" if none). The pointer
  * stays valid until the thread's next call into the library. */
 const char* moe_layer_last_error(void);

@@ -78,6 +78,7 @@ PROTOTYPES = {
     "moe_layer_get_profile": (_I32, [_P, ctypes.POINTER(moe_layer_profile_t)]),
     "moe_layer_destroy": (_I32, [_P]),
     "moe_layer_last_error": (ctypes.c_char_p, []),
+    "moe_route_topk_static": (_I32, [_P, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
     # include/moe_residency.h
     "moe_slot_planner_create": (_P, [_I32, _I32]),
     "moe_slot_planner_plan": (_I32, [_P, ctypes.POINTER(_I32), _I32, _I32, ctypes.POINTER(_I32),
