@@ -124,6 +124,7 @@ typedef struct {
   float total_ms;         /* whole forward */
   int32_t active_experts; /* distinct routed experts selected (E_u) */
   int32_t tokens;         /* T of the profiled forward */
+  int32_t single_launch;  /* 1: the forward ran as one kernel (stage times are 0, total_ms is the kernel) */
 } moe_layer_profile_t;
 
 /* ABI version of the loaded library (MOE_ABI_VERSION of its build). */

@@ -48,7 +48,7 @@ class moe_layer_stats_t(ctypes.Structure):
 class moe_layer_profile_t(ctypes.Structure):
     _fields_ = [("route_ms", ctypes.c_float), ("gate_up_ms", ctypes.c_float), ("down_ms", ctypes.c_float),
                 ("combine_ms", ctypes.c_float), ("total_ms", ctypes.c_float),
-                ("active_experts", ctypes.c_int32), ("tokens", ctypes.c_int32)]
+                ("active_experts", ctypes.c_int32), ("tokens", ctypes.c_int32), ("single_launch", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):

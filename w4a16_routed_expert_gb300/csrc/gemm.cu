@@ -4,10 +4,12 @@
 // in GPU memory and run with FP16 activations; here a weight tile is expanded
 // to FP16 only inside shared memory, for the MMAs that consume it.
 //
-// Tile = 128 weight rows x 128 tokens of one expert segment; the weights are
-// the MMA's A operand (M = 128) and the tokens its B operand (N = 128), so
-// each dequantised weight tile serves 128 tokens and the accumulator's TMEM
-// lane is the output unit, its column the token.
+// Tile = 128 MMA rows x 256 tokens of one expert segment. The weights are
+// the MMA's A operand (M = 128) and the tokens its B operand (N = 256), so
+// each dequantised weight row serves 256 tokens; the accumulator's TMEM lane
+// is the output unit, its column the token. Gate/up tiles interleave the two
+// matrices in M: row 2u is gate unit i0+u, row 2u+1 is up unit i0+u (64 units
+// per tile), so SwiGLU pairs sit in adjacent lanes and meet with one shuffle.
 //
 // Warp roles of a persistent CTA (one per SM):
 //   warp 0      TMA producer: INT4 code tiles (3-D tensor map over the slot
@@ -35,8 +37,8 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128;  // weight rows per tile
-constexpr int BN = 128;  // tokens per tile
+constexpr int BM = 128;  // MMA rows per tile (DUAL: 64 gate + 64 up, interleaved)
+constexpr int BN = 256;  // tokens per tile
 constexpr int BK = 64;   // K per pipeline step (128 bytes of FP16)
 constexpr int kCodeStages = 4;
 constexpr int kAStages = 3;
@@ -52,22 +54,22 @@ constexpr int kMaxSeg = 1025;
 
 template <bool DUAL>
 struct Smem {
-  static constexpr int mats = DUAL ? 2 : 1;
-  static constexpr uint32_t a_tile = BM * BK * 2;
-  static constexpr uint32_t b_tile = BN * BK * 2;
-  static constexpr uint32_t code_tile = BM * BK / 2;
+  static constexpr uint32_t a_tile = BM * BK * 2;      // 16 KB
+  static constexpr uint32_t b_tile = BN * BK * 2;      // 32 KB
+  static constexpr uint32_t code_tile = BM * BK / 2;   // 4 KB (DUAL: 64 gate rows then 64 up rows)
   static constexpr uint32_t off_a = 0;
-  static constexpr uint32_t off_b = off_a + kAStages * mats * a_tile;
+  static constexpr uint32_t off_b = off_a + kAStages * a_tile;
   static constexpr uint32_t off_codes = off_b + kBStages * b_tile;
-  static constexpr uint32_t off_bar = off_codes + kCodeStages * mats * code_tile;
+  static constexpr uint32_t off_bar = off_codes + kCodeStages * code_tile;
   // codes_full/empty, a_full/empty, b_full/empty, acc_full/empty, drain
   static constexpr uint32_t n_bars = 2 * kCodeStages + 2 * kAStages + 2 * kBStages + 4 + 1;
   static constexpr uint32_t off_misc = off_bar + n_bars * 8;
   static constexpr uint32_t off_prefix = off_misc + 64;
   static constexpr uint32_t bytes = off_prefix + (kMaxSeg + 1) * 4;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
-  static constexpr uint32_t tmem_cols = DUAL ? 512 : 256;
-  static constexpr uint32_t acc_stride = DUAL ? 256 : 128;
+  static constexpr uint32_t tmem_cols = 512;
+  static constexpr uint32_t acc_stride = BN;        // two accumulator buffers of 256 columns
+  static constexpr int units = DUAL ? BM / 2 : BM;  // output units per tile
 };
 
 struct Bars {
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   // tile prefix over the segments (segment s has m_tiles * ceil(count/BN) tiles)
   const int nseg = min(*a.num_seg, kMaxSeg);
-  const int m_tiles = (a.N + BM - 1) / BM;
+  const int m_tiles = (a.N + L::units - 1) / L::units;
   if (warp == 0) {
     int run = 0;
     for (int base = 0; base < nseg; base += 32) {
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int local = t - prefix[s];
       const int cnt = a.seg_count[s];
       const int ntl = (cnt + BN - 1) / BN;
-      const int m0 = (local / ntl) * BM, n0 = (local % ntl) * BN;
+      const int m0 = (local / ntl) * L::units, n0 = (local % ntl) * BN;
       const int e = a.seg_expert[s];
       int slot = a.expert_to_slot[e];
       if (slot < 0 || slot >= a.num_slots) {
@@ -228,11 +230,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         slot = 0;
       }
       const int pos0 = a.seg_start[s];
-      int rows[4] = {0, 0, 0, 0};
+      int rows[8] = {0, 0, 0, 0, 0, 0, 0, 0};
       if (DUAL) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int tok = min(n0 + 4 * lane + i, cnt - 1);
+        for (int i = 0; i < 8; ++i) {
+          const int tok = min(n0 + 8 * lane + i, cnt - 1);
           const int p = pos0 + tok;
           rows[i] = (p < a.Tk) ? (__ldg(a.perm + p) / a.k) : (p - a.Tk);
         }
@@ -243,10 +245,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
           good = mbar_wait(&B.codes_empty[sc], ((g / kCodeStages) & 1u) ^ 1u, abort_flag, a.err);
           if (good) {
-            unsigned char* cdst = smem + L::off_codes + (uint32_t)sc * L::mats * L::code_tile;
-            mbar_arrive_expect_tx(&B.codes_full[sc], L::mats * L::code_tile);
+            unsigned char* cdst = smem + L::off_codes + (uint32_t)sc * L::code_tile;
+            mbar_arrive_expect_tx(&B.codes_full[sc], L::code_tile);
             tma_load_3d(cdst, &tm_codes0, kk * (BK / 2), m0, slot, &B.codes_full[sc]);
-            if (DUAL) tma_load_3d(cdst + L::code_tile, &tm_codes1, kk * (BK / 2), m0, slot, &B.codes_full[sc]);
+            if (DUAL) tma_load_3d(cdst + L::code_tile / 2, &tm_codes1, kk * (BK / 2), m0, slot, &B.codes_full[sc]);
             misc->codes_issued = (int)g + 1;
             good = mbar_wait(&B.b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err);
             if (good) mbar_arrive_expect_tx(&B.b_full[sb], L::b_tile);
@@ -259,7 +261,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         unsigned char* bdst = smem + L::off_b + (uint32_t)sb * L::b_tile;
         if (DUAL) {
-          tma_gather4(bdst + lane * 4 * (BK * 2), &tm_act, kk * BK, rows[0], rows[1], rows[2], rows[3], &B.b_full[sb]);
+          unsigned char* d0 = bdst + lane * 8 * (BK * 2);
+          tma_gather4(d0, &tm_act, kk * BK, rows[0], rows[1], rows[2], rows[3], &B.b_full[sb]);
+          tma_gather4(d0 + 4 * (BK * 2), &tm_act, kk * BK, rows[4], rows[5], rows[6], rows[7], &B.b_full[sb]);
         } else if (lane == 0) {
           tma_load_2d(bdst, &tm_act, kk * BK, pos0 + n0, &B.b_full[sb]);
         }
@@ -287,14 +291,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + L::off_a + (uint32_t)sa * L::mats * L::a_tile);
+          const uint32_t a0 = smem_u32(smem + L::off_a + (uint32_t)sa * L::a_tile);
           const uint32_t bb = smem_u32(smem + L::off_b + (uint32_t)sb * L::b_tile);
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             const uint32_t acc = (kk > 0 || k16 > 0) ? 1u : 0u;
-            const uint64_t bdesc = smem_desc_sw128(bb + k16 * 32);
-            mma_f16(d0, smem_desc_sw128(a0 + k16 * 32), bdesc, idesc, acc);
-            if (DUAL) mma_f16(d0 + 128, smem_desc_sw128(a0 + L::a_tile + k16 * 32), bdesc, idesc, acc);
+            mma_f16(d0, smem_desc_sw128(a0 + k16 * 32), smem_desc_sw128(bb + k16 * 32), idesc, acc);
           }
           misc->mma_issued = 1;
           mma_commit(&B.a_empty[sa]);
@@ -308,6 +310,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ------------------------------------------------------------ dequant
     const int dt = tid - kWarpDequant0 * 32;
     const int r = dt >> 1, hsel = dt & 1;
+    // A row r: DUAL -> unit r/2 of the gate (even r) or up (odd r) matrix,
+    // codes row r/2 or 64 + r/2 of the stage; single -> row r.
+    const int unit = DUAL ? (r >> 1) : r;
+    const bool upper = DUAL && (r & 1);
+    const int crow = DUAL ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
     uint32_t g = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -315,39 +322,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int local = t - prefix[s];
       const int cnt = a.seg_count[s];
       const int ntl = (cnt + BN - 1) / BN;
-      const int m0 = (local / ntl) * BM;
+      const int m0 = (local / ntl) * L::units;
       const int e = a.seg_expert[s];
       int slot = a.expert_to_slot[e];
       if (slot < 0 || slot >= a.num_slots) slot = 0;
-      const bool rvalid = m0 + r < a.N;
-      const __half* sp0 = reinterpret_cast<const __half*>(a.pool + (size_t)slot * a.record_bytes + a.s_off0) +
-                          (size_t)(m0 + r) * a.ng;
-      const __half* sp1 = reinterpret_cast<const __half*>(a.pool + (size_t)slot * a.record_bytes + a.s_off1) +
-                          (size_t)(m0 + r) * a.ng;
+      const bool rvalid = m0 + unit < a.N;
+      const __half* sp = reinterpret_cast<const __half*>(a.pool + (size_t)slot * a.record_bytes +
+                                                         (upper ? a.s_off1 : a.s_off0)) +
+                         (size_t)(m0 + unit) * a.ng;
+      // scales of K-step kk are loaded one step ahead (latency off the critical path)
+      __half sn = rvalid ? __ldg(sp) : __float2half(0.f);
       for (int kk = 0; kk < nK; ++kk, ++g) {
         const int sc = g % kCodeStages, sa = g % kAStages;
-        const int grp = (kk * BK) / a.G;
-        const __half s0 = rvalid ? __ldg(sp0 + grp) : __float2half(0.f);
-        const __half s1 = (DUAL && rvalid) ? __ldg(sp1 + grp) : __float2half(0.f);
-        if (!mbar_wait(&B.codes_full[sc], (g / kCodeStages) & 1u, abort_flag, a.err) ||
-            !mbar_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err)) {
+        const __half s0 = sn;
+        if (kk + 1 < nK && rvalid) sn = __ldg(sp + ((kk + 1) * BK) / a.G);
+        int good = 1;
+        if (lane == 0)
+          good = mbar_wait(&B.codes_full[sc], (g / kCodeStages) & 1u, abort_flag, a.err) &&
+                 mbar_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
           ok = false;
           break;
         }
-        const unsigned char* csrc = smem + L::off_codes + (uint32_t)sc * L::mats * L::code_tile;
-        unsigned char* adst = smem + L::off_a + (uint32_t)sa * L::mats * L::a_tile;
+        const unsigned char* csrc = smem + L::off_codes + (uint32_t)sc * L::code_tile;
+        unsigned char* rowp = smem + L::off_a + (uint32_t)sa * L::a_tile + r * (BK * 2);
+        const uint4 w = *reinterpret_cast<const uint4*>(csrc + crow * (BK / 2) + hsel * 16);
+        const __half2 s2 = __half2half2(s0);
+        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int mat = 0; mat < L::mats; ++mat) {
-          const uint4 w = *reinterpret_cast<const uint4*>(csrc + mat * L::code_tile + r * (BK / 2) + hsel * 16);
-          const __half2 s2 = __half2half2(mat == 0 ? s0 : s1);
-          const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-          unsigned char* rowp = adst + mat * L::a_tile + r * (BK * 2);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = hsel * 4 + i;  // 16-byte chunk (8 halves) of the 128-byte row
-            const uint4 v = dequant8(words[i], s2);
-            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = v;
-          }
+        for (int i = 0; i < 4; ++i) {
+          const int c = hsel * 4 + i;  // 16-byte chunk (8 halves) of the 128-byte row
+          *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = dequant8(words[i], s2);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -367,39 +373,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int local = t - prefix[s];
       const int cnt = a.seg_count[s];
       const int ntl = (cnt + BN - 1) / BN;
-      const int m0 = (local / ntl) * BM, n0 = (local % ntl) * BN;
+      const int m0 = (local / ntl) * L::units, n0 = (local % ntl) * BN;
       const int pos0 = a.seg_start[s];
       const int ab = j & 1;
-      if (!mbar_wait(&B.acc_full[ab], (uint32_t)(j >> 1) & 1u, abort_flag, a.err)) break;
+      int good = 1;
+      if (lane == 0) good = mbar_wait(&B.acc_full[ab], (uint32_t)(j >> 1) & 1u, abort_flag, a.err);
+      good = __shfl_sync(0xffffffffu, good, 0);
+      if (!good) break;
       tc_fence_after();
-      const int grow = m0 + row;
-      const bool rvalid = grow < a.N;
+      // DUAL: even lanes own gate unit row/2, odd lanes its up value
+      const int gunit = m0 + (DUAL ? (row >> 1) : row);
+      const bool rvalid = gunit < a.N;
       const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * L::acc_stride;
 #pragma unroll 1
       for (int cb = 0; cb < BN / 32; ++cb) {
-        uint32_t gv[32];
-        tmem_ld32(tacc + cb * 32, gv);
+        uint32_t v[32];
+        tmem_ld32(tacc + cb * 32, v);
+        tmem_ld_wait();
         if (DUAL) {
-          uint32_t uv[32];
-          tmem_ld32(tacc + 128 + cb * 32, uv);
-          tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
+            const float mine = __uint_as_float(v[c]);
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
             const int tok = n0 + cb * 32 + c;
-            if (rvalid && tok < cnt) {
-              const float h = silu_f(__uint_as_float(gv[c])) * __uint_as_float(uv[c]);
-              a.h_out[(size_t)(pos0 + tok) * a.N + grow] = __float2half_rn(h);
+            if (!(lane & 1) && rvalid && tok < cnt) {
+              const float h = silu_f(mine) * other;
+              a.h_out[(size_t)(pos0 + tok) * a.N + gunit] = __float2half_rn(h);
             }
           }
         } else {
-          tmem_ld_wait();
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const int tok = n0 + cb * 32 + c;
             if (rvalid && tok < cnt) {
               const int pos = pos0 + tok;
               const int f = (pos < a.Tk) ? __ldg(a.perm + pos) : pos;
-              a.y_out[(size_t)f * a.N + grow] = __uint_as_float(gv[c]);
+              a.y_out[(size_t)f * a.N + gunit] = __uint_as_float(v[c]);
             }
           }
         }
@@ -464,12 +473,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes) {
+bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes,
+                      int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)N, (cuuint64_t)num_slots};
   const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)record_bytes};
-  const cuuint32_t box[3] = {BK / 2, BM, 1};
+  const cuuint32_t box[3] = {BK / 2, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool_section), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,

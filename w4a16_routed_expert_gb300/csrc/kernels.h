@@ -12,7 +12,7 @@
 namespace moe {
 
 // Tokens per routing chunk of the multi-CTA routing path.
-constexpr int kRouteChunkTokens = 64;
+constexpr int kRouteChunkTokens = 32;
 // Largest T handled by the fused single-launch routing kernel.
 constexpr int kSmallRouteMaxT = 16;
 
@@ -93,6 +93,19 @@ struct GemmArgs {
   uint32_t* err;
 };
 
+// Whole-layer decode megakernel (T <= kSmallRouteMaxT, full residency).
+struct DecodeArgs {
+  RouteArgs r;           // routing inputs and global outputs
+  GemvArgs g;            // gate/up items (segment pointers are replaced in-kernel)
+  GemvArgs d;            // down items
+  __half* out;           // [T][H]
+  const __half* x_res;   // residual input or nullptr
+  int has_shared;
+  uint32_t* ctr;         // zeroed counters: logits_done, final ticket, done_gu[E+1], done_dn[]
+  int stages;
+  uint32_t slot_bytes;   // ring slot size (max of the two item layouts)
+};
+
 // Tensor maps of the three code sections of a slot pool.
 struct CodeMaps {
   CUtensorMap gate, up, down;
@@ -152,10 +165,14 @@ int gemv_kch(int K, int lpr);
 int gemv_lanes_per_row(int K);
 size_t gemv_smem_bytes(int stages, uint32_t stage_bytes);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
+size_t decode_smem_bytes(int stages, uint32_t slot_bytes);
+bool decode_supported(int kg, int ntg, int kd, int ntd);
+cudaError_t launch_decode(const DecodeArgs& a, int kg, int ntg, int kd, int ntd, int grid, cudaStream_t s);
 cudaError_t launch_gemm(bool dual, const CUtensorMap& codes0, const CUtensorMap& codes1, const CUtensorMap& act,
                         const GemmArgs& a, int grid, cudaStream_t s, bool pdl);
 size_t gemm_smem_bytes(bool dual);
-bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes);
+bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes,
+                      int box_rows);
 bool encode_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, int box_rows);
 int gemm_tile_n();
 int gemm_tile_k();

@@ -73,6 +73,9 @@ struct moe_layer {
   int32_t* ids_stage = nullptr;
   float* w_stage = nullptr;
   int last_T = 0;
+  bool megakernel = true;        // single-launch decode for T <= 16 (full residency)
+  bool last_single = false;      // the last profiled forward was one launch
+  uint32_t* ctr = nullptr;       // megakernel counters (zero between launches)
   // prefill (tensor-core) path
   int gemm_min_tokens = 256;
   bool gemm_ok = false;         // shapes suit the GEMM (H, I multiples of 64)
@@ -102,6 +105,9 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
                              const CodeMaps* maps);
 // Encode the three code-section tensor maps of a slot pool.
 bool encode_pool_maps(const moe_layer* L, const uint8_t* pool, int num_slots, CodeMaps* maps);
+// Single-launch decode; MOE_ERR_UNSUPPORTED when no variant fits the shapes.
+moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, int32_t* ids_user, float* w_user,
+                            cudaStream_t s);
 // Enqueue the weighted combine of the expert outputs into out.
 moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s);
 // Record the calling thread's error message; returns st.

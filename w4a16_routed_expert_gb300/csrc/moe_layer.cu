@@ -104,6 +104,7 @@ size_t workspace_bytes(const moe_layer_config_t& c) {
   b += align256(P * H * 4);             // ypart
   b += 2 * align256(T * H * 2);         // x/out staging
   b += align256(T * k * 4) * 2;         // ids/w staging
+  b += align256(2048 * 4);              // megakernel counters
   return b;
 }
 
@@ -145,6 +146,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
   L->n_records = config->num_experts + config->has_shared_expert;
   const char* pdl_env = getenv("MOE_PDL");
   L->pdl = !(pdl_env && pdl_env[0] == '0');
+  const char* mk_env = getenv("MOE_MEGAKERNEL");
+  L->megakernel = !(mk_env && mk_env[0] == '0');
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
   if (e != cudaSuccess) {
@@ -186,9 +189,11 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     L->out_stage = carve<__half>(p, T * H);
     L->ids_stage = carve<int32_t>(p, T * k);
     L->w_stage = carve<float>(p, T * k);
+    L->ctr = carve<uint32_t>(p, 2048);
   }
   // zero the small control words (ticket, error word, segment count)
   e = cudaMemset(L->num_seg, 0, 4 * 256);
+  if (e == cudaSuccess) e = cudaMemset(L->ctr, 0, 2048 * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(L->ws);
@@ -250,9 +255,10 @@ moe_status_t set_error(moe_status_t st, const char* fmt, ...) {
 bool encode_pool_maps(const moe_layer* L, const uint8_t* pool, int num_slots, CodeMaps* maps) {
   const int H = L->cfg.hidden, I = L->cfg.intermediate;
   const size_t rb = L->lay.record;
-  maps->valid = encode_codes_map(&maps->gate, pool + L->lay.off[0], H, I, num_slots, rb) &&
-                encode_codes_map(&maps->up, pool + L->lay.off[1], H, I, num_slots, rb) &&
-                encode_codes_map(&maps->down, pool + L->lay.off[2], I, H, num_slots, rb);
+  // gate/up tiles take 64 rows of each matrix, down tiles 128 rows
+  maps->valid = encode_codes_map(&maps->gate, pool + L->lay.off[0], H, I, num_slots, rb, 64) &&
+                encode_codes_map(&maps->up, pool + L->lay.off[1], H, I, num_slots, rb, 64) &&
+                encode_codes_map(&maps->down, pool + L->lay.off[2], I, H, num_slots, rb, 128);
   return maps->valid;
 }
 
@@ -376,6 +382,94 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   return MOE_OK;
 }
 
+// Single-launch decode (routing, experts, combine) for T <= kSmallRouteMaxT.
+// Returns MOE_ERR_UNSUPPORTED (without launching) when the shapes have no
+// megakernel variant, so the caller takes the multi-kernel path.
+moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, int32_t* ids_user, float* w_user,
+                            cudaStream_t s) {
+  const moe_layer_config_t& c = L->cfg;
+  const int H = c.hidden, I = c.intermediate, E = c.num_experts, k = c.top_k, G = c.group_size;
+  const GemvPlan pg = plan_gemv(I, H, G, true, T);
+  const GemvPlan pd = plan_gemv(H, I, G, false, T);
+  if (!decode_supported(pg.kch, pg.nt, pd.kch, pd.nt) || (H + pd.rb - 1) / pd.rb > 2048 - 2 - (E + 1))
+    return MOE_ERR_UNSUPPORTED;
+  DecodeArgs a = {};
+  RouteArgs& r = a.r;
+  r.x = x;
+  r.wr = L->w.router_w;
+  r.bias = L->w.router_bias;
+  r.T = T;
+  r.H = H;
+  r.E = E;
+  r.k = k;
+  r.renorm = c.renormalize;
+  r.has_shared = c.has_shared_expert;
+  r.logits = L->logits;
+  r.ids = L->ids;
+  r.w = L->wts;
+  r.ids_user = ids_user;
+  r.w_user = w_user;
+  r.counts = L->counts;
+  r.offsets = L->offsets;
+  r.perm = L->perm;
+  r.inv_perm = L->inv_perm;
+  r.seg_expert = L->seg_expert;
+  r.seg_start = L->seg_start;
+  r.seg_count = L->seg_count;
+  r.num_seg = L->num_seg;
+  r.err = L->err;
+  GemvArgs& g = a.g;
+  g.pool = static_cast<const uint8_t*>(L->w.slot_pool);
+  g.record_bytes = (long long)L->lay.record;
+  g.expert_to_slot = L->w.expert_to_slot;
+  g.num_slots = c.num_slots;
+  g.q_off0 = L->lay.off[0];
+  g.q_off1 = L->lay.off[1];
+  g.s_off0 = L->lay.off[3];
+  g.s_off1 = L->lay.off[4];
+  g.N = I;
+  g.K = H;
+  g.G = G;
+  g.ng = (H + G - 1) / G;
+  g.lpr = pg.lpr;
+  g.rb = pg.rb;
+  g.act = x;
+  g.act_gather = 1;
+  g.Tk = T * k;
+  g.k = k;
+  g.h_out = L->hbuf;
+  g.err = L->err;
+  GemvArgs& d = a.d;
+  d = g;
+  d.q_off0 = L->lay.off[2];
+  d.q_off1 = 0;
+  d.s_off0 = L->lay.off[5];
+  d.s_off1 = 0;
+  d.N = H;
+  d.K = I;
+  d.ng = (I + G - 1) / G;
+  d.lpr = pd.lpr;
+  d.rb = pd.rb;
+  d.act = L->hbuf;
+  d.act_gather = 0;
+  d.h_out = nullptr;
+  d.y_out = L->ypart;
+  a.out = out;
+  a.x_res = c.add_residual ? x : nullptr;
+  a.has_shared = c.has_shared_expert;
+  a.ctr = L->ctr;
+  a.slot_bytes = std::max(pg.stage_bytes, pd.stage_bytes);
+  const size_t budget = 227 * 1024 - decode_smem_bytes(0, 0);
+  a.stages = (int)std::min<size_t>(8, budget / a.slot_bytes);
+  if (a.stages < 2) return MOE_ERR_UNSUPPORTED;
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
+  cudaError_t e = launch_decode(a, pg.kch, pg.nt, pd.kch, pd.nt, L->num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
+  L->last_single = true;
+  return MOE_OK;
+}
+
 moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s) {
   const moe_layer_config_t& c = L->cfg;
   CombineArgs ca = {};
@@ -429,6 +523,7 @@ moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_us
   ra.err = L->err;
   const bool small = T <= moe::kSmallRouteMaxT && (size_t)T * c.hidden * 2 <= 200 * 1024;
   if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
+  L->last_single = false;
   cudaError_t e = small ? moe::launch_route_small(ra, s, L->pdl) : moe::launch_route_large(ra, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "routing launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[1], s, cudaEventRecordExternal);
@@ -452,6 +547,17 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
   // programmatic dependent launch only on explicitly created streams
   const bool pdl_saved = layer->pdl;
   if (s == nullptr) layer->pdl = false;
+  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->megakernel && T <= moe::kSmallRouteMaxT) {
+    moe_status_t sd = moe::enqueue_decode(layer, xh, T, oh, topk_ids, topk_w, s);
+    if (sd != MOE_ERR_UNSUPPORTED) {
+      layer->pdl = pdl_saved;
+      if (sd != MOE_OK) return sd;
+      layer->last_T = T;
+      layer->stats.forward_calls += 1;
+      layer->stats.tokens += (uint64_t)T;
+      return MOE_OK;
+    }
+  }
   moe_status_t st = enqueue_route(layer, xh, T, topk_ids, topk_w, s);
   if (st != MOE_OK) {
     layer->pdl = pdl_saved;
@@ -545,7 +651,8 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* p) {
   if (!layer->ev[0]) return fail(MOE_ERR_INVALID_ARG, "profiling was never enabled");
   cudaError_t e = cudaEventSynchronize(layer->ev[4]);
   float ms[4] = {0, 0, 0, 0}, tot = 0;
-  for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&ms[i], layer->ev[i], layer->ev[i + 1]);
+  if (!layer->last_single)
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&ms[i], layer->ev[i], layer->ev[i + 1]);
   if (e == cudaSuccess) e = cudaEventElapsedTime(&tot, layer->ev[0], layer->ev[4]);
   int32_t nseg = 0;
   if (e == cudaSuccess) e = cudaMemcpy(&nseg, layer->num_seg, 4, cudaMemcpyDeviceToHost);
@@ -557,6 +664,7 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* p) {
   p->total_ms = tot;
   p->active_experts = nseg - layer->cfg.has_shared_expert;
   p->tokens = layer->last_T;
+  p->single_launch = layer->last_single ? 1 : 0;
   return MOE_OK;
 }
 

@@ -1,0 +1,321 @@
+// Device-side routing pieces shared by the routing kernels (route.cu) and the
+// decode megakernel (decode.cu). Outputs go wherever the RouteArgs pointers
+// point (global or shared memory); logits are read through L2.
+#pragma once
+
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// In-place exclusive prefix sum of n ints in shared memory; returns the total.
+// Called by all threads of the block. scratch: 33 ints of shared memory.
+__device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int start = tid * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int idx = start + i;
+    if (idx < n) local += data[idx];
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int wv = (lane < nwarps) ? scratch[lane] : 0;
+    int wincl = wv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wincl, o);
+      if (lane >= o) wincl += y;
+    }
+    scratch[lane] = wincl - wv;
+    if (lane == 31) scratch[32] = wincl;
+  }
+  __syncthreads();
+  int base = scratch[warp] + incl - local;
+  for (int i = 0; i < per; ++i) {
+    const int idx = start + i;
+    if (idx < n) {
+      const int c = data[idx];
+      data[idx] = base;
+      base += c;
+    }
+  }
+  const int total = scratch[32];
+  __syncthreads();
+  return total;
+}
+
+// One warp: softmax over the E logits of token t and selection of the top k
+// (largest logit first, lower id first among equal logits). NV = values held
+// per lane (E <= 32 * NV). Writes ids / weights to the workspace, the user
+// buffers (if any) and s_ids (chunk-local copy).
+template <int NV>
+__device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int32_t* s_ids_row) {
+  const int lane = threadIdx.x & 31;
+  const int E = a.E, k = a.k;
+  const float* L = a.logits + (size_t)t * E;
+  float v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? __ldcg(L + e) : -INFINITY;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) m = fmaxf(m, v[i]);
+  m = warp_max(m);
+  float ssum = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    if (lane + 32 * i < E) ssum += expf(v[i] - m);
+  ssum = warp_sum(ssum);
+
+  uint32_t taken = 0;
+  float my_p = 0.f, psel = 0.f;
+  int my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      // within a lane e grows with i, so '>' keeps the lowest id of equal values
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const float p = expf(bv - m) / ssum;
+    if (lane == j) {
+      my_p = p;
+      my_id = bi;
+    }
+    psel += p;
+  }
+  if (lane < k) {
+    const float wv = a.renorm ? my_p / psel : my_p;
+    const size_t o = (size_t)t * k + lane;
+    a.ids[o] = my_id;
+    a.w[o] = wv;
+    if (a.ids_user) a.ids_user[o] = my_id;
+    if (a.w_user) a.w_user[o] = wv;
+    if (s_ids_row) s_ids_row[lane] = my_id;
+  }
+}
+
+// Warp-level stable scatter of flat indices [f_begin, f_end) (ids in s_ids,
+// indexed from f_begin) using per-expert running cursors.
+__device__ __forceinline__ void warp_stable_scatter(const RouteArgs& a, const int32_t* s_ids, int f_begin, int f_end,
+                                    int* cursor) {
+  const int lane = threadIdx.x & 31;
+  for (int f0 = f_begin; f0 < f_end; f0 += 32) {
+    const int f = f0 + lane;
+    const bool valid = f < f_end;
+    const int e = valid ? s_ids[f - f_begin] : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    int pos = 0;
+    if (valid) {
+      pos = cursor[e] + __popc(peers & lanemask_lt());
+      a.perm[pos] = f;
+      a.inv_perm[f] = pos;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) cursor[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Warp-level list of active experts (count > 0) in ascending id, plus the
+// shared expert segment at the end.
+__device__ __forceinline__ void warp_segments(const RouteArgs& a, const int* s_counts, const int* s_off) {
+  const int lane = threadIdx.x & 31;
+  int n = 0;
+  for (int base = 0; base < a.E; base += 32) {
+    const int e = base + lane;
+    const bool act = e < a.E && s_counts[e] > 0;
+    const uint32_t mask = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const int idx = n + __popc(mask & lanemask_lt());
+      a.seg_expert[idx] = e;
+      a.seg_start[idx] = s_off[e];
+      a.seg_count[idx] = s_counts[e];
+    }
+    n += __popc(mask);
+  }
+  if (lane == 0) {
+    if (a.has_shared) {
+      a.seg_expert[n] = a.E;
+      a.seg_start[n] = a.T * a.k;
+      a.seg_count[n] = a.T;
+      ++n;
+    }
+    *a.num_seg = n;
+  }
+}
+
+// ------------------------------------------------------------ small path
+// Single-warp finish for n = T*k <= 32 (token, rank) pairs: lane f holds pair
+// f; its sorted position is the number of pairs with a lower expert id, or
+// the same id and a lower flat index (a stable counting sort by rank). Also
+// writes the segment list and the per-expert counts / offsets (by binary
+// search over the sorted ids, all threads).
+__device__ __forceinline__ void finish_tiny(const RouteArgs& a, int32_t* s_ids, int32_t* s_sorted) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n = a.T * a.k;
+  if (tid < 32) {
+    const int e = lane < n ? s_ids[lane] : 0x7fffffff;
+    int rank = 0;
+    for (int o = 0; o < n; ++o) {
+      const int eo = __shfl_sync(0xffffffffu, e, o);
+      rank += (eo < e || (eo == e && o < lane)) ? 1 : 0;
+    }
+    if (lane < n) {
+      a.perm[rank] = lane;
+      a.inv_perm[lane] = rank;
+      s_sorted[rank] = e;
+    }
+    __syncwarp();
+    const int se = lane < n ? s_sorted[lane] : -1;
+    const bool start = lane < n && (lane == 0 || s_sorted[lane - 1] != se);
+    const uint32_t mask = __ballot_sync(0xffffffffu, start);
+    if (start) {
+      const int idx = __popc(mask & lanemask_lt());
+      const uint32_t later = mask & ~((2u << lane) - 1u);
+      const int next = later ? (__ffs(later) - 1) : n;
+      a.seg_expert[idx] = se;
+      a.seg_start[idx] = lane;
+      a.seg_count[idx] = next - lane;
+    }
+    if (lane == 0) {
+      int ns = __popc(mask);
+      if (a.has_shared) {
+        a.seg_expert[ns] = a.E;
+        a.seg_start[ns] = n;
+        a.seg_count[ns] = a.T;
+        ++ns;
+      }
+      *a.num_seg = ns;
+    }
+  }
+  __syncthreads();
+  // offsets[e] = number of pairs with expert < e
+  for (int e = tid; e <= a.E; e += blockDim.x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_sorted[mid] < e)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    a.offsets[e] = lo;
+    s_ids[32 + e] = lo;  // scratch copy for the counts
+  }
+  __syncthreads();
+  for (int e = tid; e < a.E; e += blockDim.x) a.counts[e] = s_ids[32 + e + 1] - s_ids[32 + e];
+}
+
+// Router logits of expert e for the T <= kSmallRouteMaxT tokens of x, by one
+// warp: lane-strided FP32 FMA over the row in float4 steps, then a butterfly
+// sum. Every small-batch path uses this one function, so they agree bit for
+// bit on the logits (and hence on the selection).
+__device__ __forceinline__ void warp_expert_logits(const RouteArgs& a, int e) {
+  const int lane = threadIdx.x & 31;
+  const int T = a.T, H = a.H, E = a.E;
+  float acc[kSmallRouteMaxT];
+#pragma unroll
+  for (int t = 0; t < kSmallRouteMaxT; ++t) acc[t] = 0.f;
+  const float4* wr4 = reinterpret_cast<const float4*>(a.wr + (size_t)e * H);
+  const uint2* x2 = reinterpret_cast<const uint2*>(a.x);
+#pragma unroll 16
+  for (int h4 = lane; h4 < H / 4; h4 += 32) {
+    const float4 wv = __ldg(wr4 + h4);
+#pragma unroll
+    for (int t = 0; t < kSmallRouteMaxT; ++t) {
+      if (t < T) {
+        const uint2 raw = __ldg(x2 + (size_t)t * (H / 4) + h4);
+        const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        acc[t] = fmaf(wv.x, x01.x, acc[t]);
+        acc[t] = fmaf(wv.y, x01.y, acc[t]);
+        acc[t] = fmaf(wv.z, x23.x, acc[t]);
+        acc[t] = fmaf(wv.w, x23.y, acc[t]);
+      }
+    }
+  }
+  const float b = a.bias ? __ldg(a.bias + e) : 0.f;
+#pragma unroll
+  for (int t = 0; t < kSmallRouteMaxT; ++t)
+    if (t < T) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0) a.logits[(size_t)t * E + e] = v + b;
+    }
+}
+
+// Top-k for all T tokens, the permutation and the segment list, computed by
+// one CTA (all its threads). scratch: >= T*k + 3*E + 66 ints of shared
+// memory; s_scan: 33 ints of shared memory.
+template <int NV>
+__device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* scratch, int* s_scan) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const int T = a.T, E = a.E, k = a.k;
+  int32_t* s_ids = scratch;
+  if (T * k <= 32) {
+    int32_t* s_sorted = s_ids + 32 + E + 1;
+    if (warp == 0)
+      for (int t = 0; t < T; ++t) warp_softmax_topk<NV>(a, t, s_ids + t * k);
+    __syncthreads();
+    finish_tiny(a, s_ids, s_sorted);
+  } else {
+    int* s_counts = s_ids + T * k;
+    int* s_off = s_counts + E;
+    int* s_cur = s_off + E + 1;
+    for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k);
+    for (int i = tid; i < E; i += blockDim.x) s_counts[i] = 0;
+    __syncthreads();
+    for (int f = tid; f < T * k; f += blockDim.x) atomicAdd(&s_counts[s_ids[f]], 1);
+    __syncthreads();
+    for (int i = tid; i < E; i += blockDim.x) {
+      s_off[i] = s_counts[i];
+      a.counts[i] = s_counts[i];
+    }
+    __syncthreads();
+    block_exclusive_scan(s_off, E, s_scan);
+    for (int i = tid; i < E; i += blockDim.x) {
+      s_cur[i] = s_off[i];
+      a.offsets[i] = s_off[i];
+    }
+    if (tid == 0) {
+      s_off[E] = T * k;
+      a.offsets[E] = T * k;
+    }
+    __syncthreads();
+    if (warp == 0) warp_stable_scatter(a, s_ids, 0, T * k, s_cur);
+    if (warp == 1) warp_segments(a, s_counts, s_off);
+    __syncthreads();
+  }
+}
+
+}  // namespace moe
