@@ -9,6 +9,8 @@
 #include <cstdint>
 #include <cuda_fp16.h>
 
+#include "kernels.h"
+
 namespace moe {
 
 constexpr uint32_t MOE_DEV_OK = 0;
@@ -24,6 +26,16 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) {
   if (err) atomicCAS(err, 0u, code);
+}
+
+// Phase trace of the single-launch decode kernel: kTraceStamps global-timer
+// stamps (ns) per CTA, CTA-major.
+__device__ __forceinline__ void trace_mark(unsigned long long* tr, int i) {
+  if (tr) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    tr[blockIdx.x * kTraceStamps + i] = t;
+  }
 }
 
 // ---------------------------------------------------------------- mbarrier

@@ -5,39 +5,50 @@
 // routing, gate/up, down and the combine; at batch 1 each of those costs as
 // much as streaming the weights. Here, inside one persistent grid whose CTAs
 // are all resident (cooperative launch):
-//   1. router logits: one expert row per warp across the whole grid;
-//   2. a grid-wide arrival count on the logits; then every CTA computes the
-//      top-k, the permutation and the segment list itself, into its own
-//      shared memory (identical results in every CTA, no second grid hop);
-//      CTA 0 also publishes them to global memory;
-//   3. gate/up + SwiGLU work items (the GEMV's items); every consumer warp
-//      signals a per-segment counter after its h rows are written;
+//   1. router logits: (expert, part) partial dot products spread over every
+//      warp of the grid;
+//   2. a grid-wide arrival count on the partials; then every CTA sums them
+//      in order and computes the top-k, the permutation and the segment list
+//      itself, into its own shared memory (identical results in every CTA,
+//      no second grid hop); CTA 0 also publishes them to global memory;
+//   3. gate/up + SwiGLU work items on the tensor cores (tcgemv_dev.cuh:
+//      codes dequantised in registers into mma.sync fragments);
 //   4. down work items, whose weights the producer streams into the ring
-//      while gate/up items are still being computed; a consumer warp waits
-//      for its segment's gate/up counter before reading h;
-//   5. every down item signals a per-row-block counter; the warp that
+//      while gate/up items are still being computed; the consumers wait once
+//      per segment for that segment's gate/up counter before reading h;
+//   5. every down item counts on a per-row-block counter; the CTA that
 //      completes a row block performs the weighted combine for those rows
 //      (fixed order: ranks j = 0..k-1, then the shared expert).
+// Warp roles: 8 consumer warps compute items out of a shared-memory ring; one
+// producer warp fills the ring with TMA copies; one signalling warp turns
+// each finished item into its GPU-scope counter update (and runs the
+// combines), so that no consumer ever waits on a release or an atomic.
 // Every cross-CTA wait is a bounded spin; on time-out the CTA records an
 // error, stops, lets its issued copies land and still passes the final
 // ticket, whose last holder resets all counters for the next launch.
-#include "gemv_dev.cuh"
 #include "route_dev.cuh"
+#include "tcgemv_dev.cuh"
 
 namespace moe {
 
 namespace {
 
+constexpr int kProducerWarp = kTcWarps;
+constexpr int kSignalWarp = kTcWarps + 1;
+constexpr int kDecodeThreads = (kTcWarps + 2) * 32;
+
 struct DecodeHdr {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
+  uint64_t full[kDecodeMaxStages];   // producer -> consumers: the item's bytes landed
+  uint64_t done[kDecodeMaxStages];   // consumers -> signaller: the item is computed
+  uint64_t empty[kDecodeMaxStages];  // signaller -> producer: the stage is free
   int abort_flag;
   int issued;
   int last;
 };
+static_assert(sizeof(DecodeHdr) <= kHdrBytes, "decode header exceeds its reserved bytes");
 
 // Release-ordered increment (fire and forget): the caller's prior writes, and
-// those of the warp lanes synchronised with it, are visible before it.
+// those it has observed (e.g. through an mbarrier), are visible before it.
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -70,39 +81,93 @@ __device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, v
   }
 }
 
-template <int NV, int KG, int NTG, int KD, int NTD>
-__global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
+// Weighted combine of down row block rbi by one warp (the signalling warp of
+// the CTA that completed it): out[t][row] = sum_j w[t][j] * y[(t, j)][row]
+// in rank order, then the shared expert, the FP16 rounding and the residual.
+// The same arithmetic, in the same order, as the multi-kernel combine.
+__device__ __forceinline__ void decode_combine_rows(const DecodeArgs& a, const TcGemvArgs& d, int rbi,
+                                                    const float* s_w, int lane) {
+  const int T = a.r.T, H = a.r.H, k = a.r.k, Tk = T * k;
+  const int r0 = rbi * d.rb;
+  const int nrows = min(d.rb, H - r0);
+#pragma unroll 2
+  for (int q = lane; q < nrows * T; q += 32) {
+    const int t = q / nrows, row = r0 + q % nrows;
+    const float* yp = d.y_out + (size_t)t * k * H + row;
+    float acc = 0.f;
+    int j = 0;
+    for (; j + 8 <= k; j += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(yp + (size_t)(j + u) * H);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc = fmaf(s_w[t * k + j + u], v[u], acc);
+    }
+    for (; j < k; ++j) acc = fmaf(s_w[t * k + j], __ldcg(yp + (size_t)j * H), acc);
+    if (a.has_shared) acc += __ldcg(d.y_out + (size_t)(Tk + t) * H + row);
+    __half o = __float2half_rn(acc);
+    if (a.x_res) o = __float2half_rn(__half2float(a.x_res[(size_t)t * H + row]) + __half2float(o));
+    a.out[(size_t)t * H + row] = o;
+  }
+}
+
+// Dynamic shared memory: header, then (1024-byte aligned) the ring, the B
+// fragments, the group constants, the K-part partials (two buffers) and the
+// routing arrays.
+struct DecodeSmem {
+  uint32_t ring, bs, cs, red, route, total;
+};
+__host__ __device__ inline DecodeSmem decode_smem_layout(const DecodeArgs& a, int stages) {
+  DecodeSmem L;
+  const uint32_t Tk = (uint32_t)(a.r.T * a.r.k), E = (uint32_t)a.r.E, ns = (uint32_t)a.ns;
+  L.ring = kHdrBytes;  // rounded up to 1024 in the kernel (slack below)
+  L.bs = L.ring + 1024u + (uint32_t)stages * a.slot_bytes;
+  L.cs = L.bs + (uint32_t)a.bs_chunks * ns * 64u;
+  L.red = L.cs + (((uint32_t)a.cs_groups * ns * 4u + 15u) & ~15u);
+  L.route = L.red + 2u * kTcWarps * 2u * 16u * ns * 4u;
+  L.total = L.route + (5u * Tk + 8u * E + 74u) * 4u;
+  return L;
+}
+
+template <int NV>
+__global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_scan[33];
   DecodeHdr* hdr = reinterpret_cast<DecodeHdr*>(smem);
-  unsigned char* ring = smem + kHdrBytes;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.stages;
-  const int T = a.r.T, H = a.r.H, E = a.r.E, k = a.r.k;
+  const int T = a.r.T, E = a.r.E, k = a.r.k;
   const int Tk = T * k;
+  const int NS = a.ns;
   uint32_t* logits_done = a.ctr;
   uint32_t* final_ticket = a.ctr + 1;
   uint32_t* done_gu = a.ctr + 2;
   uint32_t* done_dn = a.ctr + 2 + (E + 1);
 
-  // routing results of this CTA, in shared memory
-  int32_t* rs = reinterpret_cast<int32_t*>(ring + (size_t)S * a.slot_bytes);
-  int32_t* s_ids = rs;                 // [Tk]
-  float* s_w = reinterpret_cast<float*>(s_ids + 512);
-  int32_t* s_counts = s_ids + 1024;    // [E]
-  int32_t* s_off = s_counts + 1024;    // [E+1]
-  int32_t* s_perm = s_off + 1025;      // [Tk]
-  int32_t* s_inv = s_perm + 512;       // [Tk]
-  int32_t* s_sexp = s_inv + 512;       // [E+1]
-  int32_t* s_sstart = s_sexp + 1025;   // [E+1]
-  int32_t* s_scount = s_sstart + 1025; // [E+1]
-  int32_t* s_nseg = s_scount + 1025;   // [1]
-  int32_t* s_scratch = s_nseg + 4;     // [Tk + 3E + 66]
+  const DecodeSmem lay = decode_smem_layout(a, S);
+  const uint32_t sbase = smem_u32(smem);
+  unsigned char* ring = smem + (((sbase + lay.ring + 1023u) & ~1023u) - sbase);
+  uint4* Bs = reinterpret_cast<uint4*>(smem + lay.bs);
+  float* Cs = reinterpret_cast<float*>(smem + lay.cs);
+  float* red = reinterpret_cast<float*>(smem + lay.red);
+  // routing results of this CTA, sized for this E and T*k
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem + lay.route);  // [Tk]
+  float* s_w = reinterpret_cast<float*>(s_ids + Tk);               // [Tk]
+  int32_t* s_counts = reinterpret_cast<int32_t*>(s_w + Tk);        // [E]
+  int32_t* s_off = s_counts + E;                                   // [E+1]
+  int32_t* s_perm = s_off + E + 1;                                 // [Tk]
+  int32_t* s_inv = s_perm + Tk;                                    // [Tk]
+  int32_t* s_sexp = s_inv + Tk;                                    // [E+1]
+  int32_t* s_sstart = s_sexp + E + 1;                              // [E+1]
+  int32_t* s_scount = s_sstart + E + 1;                            // [E+1]
+  int32_t* s_nseg = s_scount + E + 1;                              // [1] (+3 pad)
+  int32_t* s_scratch = s_nseg + 4;                                 // [Tk + 3E + 66]
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&hdr->full[s], 1);
-      mbar_init(&hdr->empty[s], kConsumerWarps);
+      mbar_init(&hdr->done[s], kTcWarps);
+      mbar_init(&hdr->empty[s], 1);
     }
     hdr->abort_flag = 0;
     hdr->issued = 0;
@@ -111,19 +176,26 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
   }
   __syncthreads();
   volatile int* abort_flag = &hdr->abort_flag;
+  unsigned long long* tr = (tid == 0) ? a.trace : nullptr;
+  trace_mark(tr, 0);
 
   // ------------------------------------------------ 1. router logits (FP32)
+  // (expert, part) tasks spread over every warp of the grid; the partials are
+  // summed in order when the logits are read (routing below).
   {
-    const int nw = gridDim.x * (kGemvThreads / 32);
-    for (int e = warp * gridDim.x + blockIdx.x; e < E; e += nw) warp_expert_logits(a.r, e);
+    const int nw = gridDim.x * (kDecodeThreads / 32);
+    for (int q = warp * gridDim.x + blockIdx.x; q < E * kLogitParts; q += nw)
+      warp_logit_partial(a.r, q / kLogitParts, q % kLogitParts, a.r.logit_part);
   }
-  __threadfence();
   __syncthreads();
+  trace_mark(tr, 1);
   if (tid == 0) {
-    atomicAdd(logits_done, 1u);
+    // bar.sync above orders every warp's partials before this release
+    red_release_add(logits_done, 1u);
     wait_count(logits_done, gridDim.x, abort_flag, a.r.err);
   }
   __syncthreads();
+  trace_mark(tr, 2);
 
   int nseg = 0;
   if (!*abort_flag) {
@@ -141,8 +213,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
     L.seg_start = s_sstart;
     L.seg_count = s_scount;
     L.num_seg = s_nseg;
-    route_finish_cta<NV>(L, s_scratch, s_scan);
+    route_finish_cta<NV>(L, s_scratch, s_scan, a.r.logit_part, tr);
     __syncthreads();
+    trace_mark(tr, 4);
     nseg = *s_nseg;
     if (blockIdx.x == 0) {
       // publish for moe_layer_routing and the routing outputs
@@ -159,7 +232,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
   }
 
   // ------------------------------------ 3./4. gate/up then down work items
-  GemvArgs g = a.g, d = a.d;
+  TcGemvArgs g = a.g, d = a.d;
   g.seg_expert = d.seg_expert = s_sexp;
   g.seg_start = d.seg_start = s_sstart;
   g.seg_count = d.seg_count = s_scount;
@@ -167,15 +240,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
   const int nrb_g = (g.N + g.rb - 1) / g.rb;
   const int nrb_d = (d.N + d.rb - 1) / d.rb;
   const int tot_g = nseg * nrb_g, tot_d = nseg * nrb_d;
-  const int ipc_g = (tot_g + gridDim.x - 1) / gridDim.x, ipc_d = (tot_d + gridDim.x - 1) / gridDim.x;
-  const int fg = blockIdx.x * ipc_g, fd = blockIdx.x * ipc_d;
-  const int ng_it = max(0, min(tot_g, fg + ipc_g) - fg);
-  const int nd_it = max(0, min(tot_d, fd + ipc_d) - fd);
+  // balanced contiguous split: CTA b takes items [b * tot / grid, (b+1) * tot / grid)
+  const int fg = (int)((long long)blockIdx.x * tot_g / gridDim.x);
+  const int fd = (int)((long long)blockIdx.x * tot_d / gridDim.x);
+  const int ng_it = (int)((long long)(blockIdx.x + 1) * tot_g / gridDim.x) - fg;
+  const int nd_it = (int)((long long)(blockIdx.x + 1) * tot_d / gridDim.x) - fd;
   const int n_it = *abort_flag ? 0 : ng_it + nd_it;
-  const uint32_t gu_target = (uint32_t)nrb_g * kConsumerWarps;
-  const uint32_t dn_target = (uint32_t)nseg * kConsumerWarps;
+  const uint32_t gu_target = (uint32_t)nrb_g;  // gate/up items per segment
+  const uint32_t dn_target = (uint32_t)nseg;   // down items per row block
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       for (int it = 0; it < n_it; ++it) {
@@ -184,68 +259,127 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
         if (!mbar_wait(&hdr->empty[st], ph ^ 1u, abort_flag, a.r.err)) break;
         unsigned char* slot = ring + (size_t)st * a.slot_bytes;
         if (it < ng_it)
-          gemv_issue_item<true>(g, fg + it, nrb_g, slot, &hdr->full[st], pol);
+          tc_issue_item<true>(g, &a.tm_gate, &a.tm_up, fg + it, nrb_g, slot, &hdr->full[st], pol);
         else
-          gemv_issue_item<false>(d, fd + it - ng_it, nrb_d, slot, &hdr->full[st], pol);
+          tc_issue_item<false>(d, &a.tm_down, &a.tm_down, fd + it - ng_it, nrb_d, slot, &hdr->full[st], pol);
         hdr->issued = it + 1;
       }
     }
-  } else {
-    XRegs<KG, NTG> xg;
-    XRegs<KD, NTD> xd;
+  } else if (warp == kSignalWarp) {
+    // ---------------------------------------------------------- signaller
+    // Stage release first (the producer refills at once), then the counter:
+    // gate/up items add to their segment's counter, one release per run of
+    // already-finished items of that segment; down items count on their row
+    // block, and the item that completes it leads to that block's combine.
+    // The consumers' writes reach this warp through the `done` mbarrier
+    // (release / acquire at CTA scope); the GPU-scope release is cumulative.
+    uint32_t pending = 0;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % S;
       const uint32_t ph = (uint32_t)(it / S) & 1u;
-      if (!mbar_wait(&hdr->full[st], ph, abort_flag, a.r.err)) break;
-      const unsigned char* slot = ring + (size_t)st * a.slot_bytes;
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(&hdr->done[st], ph, abort_flag, a.r.err);
+        if (ok) mbar_arrive(&hdr->empty[st]);
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
       if (it < ng_it) {
-        const int item = fg + it;
-        gemv_consume_item<KG, NTG, true, false>(g, item, nrb_g, slot, xg, warp, lane);
-        __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&hdr->empty[st]);
-          red_release_add(done_gu + item / nrb_g, 1u);
-        }
-      } else {
-        const int item = fd + it - ng_it;
-        const int sgi = item / nrb_d, rbi = item % nrb_d;
-        int ok = 1;
-        if (lane == 0) ok = wait_count(done_gu + sgi, gu_target, abort_flag, a.r.err);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        gemv_consume_item<KD, NTD, false, true>(d, item, nrb_d, slot, xd, warp, lane);
-        __syncwarp();
-        uint32_t prev = 0;
-        if (lane == 0) {
-          mbar_arrive(&hdr->empty[st]);
-          prev = atom_acq_rel_add(done_dn + rbi, 1u);
-        }
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev + 1 == dn_target) {
-          // ------------------------------- 5. combine of this row block
-          // (lane 0's acq_rel increment observed every other warp's release)
-          __syncwarp();
-          const int r0 = rbi * d.rb;
-          const int nrows = min(d.rb, H - r0);
-          for (int r = lane; r < nrows; r += 32) {
-            const int row = r0 + r;
-            for (int t = 0; t < T; ++t) {
-              float acc = 0.f;
-              for (int j = 0; j < k; ++j)
-                acc = fmaf(s_w[t * k + j], __ldcg(d.y_out + (size_t)(t * k + j) * H + row), acc);
-              if (a.has_shared) acc += __ldcg(d.y_out + (size_t)(Tk + t) * H + row);
-              __half o = __float2half_rn(acc);
-              if (a.x_res) o = __float2half_rn(__half2float(a.x_res[(size_t)t * H + row]) + __half2float(o));
-              a.out[(size_t)t * H + row] = o;
-            }
+          const int sgi = (fg + it) / nrb_g;
+          ++pending;
+          const int nx = it + 1;
+          bool flush = true;
+          if (nx < ng_it && (fg + nx) / nrb_g == sgi)
+            flush = !mbar_try_wait(&hdr->done[nx % S], (uint32_t)(nx / S) & 1u);
+          if (flush) {
+            red_release_add(done_gu + sgi, pending);
+            pending = 0;
           }
         }
+      } else {
+        const int rbi = (fd + it - ng_it) % nrb_d;
+        uint32_t prev = 0;
+        if (lane == 0) prev = atom_acq_rel_add(done_dn + rbi, 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        __syncwarp();
+        // lane 0's acq_rel increment observed every other CTA's release
+        if (prev + 1 == dn_target) decode_combine_rows(a, d, rbi, s_w, lane);
       }
     }
+    if (lane == 0 && a.trace) {
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      a.trace[blockIdx.x * kTraceStamps + 9] = t;
+    }
+  } else {
+    // ----------------------------------------------------------- consumers
+    // Every consumer warp runs the same sequence of named barriers (it
+    // depends only on the routing in shared memory), also after a failed
+    // wait: the work is then skipped in effect (stale data), never the
+    // barrier, so no warp can be left waiting.
+    int b_seg = -1, b_tb = -1, b_gu = -1;  // token tile the B buffer holds
+    int ready_seg = -1;
+    int buf = 0;
+    const int red_words = kTcWarps * 2 * 16 * NS;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % S;
+      const uint32_t ph = (uint32_t)(it / S) & 1u;
+      mbar_wait(&hdr->full[st], ph, abort_flag, a.r.err);
+      if (it < kTraceItems) trace_mark(tr, kTracePhases + 2 * it);
+      const unsigned char* slot = ring + (size_t)st * a.slot_bytes;
+      const bool gu = it < ng_it;
+      const int item = gu ? fg + it : fd + it - ng_it;
+      const int nrb = gu ? nrb_g : nrb_d;
+      const int sgi = item / nrb;
+      const int cnt = s_scount[sgi];
+      if (it == 0) trace_mark(tr, 5);
+      for (int tb = 0; tb < cnt; tb += kTcMaxTok) {
+        const int ntok = min(kTcMaxTok, cnt - tb);
+        if (sgi != b_seg || tb != b_tb || (int)gu != b_gu) {
+          if (gu) {
+            tc_build_b<false>(g, sgi, tb, ntok, NS, Bs, Cs, tid);
+          } else {
+            if (sgi != ready_seg) {
+              // h of this segment: every gate/up item of it, from every CTA
+              int ok = 1;
+              if (lane == 0) ok = wait_count(done_gu + sgi, gu_target, abort_flag, a.r.err);
+              ok = __shfl_sync(0xffffffffu, ok, 0);
+              __syncwarp();
+              (void)ok;  // on failure the abort flag is set; the barriers still run
+              ready_seg = sgi;
+            }
+            tc_build_b<true>(d, sgi, tb, ntok, NS, Bs, Cs, tid);
+          }
+          b_seg = sgi;
+          b_tb = tb;
+          b_gu = gu;
+          tc_bar();
+        }
+        float* rb = red + buf * red_words;
+        if (gu) {
+          tc_compute<true>(g, slot, Bs, Cs, ntok, NS, rb, warp, lane);
+          tc_bar();
+          tc_finish<true>(g, item, nrb, tb, ntok, NS, rb, tid);
+        } else {
+          if (it == ng_it && tb == 0) trace_mark(tr, 7);
+          tc_compute<false>(d, slot, Bs, Cs, ntok, NS, rb, warp, lane);
+          tc_bar();
+          tc_finish<false>(d, item, nrb, tb, ntok, NS, rb, tid);
+        }
+        buf ^= 1;
+      }
+      if (gu && it == ng_it - 1) trace_mark(tr, 6);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&hdr->done[st]);
+      if (it < kTraceItems) trace_mark(tr, kTracePhases + 2 * it + 1);
+    }
+    trace_mark(tr, 8);
   }
 
   // ---------------------------------------------------------------- teardown
   __syncthreads();
+  trace_mark(tr, 10);
   if (tid == 0 && hdr->abort_flag) {
     const int issued = hdr->issued;
     for (int s = 0; s < S && s < issued; ++s) {
@@ -254,13 +388,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
     }
   }
   if (tid == 0) {
-    __threadfence();
-    hdr->last = (atomicAdd(final_ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+    hdr->last = (atom_acq_rel_add(final_ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+    trace_mark(tr, 11);
   }
   __syncthreads();
   if (hdr->last) {
     // every CTA has finished: reset the counters for the next launch
-    __threadfence();
     for (int i = tid; i <= E; i += blockDim.x) done_gu[i] = 0u;
     for (int i = tid; i < nrb_d; i += blockDim.x) done_dn[i] = 0u;
     if (tid == 0) {
@@ -270,14 +403,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_decode(DecodeArgs a) {
   }
 }
 
-template <int NV, int KG, int NTG, int KD, int NTD>
+template <int NV>
 cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s) {
-  const size_t smem = decode_smem_bytes(a.stages, a.slot_bytes);
-  cudaError_t e = ensure_smem(k_decode<NV, KG, NTG, KD, NTD>, smem);
+  const size_t smem = decode_smem_bytes(a, a.stages);
+  cudaError_t e = ensure_smem(k_decode<NV>, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kGemvThreads);
+  cfg.blockDim = dim3(kDecodeThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -285,36 +418,34 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<NV, KG, NTG, KD, NTD>, a);
-}
-
-template <int KG, int NTG, int KD, int NTD>
-cudaError_t launch_decode_nv(const DecodeArgs& a, int grid, cudaStream_t s) {
-  if (a.r.E <= 64) return launch_decode_t<2, KG, NTG, KD, NTD>(a, grid, s);
-  if (a.r.E <= 128) return launch_decode_t<4, KG, NTG, KD, NTD>(a, grid, s);
-  if (a.r.E <= 256) return launch_decode_t<8, KG, NTG, KD, NTD>(a, grid, s);
-  if (a.r.E <= 512) return launch_decode_t<16, KG, NTG, KD, NTD>(a, grid, s);
-  return launch_decode_t<32, KG, NTG, KD, NTD>(a, grid, s);
+  return cudaLaunchKernelEx(&cfg, k_decode<NV>, a);
 }
 
 }  // namespace
 
-size_t decode_smem_bytes(int stages, uint32_t slot_bytes) {
-  // header, ring, routing arrays (8 x 1025 + 4 ints), finish scratch (512 + 3 x 1024 + 66 ints)
-  return kHdrBytes + (size_t)stages * slot_bytes + (8 * 1025 + 4 + 512 + 3 * 1024 + 66) * sizeof(int32_t);
+size_t decode_smem_bytes(const DecodeArgs& a, int stages) { return decode_smem_layout(a, stages).total; }
+
+TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes) {
+  TcGemvPlan p;
+  const int mats = dual ? 2 : 1;
+  p.rb = 16;
+  while (p.rb * 2 <= N && p.rb * 2 / 16 <= kTcWarps && mats * (p.rb * 2) * (K / 2) <= item_bytes) p.rb *= 2;
+  p.rt = p.rb / 16;
+  p.kparts = kTcWarps / p.rt;
+  p.nbox = (K / 2 + 127) / 128;
+  p.code_mat_bytes = (uint32_t)p.nbox * 128u * (uint32_t)p.rb;
+  const int ng = (K + G - 1) / G;
+  p.sstride = ((uint32_t)p.rb * ng * 2u + 15u) & ~15u;
+  p.slot_bytes = ((uint32_t)mats * (p.code_mat_bytes + p.sstride) + 1023u) & ~1023u;
+  return p;
 }
 
-bool decode_supported(int kg, int ntg, int kd, int ntd) {
-  return (kg == 2 && kd == 1 && ntg == 1 && (ntd == 1 || ntd == 2)) ||
-         (kg == 1 && kd == 1 && ((ntg == 1 && ntd == 1) || (ntg == 2 && ntd == 2)));
-}
-
-cudaError_t launch_decode(const DecodeArgs& a, int kg, int ntg, int kd, int ntd, int grid, cudaStream_t s) {
-  if (kg == 2 && kd == 1 && ntg == 1 && ntd == 1) return launch_decode_nv<2, 1, 1, 1>(a, grid, s);
-  if (kg == 2 && kd == 1 && ntg == 1 && ntd == 2) return launch_decode_nv<2, 1, 1, 2>(a, grid, s);
-  if (kg == 1 && kd == 1 && ntg == 1 && ntd == 1) return launch_decode_nv<1, 1, 1, 1>(a, grid, s);
-  if (kg == 1 && kd == 1 && ntg == 2 && ntd == 2) return launch_decode_nv<1, 2, 1, 2>(a, grid, s);
-  return cudaErrorInvalidConfiguration;
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
+  if (a.r.E <= 64) return launch_decode_t<2>(a, grid, s);
+  if (a.r.E <= 128) return launch_decode_t<4>(a, grid, s);
+  if (a.r.E <= 256) return launch_decode_t<8>(a, grid, s);
+  if (a.r.E <= 512) return launch_decode_t<16>(a, grid, s);
+  return launch_decode_t<32>(a, grid, s);
 }
 
 }  // namespace moe

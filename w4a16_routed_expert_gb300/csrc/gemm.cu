@@ -486,6 +486,19 @@ bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tcgemv_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes,
+                       int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)N, (cuuint64_t)num_slots};
+  const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)record_bytes};
+  const cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool_section), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;

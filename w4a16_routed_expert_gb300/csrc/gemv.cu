@@ -1,55 +1,64 @@
-// Decode-regime grouped W4A16 GEMV over expert segments, and the weighted
-// combine.
+// Decode-regime grouped W4A16 GEMV over expert segments (multi-kernel path:
+// one launch for gate/up + SwiGLU, one for down), and the weighted combine.
 //
 // Horizon RunMap report, "What is implemented": the INT4 routed experts stay
 // compact in GPU memory and are executed with FP16 activations; the weights
 // are expanded only in registers, never stored expanded.
 //
 // Work item = (expert segment, block of rb output rows). A persistent CTA
-// (one per SM) walks a contiguous range of items. Its producer thread copies
-// each item's INT4 rows and FP16 scales — contiguous byte ranges of the
-// expert's record — into a ring of shared-memory stages with bulk async
-// copies (cp.async.bulk, completion counted on an mbarrier). Eight consumer
-// warps dequantise 16-byte code chunks in registers and accumulate in FP32;
-// LPR lanes share a row and finish it with xor-shuffles.
-//
-// Dequantisation in registers. A code q in bits [4j, 4j+4) of a 32-bit word
-// is isolated with one AND (nibbles 0..5) or one/two shifts (nibbles 6, 7).
-// Read as an FP32 bit pattern below 2^24, the masked word is exactly
-// q * 2^(p - 149), p the bit position it was left at. The activation is
-// pre-scaled by 2^(100 - p) (exact), so every product is q * x * 2^-49 with
-// no rounding, and the sum over a 32-code chunk is rescaled by 2^49. The zero
-// point is applied once per chunk: sum_k (q_k - 8) x_k = sum_k q_k x_k -
-// 8 sum_k x_k, and the chunk's FP16 scale multiplies the result (a chunk
-// never straddles a scale group since 32 divides G). Products are exact and
-// sums are FP32, so the only roundings are FP32 additions.
+// (one per SM) walks a balanced contiguous range of items. Its producer
+// thread copies each item's codes (TMA, 128-byte swizzled boxes) and FP16
+// scales (bulk copy) into a ring of shared-memory stages; eight consumer
+// warps compute the item on the tensor cores with the device functions of
+// tcgemv_dev.cuh, which the single-launch decode kernel shares, so both paths
+// produce the same bits for the same plan.
 #include <algorithm>
 
-#include "gemv_dev.cuh"
+#include "tcgemv_dev.cuh"
 
 namespace moe {
 
 namespace {
 
 struct GemvHdr {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
+  uint64_t full[kDecodeMaxStages];
+  uint64_t empty[kDecodeMaxStages];
   int abort_flag;
   int issued;
 };
+static_assert(sizeof(GemvHdr) <= kHdrBytes, "GEMV header exceeds its reserved bytes");
 
-template <int KCH, int NT, bool DUAL>
-__global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(GemvArgs a) {
+struct GemvSmem {
+  uint32_t ring, bs, cs, red, total;
+};
+GemvSmem __host__ __device__ inline gemv_smem_layout(const TcGemvLaunch& p) {
+  GemvSmem L;
+  const uint32_t ns = (uint32_t)p.ns;
+  L.ring = kHdrBytes;  // rounded up to 1024 in the kernel (slack below)
+  L.bs = L.ring + 1024u + (uint32_t)p.stages * p.slot_bytes;
+  L.cs = L.bs + (uint32_t)p.bs_chunks * ns * 64u;
+  L.red = L.cs + (((uint32_t)p.cs_groups * ns * 4u + 15u) & ~15u);
+  L.total = L.red + 2u * kTcWarps * 2u * 16u * ns * 4u;
+  return L;
+}
+
+template <bool DUAL>
+__global__ void __launch_bounds__(kGemvThreads, 1) k_tcgemv(const __grid_constant__ TcGemvLaunch p) {
   extern __shared__ __align__(128) unsigned char smem[];
   GemvHdr* hdr = reinterpret_cast<GemvHdr*>(smem);
-  unsigned char* stages = smem + kHdrBytes;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = a.stages;
+  const int S = p.stages, NS = p.ns;
+  const GemvSmem lay = gemv_smem_layout(p);
+  const uint32_t sbase = smem_u32(smem);
+  unsigned char* ring = smem + (((sbase + lay.ring + 1023u) & ~1023u) - sbase);
+  uint4* Bs = reinterpret_cast<uint4*>(smem + lay.bs);
+  float* Cs = reinterpret_cast<float*>(smem + lay.cs);
+  float* red = reinterpret_cast<float*>(smem + lay.red);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&hdr->full[s], 1);
-      mbar_init(&hdr->empty[s], kConsumerWarps);
+      mbar_init(&hdr->empty[s], kTcWarps);
     }
     hdr->abort_flag = 0;
     hdr->issued = 0;
@@ -59,14 +68,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(GemvArgs a) {
   pdl_trigger();
   pdl_wait();
 
-  const int nseg = *a.num_seg;
+  const TcGemvArgs& a = p.a;
+  const int nseg = *p.num_seg;
   const int nrb = (a.N + a.rb - 1) / a.rb;
   const int total = nseg * nrb;
-  const int ipc = (total + gridDim.x - 1) / gridDim.x;
-  const int first = blockIdx.x * ipc;
-  const int nitems = max(0, min(total, first + ipc) - first);
+  const int first = (int)((long long)blockIdx.x * total / gridDim.x);
+  const int nitems = (int)((long long)(blockIdx.x + 1) * total / gridDim.x) - first;
 
-  if (warp == kConsumerWarps) {
+  if (warp == kTcWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
@@ -74,19 +83,40 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(GemvArgs a) {
         const int st = it % S;
         const uint32_t ph = (uint32_t)(it / S) & 1u;
         if (!mbar_wait(&hdr->empty[st], ph ^ 1u, &hdr->abort_flag, a.err)) break;
-        gemv_issue_item<DUAL>(a, first + it, nrb, stages + (size_t)st * a.stage_bytes, &hdr->full[st], pol);
+        tc_issue_item<DUAL>(a, &p.m0, &p.m1, first + it, nrb, ring + (size_t)st * p.slot_bytes, &hdr->full[st],
+                            pol);
         hdr->issued = it + 1;
       }
     }
   } else {
     // ----------------------------------------------------------- consumers
-    XRegs<KCH, NT> xr;
+    // The named-barrier sequence depends only on the segment list, so every
+    // consumer warp runs it in full, also after a failed (bounded) wait.
+    int b_seg = -1, b_tb = -1;
+    int buf = 0;
+    const int red_words = kTcWarps * 2 * 16 * NS;
     for (int it = 0; it < nitems; ++it) {
       const int st = it % S;
       const uint32_t ph = (uint32_t)(it / S) & 1u;
-      if (!mbar_wait(&hdr->full[st], ph, &hdr->abort_flag, a.err)) break;
-      gemv_consume_item<KCH, NT, DUAL, false>(a, first + it, nrb, stages + (size_t)st * a.stage_bytes, xr, warp,
-                                              lane);
+      mbar_wait(&hdr->full[st], ph, &hdr->abort_flag, a.err);
+      const unsigned char* slot = ring + (size_t)st * p.slot_bytes;
+      const int item = first + it;
+      const int sgi = item / nrb;
+      const int cnt = a.seg_count[sgi];
+      for (int tb = 0; tb < cnt; tb += kTcMaxTok) {
+        const int ntok = min(kTcMaxTok, cnt - tb);
+        if (sgi != b_seg || tb != b_tb) {
+          tc_build_b<false>(a, sgi, tb, ntok, NS, Bs, Cs, tid);
+          b_seg = sgi;
+          b_tb = tb;
+          tc_bar();
+        }
+        float* rb = red + buf * red_words;
+        tc_compute<DUAL>(a, slot, Bs, Cs, ntok, NS, rb, warp, lane);
+        tc_bar();
+        tc_finish<DUAL>(a, item, nrb, tb, ntok, NS, rb, tid);
+        buf ^= 1;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&hdr->empty[st]);
     }
@@ -101,24 +131,6 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_gemv(GemvArgs a) {
       mbar_wait(&hdr->full[s], (uint32_t)n & 1u, nullptr, nullptr);
     }
   }
-}
-
-template <int KCH, int NT, bool DUAL>
-cudaError_t launch_gemv_t(const GemvArgs& a, int grid, cudaStream_t s, bool pdl) {
-  const size_t smem = gemv_smem_bytes(a.stages, a.stage_bytes);
-  cudaError_t e = ensure_smem(k_gemv<KCH, NT, DUAL>, smem);
-  if (e != cudaSuccess) return e;
-  return launch_ex(k_gemv<KCH, NT, DUAL>, dim3(grid), dim3(kGemvThreads), smem, s, pdl, a);
-}
-
-template <bool DUAL>
-cudaError_t launch_gemv_d(const GemvArgs& a, int kch, int nt, int grid, cudaStream_t s, bool pdl) {
-  if (kch == 1 && nt == 1) return launch_gemv_t<1, 1, DUAL>(a, grid, s, pdl);
-  if (kch == 1 && nt == 2) return launch_gemv_t<1, 2, DUAL>(a, grid, s, pdl);
-  if (kch == 2 && nt == 1) return launch_gemv_t<2, 1, DUAL>(a, grid, s, pdl);
-  if (kch == 3 && nt == 1) return launch_gemv_t<3, 1, DUAL>(a, grid, s, pdl);
-  if (kch == 4 && nt == 1) return launch_gemv_t<4, 1, DUAL>(a, grid, s, pdl);
-  return cudaErrorInvalidConfiguration;
 }
 
 __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
@@ -162,47 +174,18 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
 
 }  // namespace
 
-int gemv_lanes_per_row(int K) {
-  const int chunks = K / 32;
-  int lpr = 32;
-  while (lpr > chunks && lpr > 4) lpr >>= 1;
-  return lpr;
-}
+size_t tcgemv_smem_bytes(const TcGemvLaunch& p) { return gemv_smem_layout(p).total; }
 
-int gemv_kch(int K, int lpr) { return (K / 32 + lpr - 1) / lpr; }
-
-size_t gemv_smem_bytes(int stages, uint32_t stage_bytes) { return kHdrBytes + (size_t)stages * stage_bytes; }
-
-GemvPlan plan_gemv(int N, int K, int G, bool dual, int T) {
-  GemvPlan p;
-  p.lpr = gemv_lanes_per_row(K);
-  p.kch = gemv_kch(K, p.lpr);
-  const int rows_per_pass = kConsumerWarps * (32 / p.lpr);
-  const int mats = dual ? 2 : 1;
-  const int bytes_per_pass = mats * rows_per_pass * (K / 2);
-  int m = std::max(1, 16384 / std::max(1, bytes_per_pass));
-  p.rb = rows_per_pass * m;
-  // keep work items multiples of 8 rows and no larger than needed
-  while (p.rb > 8 && p.rb > N) p.rb >>= 1;
-  p.rb = std::max(8, p.rb / 8 * 8);
-  const int ng = (K + G - 1) / G;
-  const uint32_t sstride = ((uint32_t)p.rb * ng * 2u + 15u) & ~15u;
-  p.stage_bytes = ((uint32_t)(mats * p.rb * (K / 2)) + mats * sstride + 127u) & ~127u;
-  p.stages = (int)std::min<size_t>(kMaxStages, std::max<size_t>(2, (180u * 1024u) / p.stage_bytes));
-  // token tile: the pre-scaled activations of nt tokens stay in registers
-  // (32 * kch * nt of them); keep that within the 288-thread register budget
-  p.nt = (T > 1 && p.kch == 1) ? 2 : 1;
-  return p;
-}
-
-bool gemv_plan_supported(const GemvPlan& p) {
-  if (p.kch == 1) return p.nt == 1 || p.nt == 2;
-  return p.kch >= 2 && p.kch <= 4 && p.nt == 1;
-}
-
-cudaError_t launch_gemv(const GemvArgs& a, bool dual, const GemvPlan& p, int grid, cudaStream_t s, bool pdl) {
-  if (dual) return launch_gemv_d<true>(a, p.kch, p.nt, grid, s, pdl);
-  return launch_gemv_d<false>(a, p.kch, p.nt, grid, s, pdl);
+cudaError_t launch_tcgemv(const TcGemvLaunch& p, bool dual, int grid, cudaStream_t s, bool pdl) {
+  const size_t smem = tcgemv_smem_bytes(p);
+  if (dual) {
+    cudaError_t e = ensure_smem(k_tcgemv<true>, smem);
+    if (e != cudaSuccess) return e;
+    return launch_ex(k_tcgemv<true>, dim3(grid), dim3(kGemvThreads), smem, s, pdl, p);
+  }
+  cudaError_t e = ensure_smem(k_tcgemv<false>, smem);
+  if (e != cudaSuccess) return e;
+  return launch_ex(k_tcgemv<false>, dim3(grid), dim3(kGemvThreads), smem, s, pdl, p);
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl) {

@@ -17,6 +17,13 @@ constexpr int kRouteChunkTokens = 32;
 constexpr int kSmallRouteMaxT = 16;
 
 // Routing workspace and outputs (all device pointers).
+// global-timer stamps per CTA written by the traced single-launch decode:
+// kTracePhases phase stamps, then two per work item (landed, computed) for
+// the first kTraceItems items of consumer warp 0
+constexpr int kTracePhases = 12;
+constexpr int kTraceItems = 8;
+constexpr int kTraceStamps = kTracePhases + 2 * kTraceItems;
+
 struct RouteArgs {
   const __half* x;      // [T][H]
   const float* wr;      // [E][H]
@@ -25,6 +32,7 @@ struct RouteArgs {
   int renorm;
   int has_shared;
   float* logits;        // [T][E]
+  float* logit_part;    // [T][E][16] partial logits (single-launch decode), or nullptr
   int32_t* ids;         // [T][k] workspace copy
   float* w;             // [T][k] workspace copy
   int32_t* ids_user;    // [T][k] or nullptr
@@ -41,36 +49,6 @@ struct RouteArgs {
   int32_t* num_seg;     // [1]
   uint32_t* ticket;     // [1], zero between launches
   uint32_t* err;        // [1]
-};
-
-// Grouped W4A16 GEMV over expert segments (decode regime).
-struct GemvArgs {
-  const uint8_t* pool;          // slot pool base
-  long long record_bytes;
-  const int32_t* expert_to_slot;
-  int num_slots;
-  long long q_off0, q_off1;     // code sections (gate, up) or (down, -)
-  long long s_off0, s_off1;     // scale sections
-  int N;                        // output rows per matrix
-  int K;                        // reduction length
-  int G;                        // group size
-  int ng;                       // ceil(K / G)
-  int lpr;                      // lanes per row (power of two, 4..32)
-  int rb;                       // rows per work item (multiple of 8)
-  const int32_t* num_seg;
-  const int32_t* seg_expert;
-  const int32_t* seg_start;
-  const int32_t* seg_count;
-  const __half* act;            // gate/up: x [T][K]; down: h [P][K]
-  int act_gather;               // 1: row of sorted position p is x[perm[p] / k] (p < Tk) or x[p - Tk]
-  const int32_t* perm;
-  int Tk;                       // T * k
-  int k;
-  __half* h_out;                // DUAL: [P][N] FP16 at sorted positions
-  float* y_out;                 // single: [Tk + T][N] FP32 at flat index f = perm[p] (p < Tk) or p
-  int stages;
-  uint32_t stage_bytes;
-  uint32_t* err;
 };
 
 // Grouped W4A16 GEMM over expert segments (prefill regime, tensor cores).
@@ -94,22 +72,86 @@ struct GemmArgs {
 };
 
 // Whole-layer decode megakernel (T <= kSmallRouteMaxT, full residency).
+// Tensor-core grouped GEMV over expert segments (decode regime): items of
+// rb rows (rt = rb / 16 row tiles) of one or two matrices, codes in 128-byte
+// swizzled TMA boxes.
+struct TcGemvArgs {
+  const uint8_t* pool;          // slot pool base (scale sections are read from it)
+  long long record_bytes;
+  const int32_t* expert_to_slot;
+  int num_slots;
+  long long s_off0, s_off1;     // scale sections (gate, up) or (down, -)
+  int N;                        // output rows per matrix
+  int K;                        // reduction length (multiple of 32)
+  int G;                        // group size (multiple of 32)
+  int ng;                       // ceil(K / G)
+  int rb;                       // rows per work item (multiple of 16)
+  int rt;                       // rb / 16 (divides 8)
+  int kparts;                   // 8 / rt consumer warps per row tile
+  int nbox;                     // ceil(K / 256) code boxes per matrix row
+  uint32_t code_mat_bytes;      // nbox * 128 * rb
+  uint32_t sstride;             // scale bytes per matrix in a slot (16-byte multiple)
+  const int32_t* seg_expert;
+  const int32_t* seg_start;
+  const int32_t* seg_count;
+  const __half* act;            // gate/up: x [T][K]; down: h [P][K]
+  int act_gather;               // 1: row of sorted position p is x[perm[p] / k] (p < Tk) or x[p - Tk]
+  const int32_t* perm;
+  int Tk;
+  int k;
+  __half* h_out;                // gate/up: [P][N] FP16 at sorted positions
+  float* y_out;                 // down: [Tk + T][N] FP32 at flat index
+  uint32_t* err;
+};
+
+struct TcGemvPlan {
+  int rb, rt, kparts, nbox;
+  uint32_t code_mat_bytes, sstride, slot_bytes;  // slot_bytes: multiple of 1024
+};
+// Items of about item_bytes code bytes with rb a power-of-two multiple of 16
+// and rb / 16 <= 8. Requires K % 32 == 0, G % 32 == 0, N % 16 == 0.
+TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes);
+// 3-D map {K / 2 bytes, N rows, slots} of one code section, 128-byte boxes of
+// box_rows rows, 128-byte swizzle.
+bool encode_tcgemv_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes,
+                       int box_rows);
+
+// Kernel parameters of the multi-kernel tensor-core GEMV.
+struct TcGemvLaunch {
+  TcGemvArgs a;
+  CUtensorMap m0, m1;           // code maps (gate, up) or (down, down)
+  const int32_t* num_seg;       // segment count (device)
+  int stages;
+  uint32_t slot_bytes;
+  int ns, bs_chunks, cs_groups;
+};
+size_t tcgemv_smem_bytes(const TcGemvLaunch& p);
+cudaError_t launch_tcgemv(const TcGemvLaunch& p, bool dual, int grid, cudaStream_t s, bool pdl);
+
 struct DecodeArgs {
   RouteArgs r;           // routing inputs and global outputs
-  GemvArgs g;            // gate/up items (segment pointers are replaced in-kernel)
-  GemvArgs d;            // down items
+  TcGemvArgs g;          // gate/up items (segment pointers are replaced in-kernel)
+  TcGemvArgs d;          // down items
+  CUtensorMap tm_gate, tm_up, tm_down;  // code maps (kernel parameter space)
   __half* out;           // [T][H]
   const __half* x_res;   // residual input or nullptr
   int has_shared;
   uint32_t* ctr;         // zeroed counters: logits_done, final ticket, done_gu[E+1], done_dn[]
   int stages;
-  uint32_t slot_bytes;   // ring slot size (max of the two item layouts)
+  uint32_t slot_bytes;   // ring slot size (max of the two item layouts, multiple of 1024)
+  int ns;                // token columns kept per tile (2, 4 or 8)
+  int bs_chunks;         // chunks (padded) the B buffer holds: max over gate/up and down K
+  int cs_groups;         // groups the constant buffer holds
+  unsigned long long* trace;  // nullable: [gridDim][kTraceStamps] global-timer stamps
 };
 
-// Tensor maps of the three code sections of a slot pool.
+// Tensor maps of the three code sections of a slot pool: GEMM tiles, and
+// the GEMV's 128-byte swizzled boxes.
 struct CodeMaps {
   CUtensorMap gate, up, down;
   bool valid;
+  CUtensorMap tgate, tup, tdown;
+  bool tvalid;
 };
 
 struct CombineArgs {
@@ -121,14 +163,6 @@ struct CombineArgs {
 };
 
 // Launch shape of one grouped-GEMV launch, chosen on the host.
-struct GemvPlan {
-  int lpr;              // lanes per row
-  int kch;              // 16-byte code chunks per lane per row
-  int nt;               // token tile (activations held in registers)
-  int rb;               // rows per work item
-  uint32_t stage_bytes; // shared-memory bytes per pipeline stage
-  int stages;           // pipeline depth
-};
 
 // Raise a kernel's dynamic shared-memory limit once per kernel (not per
 // launch, so launches can be captured into CUDA graphs without attribute
@@ -158,16 +192,14 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 
 cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_route_large(const RouteArgs& a, cudaStream_t s, bool pdl);
-GemvPlan plan_gemv(int N, int K, int G, bool dual, int T);
-bool gemv_plan_supported(const GemvPlan& p);
-cudaError_t launch_gemv(const GemvArgs& a, bool dual, const GemvPlan& p, int grid, cudaStream_t s, bool pdl);
-int gemv_kch(int K, int lpr);
-int gemv_lanes_per_row(int K);
-size_t gemv_smem_bytes(int stages, uint32_t stage_bytes);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
-size_t decode_smem_bytes(int stages, uint32_t slot_bytes);
-bool decode_supported(int kg, int ntg, int kd, int ntd);
-cudaError_t launch_decode(const DecodeArgs& a, int kg, int ntg, int kd, int ntd, int grid, cudaStream_t s);
+constexpr int kDecodeMaxStages = 8;  // ring stages of the single-launch decode
+// dynamic shared memory the ring kernels size themselves to: the 227 KB
+// per-block limit less room for static shared memory and the per-block
+// reservation
+constexpr size_t kSmemBudget = 227 * 1024 - 2048;
+size_t decode_smem_bytes(const DecodeArgs& a, int stages);
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gemm(bool dual, const CUtensorMap& codes0, const CUtensorMap& codes1, const CUtensorMap& act,
                         const GemmArgs& a, int grid, cudaStream_t s, bool pdl);
 size_t gemm_smem_bytes(bool dual);

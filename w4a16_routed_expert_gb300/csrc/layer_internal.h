@@ -52,6 +52,7 @@ struct moe_layer {
   // workspace (one allocation)
   void* ws = nullptr;
   float* logits = nullptr;
+  float* logit_part = nullptr;
   int32_t* ids = nullptr;
   float* wts = nullptr;
   int32_t* chunk_hist = nullptr;
@@ -75,11 +76,13 @@ struct moe_layer {
   int last_T = 0;
   bool megakernel = true;        // single-launch decode for T <= 16 (full residency)
   bool last_single = false;      // the last profiled forward was one launch
+  unsigned long long* trace = nullptr;  // per-CTA phase stamps of the single-launch decode (MOE_TRACE=1)
   uint32_t* ctr = nullptr;       // megakernel counters (zero between launches)
   // prefill (tensor-core) path
   int gemm_min_tokens = 256;
   bool gemm_ok = false;         // shapes suit the GEMM (H, I multiples of 64)
   moe::CodeMaps pool_maps = {};  // code sections of the caller's pool (full residency)
+  moe::TcGemvPlan dec_pg = {}, dec_pd = {};  // GEMV work items: gate/up, down
   CUtensorMap h_map = {};        // h workspace rows
   CUtensorMap x_map = {};        // tokens of the current forward
   bool profiling = false;

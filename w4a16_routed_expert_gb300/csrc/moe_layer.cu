@@ -93,6 +93,7 @@ size_t workspace_bytes(const moe_layer_config_t& c) {
   const size_t P = T * k + T;  // sorted positions incl. the shared segment
   size_t b = 0;
   b += align256(T * E * 4);             // logits
+  b += align256(std::min<size_t>(T, moe::kSmallRouteMaxT) * E * 16 * 4);  // logit partials
   b += 2 * align256(T * k * 4);         // ids, wts
   b += 2 * align256(nchunks * E * 4);   // chunk_hist, chunk_base
   b += align256(E * 4);                 // counts
@@ -105,6 +106,7 @@ size_t workspace_bytes(const moe_layer_config_t& c) {
   b += 2 * align256(T * H * 2);         // x/out staging
   b += align256(T * k * 4) * 2;         // ids/w staging
   b += align256(2048 * 4);              // megakernel counters
+  b += align256(1024 * moe::kTraceStamps * 8);  // phase trace (up to 1024 CTAs)
   return b;
 }
 
@@ -168,6 +170,7 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     const size_t P = T * k + T;
     char* p = static_cast<char*>(L->ws);
     L->logits = carve<float>(p, T * E);
+    L->logit_part = carve<float>(p, std::min<size_t>(T, moe::kSmallRouteMaxT) * E * 16);
     L->ids = carve<int32_t>(p, T * k);
     L->wts = carve<float>(p, T * k);
     L->chunk_hist = carve<int32_t>(p, nchunks * E);
@@ -190,6 +193,9 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     L->ids_stage = carve<int32_t>(p, T * k);
     L->w_stage = carve<float>(p, T * k);
     L->ctr = carve<uint32_t>(p, 2048);
+    unsigned long long* tr = carve<unsigned long long>(p, 1024 * 8);
+    const char* tr_env = getenv("MOE_TRACE");
+    if (tr_env && tr_env[0] == '1') L->trace = tr;
   }
   // zero the small control words (ticket, error word, segment count)
   e = cudaMemset(L->num_seg, 0, 4 * 256);
@@ -207,7 +213,10 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     const size_t P = (size_t)config->max_tokens * (config->top_k + 1);
     L->gemm_ok = (H % 64 == 0) && (I % 64 == 0) && P < (1u << 31) &&
                  moe::encode_rows_map(&L->h_map, L->hbuf, I, (int)P, moe::gemm_tile_n());
-    if (L->gemm_ok && config->residency == MOE_RESIDENCY_FULL)
+    // GEMV work items of about 32 KB of codes for both matrices' passes
+    L->dec_pg = moe::plan_tcgemv(I, H, config->group_size, true, 32768);
+    L->dec_pd = moe::plan_tcgemv(H, I, config->group_size, false, 32768);
+    if (config->residency == MOE_RESIDENCY_FULL)
       moe::encode_pool_maps(L, static_cast<const uint8_t*>(weights->slot_pool), config->num_slots, &L->pool_maps);
   }
   if (config->residency == MOE_RESIDENCY_PARTIAL) {
@@ -254,12 +263,16 @@ moe_status_t set_error(moe_status_t st, const char* fmt, ...) {
 // pool/e2s/num_slots select the record table.
 bool encode_pool_maps(const moe_layer* L, const uint8_t* pool, int num_slots, CodeMaps* maps) {
   const int H = L->cfg.hidden, I = L->cfg.intermediate;
-  const size_t rb = L->lay.record;
-  // gate/up tiles take 64 rows of each matrix, down tiles 128 rows
-  maps->valid = encode_codes_map(&maps->gate, pool + L->lay.off[0], H, I, num_slots, rb, 64) &&
-                encode_codes_map(&maps->up, pool + L->lay.off[1], H, I, num_slots, rb, 64) &&
-                encode_codes_map(&maps->down, pool + L->lay.off[2], I, H, num_slots, rb, 128);
-  return maps->valid;
+  const size_t rec = L->lay.record;
+  // GEMM: gate/up tiles take 64 rows of each matrix, down tiles 128 rows
+  maps->valid = L->gemm_ok && encode_codes_map(&maps->gate, pool + L->lay.off[0], H, I, num_slots, rec, 64) &&
+                encode_codes_map(&maps->up, pool + L->lay.off[1], H, I, num_slots, rec, 64) &&
+                encode_codes_map(&maps->down, pool + L->lay.off[2], I, H, num_slots, rec, 128);
+  // GEMV: one box row per item row
+  maps->tvalid = encode_tcgemv_map(&maps->tgate, pool + L->lay.off[0], H, I, num_slots, rec, L->dec_pg.rb) &&
+                 encode_tcgemv_map(&maps->tup, pool + L->lay.off[1], H, I, num_slots, rec, L->dec_pg.rb) &&
+                 encode_tcgemv_map(&maps->tdown, pool + L->lay.off[2], I, H, num_slots, rec, L->dec_pd.rb);
+  return maps->valid || maps->tvalid;
 }
 
 namespace {
@@ -318,65 +331,89 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   if (L->gemm_ok && maps && maps->valid && T >= L->gemm_min_tokens)
     return enqueue_gemm(L, x, T, s, pool, e2s, num_slots, seg, maps);
 
-  const GemvPlan pd = plan_gemv(I, H, G, true, T);
-  const GemvPlan ps = plan_gemv(H, I, G, false, T);
-  if (!gemv_plan_supported(pd) || !gemv_plan_supported(ps))
-    return fail(MOE_ERR_UNSUPPORTED, "no GEMV variant for H=%d I=%d", H, I);
-
-  GemvArgs gd = {};
-  gd.pool = pool;
-  gd.record_bytes = (long long)L->lay.record;
-  gd.expert_to_slot = e2s;
-  gd.num_slots = num_slots;
-  gd.q_off0 = L->lay.off[0];
-  gd.q_off1 = L->lay.off[1];
-  gd.s_off0 = L->lay.off[3];
-  gd.s_off1 = L->lay.off[4];
-  gd.N = I;
-  gd.K = H;
-  gd.G = G;
-  gd.ng = (H + G - 1) / G;
-  gd.lpr = pd.lpr;
-  gd.rb = pd.rb;
-  gd.num_seg = seg.num_seg;
-  gd.seg_expert = seg.seg_expert;
-  gd.seg_start = seg.seg_start;
-  gd.seg_count = seg.seg_count;
-  gd.act = x;
-  gd.act_gather = 1;
-  gd.perm = L->perm;
-  gd.Tk = T * k;
-  gd.k = k;
-  gd.h_out = L->hbuf;
-  gd.y_out = nullptr;
-  gd.stages = pd.stages;
-  gd.stage_bytes = pd.stage_bytes;
-  gd.err = L->err;
-  const int nrb_d = (I + pd.rb - 1) / pd.rb;
-  const int grid_d = std::max(1, std::min(L->num_sms, max_seg * nrb_d));
-  cudaError_t e = launch_gemv(gd, true, pd, grid_d, s, L->pdl);
+  if (!maps || !maps->tvalid) return fail(MOE_ERR_UNSUPPORTED, "no GEMV tensor maps for this pool");
+  const TcGemvPlan& pg = L->dec_pg;
+  const TcGemvPlan& pd = L->dec_pd;
+  TcGemvLaunch p = {};
+  TcGemvArgs& a = p.a;
+  a.pool = pool;
+  a.record_bytes = (long long)L->lay.record;
+  a.expert_to_slot = e2s;
+  a.num_slots = num_slots;
+  a.s_off0 = L->lay.off[3];
+  a.s_off1 = L->lay.off[4];
+  a.N = I;
+  a.K = H;
+  a.G = G;
+  a.ng = (H + G - 1) / G;
+  a.rb = pg.rb;
+  a.rt = pg.rt;
+  a.kparts = pg.kparts;
+  a.nbox = pg.nbox;
+  a.code_mat_bytes = pg.code_mat_bytes;
+  a.sstride = pg.sstride;
+  a.seg_expert = seg.seg_expert;
+  a.seg_start = seg.seg_start;
+  a.seg_count = seg.seg_count;
+  a.act = x;
+  a.act_gather = 1;
+  a.perm = L->perm;
+  a.Tk = T * k;
+  a.k = k;
+  a.h_out = L->hbuf;
+  a.y_out = nullptr;
+  a.err = L->err;
+  p.m0 = maps->tgate;
+  p.m1 = maps->tup;
+  p.num_seg = seg.num_seg;
+  p.slot_bytes = pg.slot_bytes;
+  // token columns: a segment holds at most T tokens
+  p.ns = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
+  p.bs_chunks = ((H / 32) + 1) & ~1;
+  p.cs_groups = a.ng;
+  p.stages = 0;
+  {
+    const size_t fixed = tcgemv_smem_bytes(p);
+    if (fixed + 2 * (size_t)p.slot_bytes > kSmemBudget) return fail(MOE_ERR_UNSUPPORTED, "GEMV item too large");
+    p.stages = (int)std::min<size_t>(kDecodeMaxStages, (kSmemBudget - fixed) / p.slot_bytes);
+  }
+  const int nrb_g = (I + pg.rb - 1) / pg.rb;
+  const int grid_g = std::max(1, std::min(L->num_sms, max_seg * nrb_g));
+  cudaError_t e = launch_tcgemv(p, true, grid_g, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[2], s, cudaEventRecordExternal);
 
-  GemvArgs gs = gd;
-  gs.q_off0 = L->lay.off[2];
-  gs.q_off1 = 0;
-  gs.s_off0 = L->lay.off[5];
-  gs.s_off1 = 0;
-  gs.N = H;
-  gs.K = I;
-  gs.ng = (I + G - 1) / G;
-  gs.lpr = ps.lpr;
-  gs.rb = ps.rb;
-  gs.act = L->hbuf;
-  gs.act_gather = 0;
-  gs.h_out = nullptr;
-  gs.y_out = L->ypart;
-  gs.stages = ps.stages;
-  gs.stage_bytes = ps.stage_bytes;
-  const int nrb_s = (H + ps.rb - 1) / ps.rb;
-  const int grid_s = std::max(1, std::min(L->num_sms, max_seg * nrb_s));
-  e = launch_gemv(gs, false, ps, grid_s, s, L->pdl);
+  TcGemvLaunch q = p;
+  TcGemvArgs& b = q.a;
+  b.s_off0 = L->lay.off[5];
+  b.s_off1 = 0;
+  b.N = H;
+  b.K = I;
+  b.ng = (I + G - 1) / G;
+  b.rb = pd.rb;
+  b.rt = pd.rt;
+  b.kparts = pd.kparts;
+  b.nbox = pd.nbox;
+  b.code_mat_bytes = pd.code_mat_bytes;
+  b.sstride = pd.sstride;
+  b.act = L->hbuf;
+  b.act_gather = 0;
+  b.h_out = nullptr;
+  b.y_out = L->ypart;
+  q.m0 = maps->tdown;
+  q.m1 = maps->tdown;
+  q.slot_bytes = pd.slot_bytes;
+  q.bs_chunks = ((I / 32) + 1) & ~1;
+  q.cs_groups = b.ng;
+  q.stages = 0;
+  {
+    const size_t fixed = tcgemv_smem_bytes(q);
+    if (fixed + 2 * (size_t)q.slot_bytes > kSmemBudget) return fail(MOE_ERR_UNSUPPORTED, "GEMV item too large");
+    q.stages = (int)std::min<size_t>(kDecodeMaxStages, (kSmemBudget - fixed) / q.slot_bytes);
+  }
+  const int nrb_d = (H + pd.rb - 1) / pd.rb;
+  const int grid_d = std::max(1, std::min(L->num_sms, max_seg * nrb_d));
+  e = launch_tcgemv(q, false, grid_d, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[3], s, cudaEventRecordExternal);
   return MOE_OK;
@@ -389,10 +426,9 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
                             cudaStream_t s) {
   const moe_layer_config_t& c = L->cfg;
   const int H = c.hidden, I = c.intermediate, E = c.num_experts, k = c.top_k, G = c.group_size;
-  const GemvPlan pg = plan_gemv(I, H, G, true, T);
-  const GemvPlan pd = plan_gemv(H, I, G, false, T);
-  if (!decode_supported(pg.kch, pg.nt, pd.kch, pd.nt) || (H + pd.rb - 1) / pd.rb > 2048 - 2 - (E + 1))
-    return MOE_ERR_UNSUPPORTED;
+  const TcGemvPlan& pg = L->dec_pg;
+  const TcGemvPlan& pd = L->dec_pd;
+  if (!L->pool_maps.tvalid || (H + pd.rb - 1) / pd.rb > 2048 - 2 - (E + 1)) return MOE_ERR_UNSUPPORTED;
   DecodeArgs a = {};
   RouteArgs& r = a.r;
   r.x = x;
@@ -405,6 +441,7 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   r.renorm = c.renormalize;
   r.has_shared = c.has_shared_expert;
   r.logits = L->logits;
+  r.logit_part = L->logit_part;
   r.ids = L->ids;
   r.w = L->wts;
   r.ids_user = ids_user;
@@ -418,52 +455,66 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   r.seg_count = L->seg_count;
   r.num_seg = L->num_seg;
   r.err = L->err;
-  GemvArgs& g = a.g;
+  TcGemvArgs& g = a.g;
   g.pool = static_cast<const uint8_t*>(L->w.slot_pool);
   g.record_bytes = (long long)L->lay.record;
   g.expert_to_slot = L->w.expert_to_slot;
   g.num_slots = c.num_slots;
-  g.q_off0 = L->lay.off[0];
-  g.q_off1 = L->lay.off[1];
   g.s_off0 = L->lay.off[3];
   g.s_off1 = L->lay.off[4];
   g.N = I;
   g.K = H;
   g.G = G;
   g.ng = (H + G - 1) / G;
-  g.lpr = pg.lpr;
   g.rb = pg.rb;
+  g.rt = pg.rt;
+  g.kparts = pg.kparts;
+  g.nbox = pg.nbox;
+  g.code_mat_bytes = pg.code_mat_bytes;
+  g.sstride = pg.sstride;
   g.act = x;
   g.act_gather = 1;
   g.Tk = T * k;
   g.k = k;
   g.h_out = L->hbuf;
   g.err = L->err;
-  GemvArgs& d = a.d;
+  TcGemvArgs& d = a.d;
   d = g;
-  d.q_off0 = L->lay.off[2];
-  d.q_off1 = 0;
   d.s_off0 = L->lay.off[5];
   d.s_off1 = 0;
   d.N = H;
   d.K = I;
   d.ng = (I + G - 1) / G;
-  d.lpr = pd.lpr;
   d.rb = pd.rb;
+  d.rt = pd.rt;
+  d.kparts = pd.kparts;
+  d.nbox = pd.nbox;
+  d.code_mat_bytes = pd.code_mat_bytes;
+  d.sstride = pd.sstride;
   d.act = L->hbuf;
   d.act_gather = 0;
   d.h_out = nullptr;
   d.y_out = L->ypart;
+  a.tm_gate = L->pool_maps.tgate;
+  a.tm_up = L->pool_maps.tup;
+  a.tm_down = L->pool_maps.tdown;
   a.out = out;
   a.x_res = c.add_residual ? x : nullptr;
   a.has_shared = c.has_shared_expert;
   a.ctr = L->ctr;
-  a.slot_bytes = std::max(pg.stage_bytes, pd.stage_bytes);
-  const size_t budget = 227 * 1024 - decode_smem_bytes(0, 0);
-  a.stages = (int)std::min<size_t>(8, budget / a.slot_bytes);
-  if (a.stages < 2) return MOE_ERR_UNSUPPORTED;
+  a.trace = L->trace;
+  a.slot_bytes = std::max(pg.slot_bytes, pd.slot_bytes);
+  // token columns per tile: the segment of an expert holds at most T tokens
+  a.ns = T <= 2 ? 2 : (T <= 4 ? 4 : 8);
+  const int kmax = std::max(H, I);
+  a.bs_chunks = ((kmax / 32) + 1) & ~1;
+  a.cs_groups = (kmax + G - 1) / G;
+  const size_t fixed = decode_smem_bytes(a, 0);
+  if (fixed + 2 * (size_t)a.slot_bytes > kSmemBudget) return MOE_ERR_UNSUPPORTED;
+  a.stages = (int)std::min<size_t>(kDecodeMaxStages, (kSmemBudget - fixed) / a.slot_bytes);
   if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
-  cudaError_t e = launch_decode(a, pg.kch, pg.nt, pd.kch, pd.nt, L->num_sms, s);
+  if (L->trace) cudaMemsetAsync(L->trace, 0, (size_t)L->num_sms * moe::kTraceStamps * 8, s);
+  cudaError_t e = launch_decode(a, L->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
   L->last_single = true;
@@ -665,6 +716,17 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* p) {
   p->active_experts = nseg - layer->cfg.has_shared_expert;
   p->tokens = layer->last_T;
   p->single_launch = layer->last_single ? 1 : 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_get_trace(moe_layer_t* layer, uint64_t* stamps, int32_t max_stamps, int32_t* n_stamps) {
+  if (!layer || !stamps || !n_stamps) return fail(MOE_ERR_INVALID_ARG, "layer, stamps and n_stamps must not be NULL");
+  if (!layer->trace) return fail(MOE_ERR_INVALID_ARG, "tracing is off (set MOE_TRACE=1 before create)");
+  const int n = std::min(max_stamps, layer->num_sms * moe::kTraceStamps);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(stamps, layer->trace, (size_t)n * 8, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "trace read");
+  *n_stamps = n;
   return MOE_OK;
 }
 

@@ -152,7 +152,7 @@ moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int 
   const int E = c.num_experts, k = c.top_k;
   if (!r->maps_tried) {
     r->maps_tried = true;
-    if (L->gemm_ok) encode_pool_maps(L, r->pool, r->num_slots, &r->maps);
+    encode_pool_maps(L, r->pool, r->num_slots, &r->maps);
   }
   // demanded experts: the only device -> host copy of the forward
   cudaError_t e = cudaMemcpyAsync(r->h_counts, L->counts, (size_t)E * sizeof(int32_t), cudaMemcpyDeviceToHost, s);

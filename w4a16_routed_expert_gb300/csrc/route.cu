@@ -28,18 +28,33 @@ namespace {
 
 constexpr int kRouteThreads = 256;
 
-// Router logits for T <= kSmallRouteMaxT tokens: one expert row per warp
-// (4 per CTA). The last CTA to finish (atomic ticket, no spinning) runs
-// top-k and the permutation for the whole batch.
+// Router logits for T <= kSmallRouteMaxT tokens: one CTA per expert, warp p
+// computes partial p of the row; the partials are summed in order (the same
+// two-level sum every small-batch path uses). The last CTA to finish
+// (atomic ticket, no spinning) runs top-k and the permutation for the batch.
 template <int NV>
-__global__ void __launch_bounds__(128) k_route_small(RouteArgs a) {
+__global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ __align__(16) float s_part[kSmallRouteMaxT * kLogitParts];
   __shared__ int s_scan[33];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int e = blockIdx.x;
   pdl_wait();
-  const int e = blockIdx.x * 4 + warp;
-  if (e < a.E) warp_expert_logits(a, e);
+  {
+    // partials into shared memory laid out as part[t][0][p] (E = 1 view)
+    RouteArgs one = a;
+    one.E = 1;
+    one.wr = a.wr + (size_t)e * a.H;
+    warp_logit_partial(one, 0, warp, s_part);
+  }
+  __syncthreads();
+  if (tid < a.T) {
+    float v = 0.f;
+#pragma unroll
+    for (int p = 0; p < kLogitParts; ++p) v += s_part[tid * kLogitParts + p];
+    a.logits[(size_t)tid * a.E + e] = v + (a.bias ? __ldg(a.bias + e) : 0.f);
+  }
 
   // the last CTA to finish its logits runs the rest of the routing
   __threadfence();
@@ -223,7 +238,7 @@ cudaError_t launch_route_small_nv(const RouteArgs& a, cudaStream_t s, bool pdl) 
   const size_t fbytes = ((size_t)a.T * a.k + 3 * (size_t)a.E + 66) * sizeof(int);
   cudaError_t e = ensure_smem(k_route_small<NV>, fbytes);
   if (e != cudaSuccess) return e;
-  return launch_ex(k_route_small<NV>, dim3((a.E + 3) / 4), dim3(128), fbytes, s, pdl, a);
+  return launch_ex(k_route_small<NV>, dim3(a.E), dim3(kLogitParts * 32), fbytes, s, pdl, a);
 }
 
 template <int NV>

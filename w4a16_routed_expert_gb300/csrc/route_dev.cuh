@@ -56,12 +56,70 @@ __device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* scrat
   return total;
 }
 
+// Router logits for T <= kSmallRouteMaxT tokens are summed in two fixed
+// levels: kLogitParts warp partials per expert row (each a lane-strided FP32
+// FMA chain over 1/kLogitParts of the row, then a butterfly), then the
+// partials in order p = 0..kLogitParts-1 plus the bias. Every small-batch path
+// uses these two functions, so they agree bit for bit.
+constexpr int kLogitParts = 16;
+
+// Partial p of expert e's logits for every token, written to part[t][e][p].
+__device__ __forceinline__ void warp_logit_partial(const RouteArgs& a, int e, int p, float* part) {
+  const int lane = threadIdx.x & 31;
+  const int T = a.T, H = a.H, E = a.E;
+  const int h4b = (p * (H / 4)) / kLogitParts, h4e = ((p + 1) * (H / 4)) / kLogitParts;
+  float acc[kSmallRouteMaxT];
+#pragma unroll
+  for (int t = 0; t < kSmallRouteMaxT; ++t) acc[t] = 0.f;
+  const float4* wr4 = reinterpret_cast<const float4*>(a.wr + (size_t)e * H) + h4b;
+  const uint2* x2 = reinterpret_cast<const uint2*>(a.x) + h4b;
+#pragma unroll 2
+  for (int h4 = lane; h4 < h4e - h4b; h4 += 32) {
+    const float4 wv = __ldg(wr4 + h4);
+#pragma unroll
+    for (int t = 0; t < kSmallRouteMaxT; ++t) {
+      if (t < T) {
+        const uint2 raw = __ldg(x2 + (size_t)t * (H / 4) + h4);
+        const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+        const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+        acc[t] = fmaf(wv.x, x01.x, acc[t]);
+        acc[t] = fmaf(wv.y, x01.y, acc[t]);
+        acc[t] = fmaf(wv.z, x23.x, acc[t]);
+        acc[t] = fmaf(wv.w, x23.y, acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kSmallRouteMaxT; ++t)
+    if (t < T) {
+      const float v = warp_sum(acc[t]);
+      if (lane == 0) part[((size_t)t * E + e) * kLogitParts + p] = v;
+    }
+}
+
+// Logit (t, e) from its kLogitParts partials (16 consecutive floats, read
+// through L2): summed in order, then the bias.
+__device__ __forceinline__ float logit_from_parts(const RouteArgs& a, const float* part, int t, int e) {
+  const float4* p4 = reinterpret_cast<const float4*>(part + ((size_t)t * a.E + e) * kLogitParts);
+  float v = 0.f;
+#pragma unroll
+  for (int q = 0; q < kLogitParts / 4; ++q) {
+    const float4 u = __ldcg(p4 + q);
+    v += u.x;
+    v += u.y;
+    v += u.z;
+    v += u.w;
+  }
+  return v + (a.bias ? __ldg(a.bias + e) : 0.f);
+}
+
 // One warp: softmax over the E logits of token t and selection of the top k
 // (largest logit first, lower id first among equal logits). NV = values held
 // per lane (E <= 32 * NV). Writes ids / weights to the workspace, the user
 // buffers (if any) and s_ids (chunk-local copy).
 template <int NV>
-__device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int32_t* s_ids_row) {
+__device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int32_t* s_ids_row,
+                                                  const float* part = nullptr) {
   const int lane = threadIdx.x & 31;
   const int E = a.E, k = a.k;
   const float* L = a.logits + (size_t)t * E;
@@ -69,7 +127,7 @@ __device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldcg(L + e) : -INFINITY;
+    v[i] = (e < E) ? (part ? logit_from_parts(a, part, t, e) : __ldcg(L + e)) : -INFINITY;
   }
   float m = -INFINITY;
 #pragma unroll
@@ -81,37 +139,80 @@ __device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int
     if (lane + 32 * i < E) ssum += expf(v[i] - m);
   ssum = warp_sum(ssum);
 
-  uint32_t taken = 0;
   float my_p = 0.f, psel = 0.f;
   int my_id = 0;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+  if constexpr (NV <= 4) {
+    // Rank selection (E <= 128): the rank of a logit is the number of logits
+    // ahead of it (larger, or equal with a lower id); the top k are ranks
+    // 0..k-1. Every comparison is independent, so the warp has no serial
+    // chain of k reductions.
+    int rank[NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      // within a lane e grows with i, so '>' keeps the lowest id of equal values
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
-        bv = v[i];
-        bi = e;
+    for (int i = 0; i < NV; ++i) rank[i] = 0;
+#pragma unroll 4
+    for (int o = 0; o < 32; ++o) {
+#pragma unroll
+      for (int i2 = 0; i2 < NV; ++i2) {
+        const float ov = __shfl_sync(0xffffffffu, v[i2], o);
+        const int oe = o + 32 * i2;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          const int e = lane + 32 * i;
+          rank[i] += (ov > v[i] || (ov == v[i] && oe < e)) ? 1 : 0;
+        }
       }
     }
+    // lane j takes the logit of rank j: walk the selected set (known to every
+    // lane through ballots) and pick the holder whose rank is j
+    float my_v = -INFINITY;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
-        bv = ov;
-        bi = oi;
+    for (int i2 = 0; i2 < NV; ++i2) {
+      uint32_t sel = __ballot_sync(0xffffffffu, lane + 32 * i2 < E && rank[i2] < k);
+      while (sel) {
+        const int src = __ffs(sel) - 1;
+        sel &= sel - 1;
+        const int r = __shfl_sync(0xffffffffu, rank[i2], src);
+        const float sv = __shfl_sync(0xffffffffu, v[i2], src);
+        if (r == lane) {
+          my_id = src + 32 * i2;
+          my_v = sv;
+        }
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    const float p = expf(bv - m) / ssum;
-    if (lane == j) {
-      my_p = p;
-      my_id = bi;
+    my_p = expf(my_v - m) / ssum;
+    for (int j = 0; j < k; ++j) psel += __shfl_sync(0xffffffffu, my_p, j);
+  } else {
+    // k rounds of a warp arg-max over the logits not yet taken
+    uint32_t taken = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        // within a lane e grows with i, so '>' keeps the lowest id of equal values
+        if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == 0x7fffffff)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      const float p = expf(bv - m) / ssum;
+      if (lane == j) {
+        my_p = p;
+        my_id = bi;
+      }
+      psel += p;
     }
-    psel += p;
   }
   if (lane < k) {
     const float wv = a.renorm ? my_p / psel : my_p;
@@ -236,65 +337,30 @@ __device__ __forceinline__ void finish_tiny(const RouteArgs& a, int32_t* s_ids, 
   for (int e = tid; e < a.E; e += blockDim.x) a.counts[e] = s_ids[32 + e + 1] - s_ids[32 + e];
 }
 
-// Router logits of expert e for the T <= kSmallRouteMaxT tokens of x, by one
-// warp: lane-strided FP32 FMA over the row in float4 steps, then a butterfly
-// sum. Every small-batch path uses this one function, so they agree bit for
-// bit on the logits (and hence on the selection).
-__device__ __forceinline__ void warp_expert_logits(const RouteArgs& a, int e) {
-  const int lane = threadIdx.x & 31;
-  const int T = a.T, H = a.H, E = a.E;
-  float acc[kSmallRouteMaxT];
-#pragma unroll
-  for (int t = 0; t < kSmallRouteMaxT; ++t) acc[t] = 0.f;
-  const float4* wr4 = reinterpret_cast<const float4*>(a.wr + (size_t)e * H);
-  const uint2* x2 = reinterpret_cast<const uint2*>(a.x);
-#pragma unroll 16
-  for (int h4 = lane; h4 < H / 4; h4 += 32) {
-    const float4 wv = __ldg(wr4 + h4);
-#pragma unroll
-    for (int t = 0; t < kSmallRouteMaxT; ++t) {
-      if (t < T) {
-        const uint2 raw = __ldg(x2 + (size_t)t * (H / 4) + h4);
-        const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-        const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-        acc[t] = fmaf(wv.x, x01.x, acc[t]);
-        acc[t] = fmaf(wv.y, x01.y, acc[t]);
-        acc[t] = fmaf(wv.z, x23.x, acc[t]);
-        acc[t] = fmaf(wv.w, x23.y, acc[t]);
-      }
-    }
-  }
-  const float b = a.bias ? __ldg(a.bias + e) : 0.f;
-#pragma unroll
-  for (int t = 0; t < kSmallRouteMaxT; ++t)
-    if (t < T) {
-      const float v = warp_sum(acc[t]);
-      if (lane == 0) a.logits[(size_t)t * E + e] = v + b;
-    }
-}
-
 // Top-k for all T tokens, the permutation and the segment list, computed by
 // one CTA (all its threads). scratch: >= T*k + 3*E + 66 ints of shared
 // memory; s_scan: 33 ints of shared memory.
 template <int NV>
-__device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* scratch, int* s_scan) {
+__device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* scratch, int* s_scan,
+                                                 const float* part = nullptr, unsigned long long* tr = nullptr) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k;
   int32_t* s_ids = scratch;
   if (T * k <= 32) {
     int32_t* s_sorted = s_ids + 32 + E + 1;
-    if (warp == 0)
-      for (int t = 0; t < T; ++t) warp_softmax_topk<NV>(a, t, s_ids + t * k);
+    for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
     __syncthreads();
+    if (tid == 0) trace_mark(tr, 3);
     finish_tiny(a, s_ids, s_sorted);
   } else {
     int* s_counts = s_ids + T * k;
     int* s_off = s_counts + E;
     int* s_cur = s_off + E + 1;
-    for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k);
+    for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
     for (int i = tid; i < E; i += blockDim.x) s_counts[i] = 0;
     __syncthreads();
+    if (tid == 0) trace_mark(tr, 3);
     for (int f = tid; f < T * k; f += blockDim.x) atomicAdd(&s_counts[s_ids[f]], 1);
     __syncthreads();
     for (int i = tid; i < E; i += blockDim.x) {
