@@ -19,10 +19,12 @@
 //   5. every down item counts on a per-row-block counter; the CTA that
 //      completes a row block performs the weighted combine for those rows
 //      (fixed order: ranks j = 0..k-1, then the shared expert).
-// Warp roles: 8 consumer warps compute items out of a shared-memory ring; one
-// producer warp fills the ring with TMA copies; one signalling warp turns
-// each finished item into its GPU-scope counter update (and runs the
-// combines), so that no consumer ever waits on a release or an atomic.
+// Warp roles: 16 consumer warps compute items out of a shared-memory ring and
+// hand their K-part partial sums over in shared memory; one producer warp
+// fills the ring with TMA copies; one finisher warp reduces the partials,
+// writes h or y, turns each finished item into its GPU-scope counter update
+// and runs the combines, so no consumer waits on an epilogue, a release or
+// an atomic.
 // Every cross-CTA wait is a bounded spin; on time-out the CTA records an
 // error, stops, lets its issued copies land and still passes the final
 // ticket, whose last holder resets all counters for the next launch.
@@ -39,8 +41,9 @@ constexpr int kDecodeThreads = (kTcWarps + 2) * 32;
 
 struct DecodeHdr {
   uint64_t full[kDecodeMaxStages];   // producer -> consumers: the item's bytes landed
-  uint64_t done[kDecodeMaxStages];   // consumers -> signaller: the item is computed
-  uint64_t empty[kDecodeMaxStages];  // signaller -> producer: the stage is free
+  uint64_t empty[kDecodeMaxStages];  // consumers -> producer: the stage is free
+  TcRedBars red;                     // consumers <-> finisher: K-part partials
+  int ncombine;                      // row blocks listed for the CTA-wide combine
   int abort_flag;
   int issued;
   int last;
@@ -124,7 +127,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(const DecodeArgs& a, in
   L.bs = L.ring + 1024u + (uint32_t)stages * a.slot_bytes;
   L.cs = L.bs + (uint32_t)a.bs_chunks * ns * 64u;
   L.red = L.cs + (((uint32_t)a.cs_groups * ns * 4u + 15u) & ~15u);
-  L.route = L.red + 2u * kTcWarps * 2u * 16u * ns * 4u;
+  L.route = L.red + ((2u * (uint32_t)tc_red_words((int)ns) * 4u + 15u) & ~15u);
   L.total = L.route + (5u * Tk + 8u * E + 74u) * 4u;
   return L;
 }
@@ -166,12 +169,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&hdr->full[s], 1);
-      mbar_init(&hdr->done[s], kTcWarps);
-      mbar_init(&hdr->empty[s], 1);
+      mbar_init(&hdr->empty[s], kTcWarps);
     }
+    tc_red_bars_init(&hdr->red);
     hdr->abort_flag = 0;
     hdr->issued = 0;
     hdr->last = 0;
+    hdr->ncombine = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -246,6 +250,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   const int ng_it = (int)((long long)(blockIdx.x + 1) * tot_g / gridDim.x) - fg;
   const int nd_it = (int)((long long)(blockIdx.x + 1) * tot_d / gridDim.x) - fd;
   const int n_it = *abort_flag ? 0 : ng_it + nd_it;
+  const int combine_cap = Tk + 3 * E + 66;      // the routing scratch, free after routing
   const uint32_t gu_target = (uint32_t)nrb_g;  // gate/up items per segment
   const uint32_t dn_target = (uint32_t)nseg;   // down items per row block
 
@@ -266,47 +271,83 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
       }
     }
   } else if (warp == kSignalWarp) {
-    // ---------------------------------------------------------- signaller
-    // Stage release first (the producer refills at once), then the counter:
-    // gate/up items add to their segment's counter, one release per run of
-    // already-finished items of that segment; down items count on their row
-    // block, and the item that completes it leads to that block's combine.
-    // The consumers' writes reach this warp through the `done` mbarrier
-    // (release / acquire at CTA scope); the GPU-scope release is cumulative.
+    // ----------------------------------------------------------- finisher
+    // Token tile by token tile (the consumers' order): wait for the K-part
+    // partials, write the outputs (h with SwiGLU, or y), free the buffer.
+    // Gate/up items add to their segment's counter, one release per run of
+    // this CTA's items of a segment; down items count on their row block
+    // once all of this CTA's down outputs are written, and the item that
+    // completes a row block leads to that block's combine. Every output this
+    // warp writes precedes its own GPU-scope release.
     uint32_t pending = 0;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % S;
-      const uint32_t ph = (uint32_t)(it / S) & 1u;
-      int ok = 1;
-      if (lane == 0) {
-        ok = mbar_wait(&hdr->done[st], ph, abort_flag, a.r.err);
-        if (ok) mbar_arrive(&hdr->empty[st]);
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      if (it < ng_it) {
-        if (lane == 0) {
-          const int sgi = (fg + it) / nrb_g;
-          ++pending;
-          const int nx = it + 1;
-          bool flush = true;
-          if (nx < ng_it && (fg + nx) / nrb_g == sgi)
-            flush = !mbar_try_wait(&hdr->done[nx % S], (uint32_t)(nx / S) & 1u);
-          if (flush) {
-            red_release_add(done_gu + sgi, pending);
-            pending = 0;
-          }
+    int ti = 0;
+    bool ok = true;
+    for (int it = 0; it < n_it && ok; ++it) {
+      const bool gu = it < ng_it;
+      const int item = gu ? fg + it : fd + it - ng_it;
+      const int nrb = gu ? nrb_g : nrb_d;
+      const int sgi = item / nrb, rbi = item - sgi * nrb;
+      const int cnt = s_scount[sgi];
+      for (int tb = 0; tb < cnt; tb += kTcMaxTok) {
+        const int ntok = min(kTcMaxTok, cnt - tb);
+        const int b = ti & 1;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&hdr->red.full[b], (uint32_t)(ti >> 1) & 1u, abort_flag, a.r.err);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
         }
-      } else {
-        const int rbi = (fd + it - ng_it) % nrb_d;
-        uint32_t prev = 0;
-        if (lane == 0) prev = atom_acq_rel_add(done_dn + rbi, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
+        const float* rbuf = red + b * tc_red_words(NS);
+        if (gu)
+          tc_finish_warp<true>(g, sgi, rbi, tb, ntok, NS, rbuf, lane);
+        else
+          tc_finish_warp<false>(d, sgi, rbi, tb, ntok, NS, rbuf, lane);
         __syncwarp();
-        // lane 0's acq_rel increment observed every other CTA's release
-        if (prev + 1 == dn_target) decode_combine_rows(a, d, rbi, s_w, lane);
+        if (lane == 0) mbar_arrive(&hdr->red.free_[b]);
+        ++ti;
+      }
+      if (!ok) break;
+      if (gu) {
+        // one release per run of this CTA's items of a segment
+        ++pending;
+        const int nx = it + 1;
+        if (nx >= ng_it || (fg + nx) / nrb_g != sgi) {
+          __syncwarp();
+          if (lane == 0) red_release_add(done_gu + sgi, pending);
+          pending = 0;
+        }
       }
     }
+    // down items: every y of this CTA written above; then one row-block count
+    // per item, lane i for item i, all in flight together. The row blocks
+    // this CTA completes are listed for the whole CTA to combine after the
+    // teardown barrier (or combined here if the list would overflow).
+    __syncwarp();
+    int nlist = 0;
+    for (int i0 = 0; ok && i0 < nd_it; i0 += 32) {
+      const int i = i0 + lane;
+      int last = 0;
+      if (i < nd_it) {
+        const int rbi = (fd + i) % nrb_d;
+        last = (atom_acq_rel_add(done_dn + rbi, 1u) + 1u == dn_target) ? 1 : 0;
+      }
+      uint32_t mask = __ballot_sync(0xffffffffu, last);
+      __syncwarp();
+      // each lane's acq_rel increment observed every other CTA's release
+      while (mask) {
+        const int l = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const int rbi = (fd + i0 + l) % nrb_d;
+        if (nlist < combine_cap) {
+          if (lane == 0) s_scratch[nlist] = rbi;
+          ++nlist;
+        } else {
+          decode_combine_rows(a, d, rbi, s_w, lane);
+        }
+      }
+    }
+    if (lane == 0) hdr->ncombine = nlist;
     if (lane == 0 && a.trace) {
       unsigned long long t;
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -317,11 +358,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
     // Every consumer warp runs the same sequence of named barriers (it
     // depends only on the routing in shared memory), also after a failed
     // wait: the work is then skipped in effect (stale data), never the
-    // barrier, so no warp can be left waiting.
+    // barrier, so no warp can be left waiting. Barriers are only needed when
+    // the B fragments are rebuilt; otherwise the warps run independently,
+    // handing their partials to the finisher through the two buffers.
     int b_seg = -1, b_tb = -1, b_gu = -1;  // token tile the B buffer holds
     int ready_seg = -1;
-    int buf = 0;
-    const int red_words = kTcWarps * 2 * 16 * NS;
+    int ti = 0;
     for (int it = 0; it < n_it; ++it) {
       const int st = it % S;
       const uint32_t ph = (uint32_t)(it / S) & 1u;
@@ -337,16 +379,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
       for (int tb = 0; tb < cnt; tb += kTcMaxTok) {
         const int ntok = min(kTcMaxTok, cnt - tb);
         if (sgi != b_seg || tb != b_tb || (int)gu != b_gu) {
+          tc_bar();  // every consumer warp is done with the previous B fragments
           if (gu) {
             tc_build_b<false>(g, sgi, tb, ntok, NS, Bs, Cs, tid);
           } else {
             if (sgi != ready_seg) {
               // h of this segment: every gate/up item of it, from every CTA
-              int ok = 1;
-              if (lane == 0) ok = wait_count(done_gu + sgi, gu_target, abort_flag, a.r.err);
-              ok = __shfl_sync(0xffffffffu, ok, 0);
+              int w = 1;
+              if (lane == 0) w = wait_count(done_gu + sgi, gu_target, abort_flag, a.r.err);
+              w = __shfl_sync(0xffffffffu, w, 0);
               __syncwarp();
-              (void)ok;  // on failure the abort flag is set; the barriers still run
+              (void)w;  // on failure the abort flag is set; the barriers still run
               ready_seg = sgi;
             }
             tc_build_b<true>(d, sgi, tb, ntok, NS, Bs, Cs, tid);
@@ -356,22 +399,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
           b_gu = gu;
           tc_bar();
         }
-        float* rb = red + buf * red_words;
+        const int b = ti & 1;
+        // the finisher has read this buffer (token tile ti - 2)
+        if (lane == 0) mbar_wait(&hdr->red.free_[b], ((uint32_t)(ti >> 1) & 1u) ^ 1u, abort_flag, a.r.err);
+        __syncwarp();
+        float* rbuf = red + b * tc_red_words(NS);
         if (gu) {
-          tc_compute<true>(g, slot, Bs, Cs, ntok, NS, rb, warp, lane);
-          tc_bar();
-          tc_finish<true>(g, item, nrb, tb, ntok, NS, rb, tid);
+          tc_compute<true>(g, slot, Bs, Cs, ntok, NS, rbuf, warp, lane);
         } else {
           if (it == ng_it && tb == 0) trace_mark(tr, 7);
-          tc_compute<false>(d, slot, Bs, Cs, ntok, NS, rb, warp, lane);
-          tc_bar();
-          tc_finish<false>(d, item, nrb, tb, ntok, NS, rb, tid);
+          tc_compute<false>(d, slot, Bs, Cs, ntok, NS, rbuf, warp, lane);
         }
-        buf ^= 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hdr->red.full[b]);
+        ++ti;
       }
       if (gu && it == ng_it - 1) trace_mark(tr, 6);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&hdr->done[st]);
+      if (lane == 0) mbar_arrive(&hdr->empty[st]);  // the slot's bytes are no longer read
       if (it < kTraceItems) trace_mark(tr, kTracePhases + 2 * it + 1);
     }
     trace_mark(tr, 8);
@@ -380,6 +425,33 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   // ---------------------------------------------------------------- teardown
   __syncthreads();
   trace_mark(tr, 10);
+  {
+    // combine of the row blocks this CTA completed, every thread of the CTA:
+    // out[t][row] = sum_j w[t][j] * y[(t, j)][row], then the shared expert,
+    // the FP16 rounding and the residual (as decode_combine_rows)
+    const int nl = hdr->ncombine;
+    const int H = a.r.H;
+    for (int q = tid; q < nl * d.rb * T; q += blockDim.x) {
+      const int li = q / (d.rb * T), rem = q - li * (d.rb * T);
+      const int t = rem / d.rb, row = s_scratch[li] * d.rb + rem % d.rb;
+      if (row >= H) continue;
+      const float* yp = d.y_out + (size_t)t * k * H + row;
+      float acc = 0.f;
+      int j = 0;
+      for (; j + 8 <= k; j += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(yp + (size_t)(j + u) * H);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) acc = fmaf(s_w[t * k + j + u], v[u], acc);
+      }
+      for (; j < k; ++j) acc = fmaf(s_w[t * k + j], __ldcg(yp + (size_t)j * H), acc);
+      if (a.has_shared) acc += __ldcg(d.y_out + (size_t)(Tk + t) * H + row);
+      __half o = __float2half_rn(acc);
+      if (a.x_res) o = __float2half_rn(__half2float(a.x_res[(size_t)t * H + row]) + __half2float(o));
+      a.out[(size_t)t * H + row] = o;
+    }
+  }
   if (tid == 0 && hdr->abort_flag) {
     const int issued = hdr->issued;
     for (int s = 0; s < S && s < issued; ++s) {
@@ -429,9 +501,11 @@ TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes) {
   TcGemvPlan p;
   const int mats = dual ? 2 : 1;
   p.rb = 16;
-  while (p.rb * 2 <= N && p.rb * 2 / 16 <= kTcWarps && mats * (p.rb * 2) * (K / 2) <= item_bytes) p.rb *= 2;
+  while (p.rb * 2 <= N && p.rb * 2 / 16 <= kTcMaxRowTiles && mats * (p.rb * 2) * (K / 2) <= item_bytes) p.rb *= 2;
   p.rt = p.rb / 16;
   p.kparts = kTcWarps / p.rt;
+  p.lkparts = 0;
+  while ((1 << p.lkparts) < p.kparts) ++p.lkparts;
   p.nbox = (K / 2 + 127) / 128;
   p.code_mat_bytes = (uint32_t)p.nbox * 128u * (uint32_t)p.rb;
   const int ng = (K + G - 1) / G;

@@ -8,8 +8,9 @@
 // Work item = (expert segment, block of rb output rows). A persistent CTA
 // (one per SM) walks a balanced contiguous range of items. Its producer
 // thread copies each item's codes (TMA, 128-byte swizzled boxes) and FP16
-// scales (bulk copy) into a ring of shared-memory stages; eight consumer
-// warps compute the item on the tensor cores with the device functions of
+// scales (bulk copy) into a ring of shared-memory stages; sixteen consumer
+// warps compute the item on the tensor cores and a finisher warp writes the
+// outputs from their partial sums with the device functions of
 // tcgemv_dev.cuh, which the single-launch decode kernel shares, so both paths
 // produce the same bits for the same plan.
 #include <algorithm>
@@ -20,9 +21,12 @@ namespace moe {
 
 namespace {
 
+constexpr int kGemvWarps = kTcWarps + 2;  // consumers, producer, finisher
+
 struct GemvHdr {
   uint64_t full[kDecodeMaxStages];
   uint64_t empty[kDecodeMaxStages];
+  TcRedBars red;
   int abort_flag;
   int issued;
 };
@@ -38,12 +42,12 @@ GemvSmem __host__ __device__ inline gemv_smem_layout(const TcGemvLaunch& p) {
   L.bs = L.ring + 1024u + (uint32_t)p.stages * p.slot_bytes;
   L.cs = L.bs + (uint32_t)p.bs_chunks * ns * 64u;
   L.red = L.cs + (((uint32_t)p.cs_groups * ns * 4u + 15u) & ~15u);
-  L.total = L.red + 2u * kTcWarps * 2u * 16u * ns * 4u;
+  L.total = L.red + ((2u * (uint32_t)tc_red_words((int)ns) * 4u + 15u) & ~15u);
   return L;
 }
 
 template <bool DUAL>
-__global__ void __launch_bounds__(kGemvThreads, 1) k_tcgemv(const __grid_constant__ TcGemvLaunch p) {
+__global__ void __launch_bounds__(kGemvWarps * 32, 1) k_tcgemv(const __grid_constant__ TcGemvLaunch p) {
   extern __shared__ __align__(128) unsigned char smem[];
   GemvHdr* hdr = reinterpret_cast<GemvHdr*>(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -60,6 +64,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_tcgemv(const __grid_constan
       mbar_init(&hdr->full[s], 1);
       mbar_init(&hdr->empty[s], kTcWarps);
     }
+    tc_red_bars_init(&hdr->red);
     hdr->abort_flag = 0;
     hdr->issued = 0;
     fence_mbar_init();
@@ -88,13 +93,38 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_tcgemv(const __grid_constan
         hdr->issued = it + 1;
       }
     }
+  } else if (warp == kTcWarps + 1) {
+    // ----------------------------------------------------------- finisher
+    // token tile by token tile: K-part partials -> h (SwiGLU) or y
+    int ti = 0;
+    bool ok = true;
+    for (int it = 0; it < nitems && ok; ++it) {
+      const int item = first + it;
+      const int sgi = item / nrb, rbi = item - sgi * nrb;
+      const int cnt = a.seg_count[sgi];
+      for (int tb = 0; tb < cnt; tb += kTcMaxTok) {
+        const int b = ti & 1;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&hdr->red.full[b], (uint32_t)(ti >> 1) & 1u, &hdr->abort_flag, a.err);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          ok = false;
+          break;
+        }
+        tc_finish_warp<DUAL>(a, sgi, rbi, tb, min(kTcMaxTok, cnt - tb), NS, red + b * tc_red_words(NS), lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hdr->red.free_[b]);
+        ++ti;
+      }
+    }
   } else {
     // ----------------------------------------------------------- consumers
     // The named-barrier sequence depends only on the segment list, so every
     // consumer warp runs it in full, also after a failed (bounded) wait.
+    // Barriers are only needed when the B fragments are rebuilt; partials go
+    // to the finisher through the two buffers.
     int b_seg = -1, b_tb = -1;
-    int buf = 0;
-    const int red_words = kTcWarps * 2 * 16 * NS;
+    int ti = 0;
     for (int it = 0; it < nitems; ++it) {
       const int st = it % S;
       const uint32_t ph = (uint32_t)(it / S) & 1u;
@@ -106,16 +136,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1) k_tcgemv(const __grid_constan
       for (int tb = 0; tb < cnt; tb += kTcMaxTok) {
         const int ntok = min(kTcMaxTok, cnt - tb);
         if (sgi != b_seg || tb != b_tb) {
+          tc_bar();  // every consumer warp is done with the previous B fragments
           tc_build_b<false>(a, sgi, tb, ntok, NS, Bs, Cs, tid);
           b_seg = sgi;
           b_tb = tb;
           tc_bar();
         }
-        float* rb = red + buf * red_words;
-        tc_compute<DUAL>(a, slot, Bs, Cs, ntok, NS, rb, warp, lane);
-        tc_bar();
-        tc_finish<DUAL>(a, item, nrb, tb, ntok, NS, rb, tid);
-        buf ^= 1;
+        const int b = ti & 1;
+        // the finisher has read this buffer (token tile ti - 2)
+        if (lane == 0) mbar_wait(&hdr->red.free_[b], ((uint32_t)(ti >> 1) & 1u) ^ 1u, &hdr->abort_flag, a.err);
+        __syncwarp();
+        tc_compute<DUAL>(a, slot, Bs, Cs, ntok, NS, red + b * tc_red_words(NS), warp, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hdr->red.full[b]);
+        ++ti;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&hdr->empty[st]);
@@ -181,11 +215,11 @@ cudaError_t launch_tcgemv(const TcGemvLaunch& p, bool dual, int grid, cudaStream
   if (dual) {
     cudaError_t e = ensure_smem(k_tcgemv<true>, smem);
     if (e != cudaSuccess) return e;
-    return launch_ex(k_tcgemv<true>, dim3(grid), dim3(kGemvThreads), smem, s, pdl, p);
+    return launch_ex(k_tcgemv<true>, dim3(grid), dim3(kGemvWarps * 32), smem, s, pdl, p);
   }
   cudaError_t e = ensure_smem(k_tcgemv<false>, smem);
   if (e != cudaSuccess) return e;
-  return launch_ex(k_tcgemv<false>, dim3(grid), dim3(kGemvThreads), smem, s, pdl, p);
+  return launch_ex(k_tcgemv<false>, dim3(grid), dim3(kGemvWarps * 32), smem, s, pdl, p);
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl) {

@@ -86,8 +86,9 @@ struct TcGemvArgs {
   int G;                        // group size (multiple of 32)
   int ng;                       // ceil(K / G)
   int rb;                       // rows per work item (multiple of 16)
-  int rt;                       // rb / 16 (divides 8)
-  int kparts;                   // 8 / rt consumer warps per row tile
+  int rt;                       // rb / 16 (1, 2, 4 or 8)
+  int kparts;                   // consumer warps per row tile (consumer warps / rt), a power of two
+  int lkparts;                  // log2(kparts)
   int nbox;                     // ceil(K / 256) code boxes per matrix row
   uint32_t code_mat_bytes;      // nbox * 128 * rb
   uint32_t sstride;             // scale bytes per matrix in a slot (16-byte multiple)
@@ -105,7 +106,7 @@ struct TcGemvArgs {
 };
 
 struct TcGemvPlan {
-  int rb, rt, kparts, nbox;
+  int rb, rt, kparts, lkparts, nbox;
   uint32_t code_mat_bytes, sstride, slot_bytes;  // slot_bytes: multiple of 1024
 };
 // Items of about item_bytes code bytes with rb a power-of-two multiple of 16

@@ -349,6 +349,7 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   a.rb = pg.rb;
   a.rt = pg.rt;
   a.kparts = pg.kparts;
+  a.lkparts = pg.lkparts;
   a.nbox = pg.nbox;
   a.code_mat_bytes = pg.code_mat_bytes;
   a.sstride = pg.sstride;
@@ -393,6 +394,7 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   b.rb = pd.rb;
   b.rt = pd.rt;
   b.kparts = pd.kparts;
+  b.lkparts = pd.lkparts;
   b.nbox = pd.nbox;
   b.code_mat_bytes = pd.code_mat_bytes;
   b.sstride = pd.sstride;
@@ -469,6 +471,7 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   g.rb = pg.rb;
   g.rt = pg.rt;
   g.kparts = pg.kparts;
+  g.lkparts = pg.lkparts;
   g.nbox = pg.nbox;
   g.code_mat_bytes = pg.code_mat_bytes;
   g.sstride = pg.sstride;
@@ -488,6 +491,7 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   d.rb = pd.rb;
   d.rt = pd.rt;
   d.kparts = pd.kparts;
+  d.lkparts = pd.lkparts;
   d.nbox = pd.nbox;
   d.code_mat_bytes = pd.code_mat_bytes;
   d.sstride = pd.sstride;

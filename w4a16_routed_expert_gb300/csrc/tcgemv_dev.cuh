@@ -25,9 +25,11 @@
 // Work split inside an item of rb rows (rt = rb / 16 row tiles) and M
 // matrices (2 for gate/up, 1 for down): consumer warp w takes row tile
 // w / kparts and the quantisation groups of K part w % kparts (kparts =
-// 8 / rt), for all M matrices at once (one B fragment load serves both gate
-// and up). Partial sums go to shared memory and are reduced over the K parts
-// in a fixed order; the gate/up epilogue applies SwiGLU.
+// kTcWarps / rt), for all M matrices at once (one B fragment load serves
+// both gate and up). Partial sums go to shared memory and are reduced over
+// the K parts in a fixed order; the gate/up epilogue applies SwiGLU. Sixteen
+// consumer warps per SM: a warp's dequantise -> MMA chain is latency bound,
+// and measured throughput per SM grows with the number of such warps.
 #pragma once
 
 #include <cuda.h>
@@ -38,10 +40,10 @@
 
 namespace moe {
 
-constexpr int kTcWarps = 8;          // consumer warps sharing an item
+constexpr int kTcWarps = 16;         // consumer warps sharing an item
+constexpr int kTcMaxRowTiles = 8;    // 16-row tiles per item (kparts = kTcWarps / tiles >= 2)
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcMaxTok = 8;         // tokens per MMA column tile
-constexpr int kGemvThreads = kTcThreads + 32;  // consumers + one producer warp
 constexpr int kHdrBytes = 256;       // mbarrier header at the start of dynamic shared memory
 
 // TMA tensor load with an L2 cache policy.
@@ -131,6 +133,13 @@ __device__ __forceinline__ void tc_issue_item(const TcGemvArgs& a, const CUtenso
 // far inside the layer's FP16 output rounding).
 __device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
+// K-part partial sums in shared memory: per (consumer warp, matrix) a block
+// of 16 rows x NS tokens, blocks tc_red_block(NS) floats apart. The odd
+// stride puts the K parts of one output in distinct banks for the finish.
+__host__ __device__ constexpr int tc_red_block(int ns) { return 16 * ns + 1; }
+// floats of one partial buffer (two matrices)
+__host__ __device__ constexpr int tc_red_words(int ns) { return kTcWarps * 2 * tc_red_block(ns); }
+
 // Consumer-only barrier (the kTcWarps consumer warps, named barrier 1).
 __device__ __forceinline__ void tc_bar() { asm volatile("bar.sync 1, %0;" ::"r"(kTcThreads) : "memory"); }
 
@@ -148,8 +157,9 @@ __device__ __forceinline__ void tc_build_b(const TcGemvArgs& a, int sgi, int tb,
   const int nchunk = K >> 5, nch_pad = (nchunk + 1) & ~1;
   const int pos0 = a.seg_start[sgi] + tb;
   const int total = nch_pad * NS * 4;
+  const int lns = NS == 2 ? 1 : (NS == 4 ? 2 : 3);  // NS is 2, 4 or 8
   for (int e = tc; e < total; e += kTcThreads) {
-    const int c = e & 3, n = (e >> 2) % NS, j = e / (4 * NS);
+    const int c = e & 3, n = (e >> 2) & (NS - 1), j = e >> (2 + lns);
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
     if (n < ntok && j < nchunk) {
       const int pos = pos0 + n;
@@ -170,7 +180,7 @@ __device__ __forceinline__ void tc_build_b(const TcGemvArgs& a, int sgi, int tb,
   // thread, fixed summation order: chunks, then c, then the four pairs
   const int cpg = a.G >> 5;
   for (int q = tc; q < a.ng * NS; q += kTcThreads) {
-    const int gi = q / NS, n = q % NS;
+    const int gi = q >> lns, n = q & (NS - 1);
     float se = 0.f, so = 0.f;
     if (n < ntok) {
       const int j1 = min((gi + 1) * cpg, nchunk);
@@ -198,10 +208,10 @@ template <bool DUAL, int CPG>
 __device__ __forceinline__ void tc_compute_g(const TcGemvArgs& a, const unsigned char* sb, const uint4* Bs,
                                              const float* Cs, int ntok, int NS, float* red, int warp, int lane) {
   constexpr int M = DUAL ? 2 : 1;
-  const int u = warp / a.kparts, kp = warp % a.kparts;
+  const int u = warp >> a.lkparts, kp = warp & (a.kparts - 1);
   const int g = lane >> 2, c = lane & 3;
   const int nchunk = a.K >> 5;
-  const int g0 = kp * a.ng / a.kparts, g1 = (kp + 1) * a.ng / a.kparts;
+  const int g0 = (kp * a.ng) >> a.lkparts, g1 = ((kp + 1) * a.ng) >> a.lkparts;
   // ldmatrix source of this lane: matrix lane / 8 = rows (mi & 1) * 8 + lane % 8 of chunk j + (mi >> 1).
   // Chunk pairs start at even j, so the pair's box is j / 8 and the
   // swizzled 16-byte column is ((j % 8) + (mi >> 1)) ^ (lane % 8).
@@ -266,10 +276,11 @@ __device__ __forceinline__ void tc_compute_g(const TcGemvArgs& a, const unsigned
       acc[m][3] = fmaf(s8, d[m][3] - cc1, acc[m][3]);
     }
   }
-  float* rw = red + (size_t)warp * M * 16 * NS;
+  const int blk = tc_red_block(NS);
+  float* rw = red + (size_t)warp * M * blk;
 #pragma unroll
   for (int m = 0; m < M; ++m) {
-    float* rm = rw + m * 16 * NS;
+    float* rm = rw + m * blk;
     if (2 * c < NS) {
       rm[g * NS + 2 * c] = acc[m][0];
       rm[(g + 8) * NS + 2 * c] = acc[m][2];
@@ -290,37 +301,43 @@ __device__ __forceinline__ void tc_compute(const TcGemvArgs& a, const unsigned c
     tc_compute_g<DUAL, 4>(a, sb, Bs, Cs, ntok, NS, red, warp, lane);
 }
 
-// Outputs of an item's token tile from the K-part partials (all consumer
-// threads, after the partials are complete): gate/up -> h (FP16, SwiGLU),
-// down -> y (FP32) at flat index perm[pos] (pos < Tk) or pos.
+// Outputs of an item's token tile from the K-part partials, by one warp (the
+// finisher): gate/up -> h (FP16, SwiGLU), down -> y (FP32) at flat index
+// perm[pos] (pos < Tk) or pos. Lane per output; the K parts are summed in
+// order kp = 0 .. kparts - 1.
 template <bool DUAL>
-__device__ __forceinline__ void tc_finish(const TcGemvArgs& a, int item, int nrb, int tb, int ntok, int NS,
-                                          const float* red, int tc) {
+__device__ __forceinline__ void tc_finish_warp(const TcGemvArgs& a, int sgi, int rbi, int tb, int ntok, int NS,
+                                               const float* red, int lane) {
   constexpr int M = DUAL ? 2 : 1;
-  const int sgi = item / nrb, rbi = item % nrb;
   const int r0 = rbi * a.rb;
   const int nrows = min(a.rb, a.N - r0);
   const int pos0 = a.seg_start[sgi] + tb;
-  const int per_tile = 16 * ntok;
-  for (int o = tc; o < a.rt * per_tile; o += kTcThreads) {
-    const int u = o / per_tile, r = (o % per_tile) / ntok, n = o % ntok;
+  const int kparts = a.kparts;
+  const int blk = tc_red_block(NS);
+  // outputs enumerated as ((u * ntok + n) * 16 + r); u = un / ntok by a
+  // multiply-shift that is exact for ntok <= 8 and un < 1024
+  const uint32_t inv_ntok = (65536u + (uint32_t)ntok - 1u) / (uint32_t)ntok;
+  const int outputs = a.rt * 16 * ntok;
+  for (int o = lane; o < outputs; o += 32) {
+    const int r = o & 15, un = o >> 4;
+    const int u = (int)(((uint32_t)un * inv_ntok) >> 16);
+    const int n = un - u * ntok;
     const int row = u * 16 + r;
     if (row >= nrows) continue;
-    // the K-part partials of this output, loaded together, summed in order
+    const float* base = red + (size_t)u * kparts * M * blk + r * NS + n;
     float p0[kTcWarps], p1[kTcWarps];
 #pragma unroll
     for (int kp = 0; kp < kTcWarps; ++kp) {
       p0[kp] = p1[kp] = 0.f;
-      if (kp < a.kparts) {
-        const float* rw = red + (size_t)(u * a.kparts + kp) * M * 16 * NS;
-        p0[kp] = rw[r * NS + n];
-        if (DUAL) p1[kp] = rw[16 * NS + r * NS + n];
+      if (kp < kparts) {
+        p0[kp] = base[(size_t)kp * M * blk];
+        if (DUAL) p1[kp] = base[(size_t)(kp * M + 1) * blk];
       }
     }
     float v0 = 0.f, v1 = 0.f;
 #pragma unroll
     for (int kp = 0; kp < kTcWarps; ++kp)
-      if (kp < a.kparts) {
+      if (kp < kparts) {
         v0 += p0[kp];
         v1 += p1[kp];
       }
@@ -334,5 +351,19 @@ __device__ __forceinline__ void tc_finish(const TcGemvArgs& a, int item, int nrb
   }
 }
 
+// Hand-off of the K-part partials between the consumer warps and the
+// finisher warp: two buffers used in turn (token tile ti uses buffer ti & 1);
+// red_full[b] counts the consumer warps that wrote buffer b, red_free[b] is
+// arrived by the finisher once it has read it.
+struct TcRedBars {
+  uint64_t full[2];
+  uint64_t free_[2];
+};
+__device__ __forceinline__ void tc_red_bars_init(TcRedBars* rb) {
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(&rb->full[b], kTcWarps);
+    mbar_init(&rb->free_[b], 1);
+  }
+}
 
 }  // namespace moe
