@@ -187,14 +187,16 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* prof
 
 /* Tracing of the single-launch decode path: when the handle was created
  * with the environment variable MOE_TRACE=1, every CTA of that kernel writes
- * 28 global-timer stamps (ns) per forward: 0 entry, 1 own logit partials
+ * 32 global-timer stamps (ns) per forward: 0 entry, 1 own logit partials
  * written, 2 all partials seen, 3 top-k done, 4 routing done, 5 first
  * gate/up item started, 6 last gate/up item done, 7 first down item started,
- * 8 consumers done, 9 signalling warp done, 10 all warps done, 11 exit; then
- * for the CTA's first 8 work items, item i's bytes landed (12 + 2i) and item
- * i computed (13 + 2i), as seen by consumer warp 0 (0 if fewer items).
- * Synchronises the device and copies min(max_stamps, 28 * CTAs) stamps,
- * CTA-major, into host memory; *n_stamps receives the count. */
+ * 8 consumers done, 9 finisher done, 10 all warps done, 11 exit, 12 first
+ * down wait entered, 13 its counter seen, 14 its activations staged, 15
+ * unused; then for the CTA's first 8 work items, item i's bytes landed
+ * (16 + 2i) and item i computed (17 + 2i), as seen by consumer warp 0 (0 if
+ * not reached). Synchronises the device and copies min(max_stamps,
+ * 32 * CTAs) stamps, CTA-major, into host memory; *n_stamps receives the
+ * count. */
 moe_status_t moe_layer_get_trace(moe_layer_t* layer, uint64_t* stamps, int32_t max_stamps, int32_t* n_stamps);
 
 /* Copies the handle's counters into *stats. */

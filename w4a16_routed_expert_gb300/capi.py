@@ -206,7 +206,7 @@ def moe_layer_get_profile(h) -> moe_layer_profile_t:
     return p
 
 
-TRACE_STAMPS = 28
+TRACE_STAMPS = 32
 
 
 def moe_layer_get_trace(h, max_stamps: int = 1024 * TRACE_STAMPS):

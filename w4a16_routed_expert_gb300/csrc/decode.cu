@@ -217,7 +217,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
     L.seg_start = s_sstart;
     L.seg_count = s_scount;
     L.num_seg = s_nseg;
-    route_finish_cta<NV>(L, s_scratch, s_scan, a.r.logit_part, tr);
+    // the ring is idle until routing is done: block top-k buffer
+    route_finish_cta<NV>(L, s_scratch, s_scan, a.r.logit_part, tr, reinterpret_cast<float*>(ring));
     __syncthreads();
     trace_mark(tr, 4);
     nseg = *s_nseg;
@@ -383,6 +384,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
           if (gu) {
             tc_build_b<false>(g, sgi, tb, ntok, NS, Bs, Cs, tid);
           } else {
+            const bool first_dn = ready_seg < 0;
+            if (first_dn) trace_mark(tr, 12);
             if (sgi != ready_seg) {
               // h of this segment: every gate/up item of it, from every CTA
               int w = 1;
@@ -392,7 +395,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
               (void)w;  // on failure the abort flag is set; the barriers still run
               ready_seg = sgi;
             }
+            if (first_dn) trace_mark(tr, 13);
             tc_build_b<true>(d, sgi, tb, ntok, NS, Bs, Cs, tid);
+            if (first_dn) trace_mark(tr, 14);
           }
           b_seg = sgi;
           b_tb = tb;

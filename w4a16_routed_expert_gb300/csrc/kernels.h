@@ -20,7 +20,7 @@ constexpr int kSmallRouteMaxT = 16;
 // global-timer stamps per CTA written by the traced single-launch decode:
 // kTracePhases phase stamps, then two per work item (landed, computed) for
 // the first kTraceItems items of consumer warp 0
-constexpr int kTracePhases = 12;
+constexpr int kTracePhases = 16;
 constexpr int kTraceItems = 8;
 constexpr int kTraceStamps = kTracePhases + 2 * kTraceItems;
 

@@ -213,9 +213,13 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     const size_t P = (size_t)config->max_tokens * (config->top_k + 1);
     L->gemm_ok = (H % 64 == 0) && (I % 64 == 0) && P < (1u << 31) &&
                  moe::encode_rows_map(&L->h_map, L->hbuf, I, (int)P, moe::gemm_tile_n());
-    // GEMV work items of about 32 KB of codes for both matrices' passes
-    L->dec_pg = moe::plan_tcgemv(I, H, config->group_size, true, 32768);
-    L->dec_pd = moe::plan_tcgemv(H, I, config->group_size, false, 32768);
+    // GEMV work items of about 64 KB of codes for both matrices' passes:
+    // two quantisation groups per consumer warp amortise the per-item work
+    // (MOE_GEMV_ITEM_BYTES overrides, for tuning)
+    int item_bytes = 65536;
+    if (const char* ib = getenv("MOE_GEMV_ITEM_BYTES")) item_bytes = std::max(4096, std::min(131072, atoi(ib)));
+    L->dec_pg = moe::plan_tcgemv(I, H, config->group_size, true, item_bytes);
+    L->dec_pd = moe::plan_tcgemv(H, I, config->group_size, false, item_bytes);
     if (config->residency == MOE_RESIDENCY_FULL)
       moe::encode_pool_maps(L, static_cast<const uint8_t*>(weights->slot_pool), config->num_slots, &L->pool_maps);
   }

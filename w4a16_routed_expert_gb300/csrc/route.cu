@@ -64,7 +64,11 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
   if (!s_last) return;
   __threadfence();
 
-  route_finish_cta<NV>(a, reinterpret_cast<int32_t*>(smem), s_scan);
+  // dynamic shared memory: the finish scratch (T*k + 3E + 66 ints), then
+  // the block top-k buffer (T*E + 2T + T*k floats)
+  int32_t* scratch = reinterpret_cast<int32_t*>(smem);
+  float* fbuf = reinterpret_cast<float*>(scratch + a.T * a.k + 3 * a.E + 66);
+  route_finish_cta<NV>(a, scratch, s_scan, nullptr, nullptr, fbuf);
   if (tid == 0) *a.ticket = 0u;
 }
 
@@ -235,7 +239,8 @@ __global__ void __launch_bounds__(32) k_scatter(RouteArgs a) {
 
 template <int NV>
 cudaError_t launch_route_small_nv(const RouteArgs& a, cudaStream_t s, bool pdl) {
-  const size_t fbytes = ((size_t)a.T * a.k + 3 * (size_t)a.E + 66) * sizeof(int);
+  const size_t fbytes = ((size_t)a.T * a.k + 3 * (size_t)a.E + 66) * sizeof(int) +
+                        ((size_t)a.T * a.E + 2 * (size_t)a.T + (size_t)a.T * a.k) * sizeof(float);
   cudaError_t e = ensure_smem(k_route_small<NV>, fbytes);
   if (e != cudaSuccess) return e;
   return launch_ex(k_route_small<NV>, dim3(a.E), dim3(kLogitParts * 32), fbytes, s, pdl, a);

@@ -337,19 +337,113 @@ __device__ __forceinline__ void finish_tiny(const RouteArgs& a, int32_t* s_ids, 
   for (int e = tid; e < a.E; e += blockDim.x) a.counts[e] = s_ids[32 + e + 1] - s_ids[32 + e];
 }
 
+// Softmax and top-k of all T tokens with every thread of the CTA (E <= 128):
+// the same results, bit for bit, as warp_softmax_topk, with the work spread
+// out. Each logit's rank (the number of logits of its token ahead of it:
+// larger, or equal with a lower id) is counted by 8 lanes over interleaved
+// eighths of the token's logits and summed with shuffles; ranks 0..k-1 are
+// the selection. The softmax maximum and denominator of a token are computed
+// by one warp exactly as in warp_softmax_topk. fbuf: T*E + 2T + T*k floats
+// of shared memory. Writes ids / weights to a.ids, a.w, the user buffers
+// (if any) and s_sel ([T][k], by rank).
+template <int NV>
+__device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const float* part, float* fbuf,
+                                                   int32_t* s_sel) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int T = a.T, E = a.E, k = a.k, n = T * E;
+  float* lg = fbuf;       // [T][E]
+  float* mx = lg + n;     // [T]
+  float* den = mx + T;    // [T]
+  float* sp = den + T;    // [T][k] probabilities by rank
+  for (int i = tid; i < n; i += blockDim.x) {
+    const int t = i / E, e = i - t * E;
+    lg[i] = part ? logit_from_parts(a, part, t, e) : __ldcg(a.logits + i);
+  }
+  for (int i = tid; i < T * k; i += blockDim.x) {
+    s_sel[i] = 0;  // defined even if NaN logits leave a rank unfilled
+    sp[i] = 0.f;
+  }
+  __syncthreads();
+  // maximum and denominator, one warp per token (as warp_softmax_topk)
+  for (int t = warp; t < T; t += nwarps) {
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? lg[t * E + e] : -INFINITY;
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) m = fmaxf(m, v[i]);
+    m = warp_max(m);
+    float ssum = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (lane + 32 * i < E) ssum += expf(v[i] - m);
+    ssum = warp_sum(ssum);
+    if (lane == 0) {
+      mx[t] = m;
+      den[t] = ssum;
+    }
+  }
+  __syncthreads();
+  // ranks: a warp takes 4 logits per round, 8 lanes each
+  const int sub = lane & 7;
+  for (int base = warp * 4; base < n; base += nwarps * 4) {
+    const int i = base + (lane >> 3);
+    const bool valid = i < n;
+    const int t = valid ? i / E : 0, e = valid ? i - t * E : 0;
+    const float v = valid ? lg[i] : 0.f;
+    int r = 0;
+    if (valid)
+      for (int e2 = sub; e2 < E; e2 += 8) {
+        const float o = lg[t * E + e2];
+        r += (o > v || (o == v && e2 < e)) ? 1 : 0;
+      }
+    r += __shfl_xor_sync(0xffffffffu, r, 1);
+    r += __shfl_xor_sync(0xffffffffu, r, 2);
+    r += __shfl_xor_sync(0xffffffffu, r, 4);
+    if (valid && sub == 0 && r < k) {
+      s_sel[t * k + r] = e;
+      sp[t * k + r] = expf(v - mx[t]) / den[t];
+    }
+  }
+  __syncthreads();
+  // routing weights: the selected probabilities summed in rank order
+  for (int o = tid; o < T * k; o += blockDim.x) {
+    const int t = o / k;
+    float psel = 0.f;
+    for (int j = 0; j < k; ++j) psel += sp[t * k + j];
+    const float p = sp[o];
+    const float wv = a.renorm ? p / psel : p;
+    const int id = s_sel[o];
+    a.ids[o] = id;
+    a.w[o] = wv;
+    if (a.ids_user) a.ids_user[o] = id;
+    if (a.w_user) a.w_user[o] = wv;
+  }
+}
+
 // Top-k for all T tokens, the permutation and the segment list, computed by
 // one CTA (all its threads). scratch: >= T*k + 3*E + 66 ints of shared
-// memory; s_scan: 33 ints of shared memory.
+// memory; s_scan: 33 ints of shared memory; fbuf (optional, used when
+// E <= 128): T*E + 2T + T*k floats of shared memory for the block-wide
+// top-k.
 template <int NV>
 __device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* scratch, int* s_scan,
-                                                 const float* part = nullptr, unsigned long long* tr = nullptr) {
+                                                 const float* part = nullptr, unsigned long long* tr = nullptr,
+                                                 float* fbuf = nullptr) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k;
   int32_t* s_ids = scratch;
+  const bool block_topk = NV <= 4 && fbuf != nullptr;
   if (T * k <= 32) {
     int32_t* s_sorted = s_ids + 32 + E + 1;
-    for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
+    if (block_topk)
+      block_softmax_topk<NV>(a, part, fbuf, s_ids);
+    else
+      for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
     finish_tiny(a, s_ids, s_sorted);
@@ -357,7 +451,10 @@ __device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* sc
     int* s_counts = s_ids + T * k;
     int* s_off = s_counts + E;
     int* s_cur = s_off + E + 1;
-    for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
+    if (block_topk)
+      block_softmax_topk<NV>(a, part, fbuf, s_ids);
+    else
+      for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
     for (int i = tid; i < E; i += blockDim.x) s_counts[i] = 0;
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
