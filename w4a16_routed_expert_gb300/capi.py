@@ -76,6 +76,7 @@ PROTOTYPES = {
     "moe_layer_get_stats": (_I32, [_P, ctypes.POINTER(moe_layer_stats_t)]),
     "moe_layer_set_profiling": (_I32, [_P, _I32]),
     "moe_layer_get_trace": (_I32, [_P, ctypes.POINTER(ctypes.c_uint64), _I32, ctypes.POINTER(_I32)]),
+    "moe_layer_get_gemm_stats": (_I32, [_P, ctypes.POINTER(ctypes.c_uint64), _I32, ctypes.POINTER(_I32)]),
     "moe_layer_get_profile": (_I32, [_P, ctypes.POINTER(moe_layer_profile_t)]),
     "moe_layer_destroy": (_I32, [_P]),
     "moe_layer_last_error": (ctypes.c_char_p, []),
@@ -213,6 +214,16 @@ def moe_layer_get_trace(h, max_stamps: int = 1024 * TRACE_STAMPS):
     buf = (ctypes.c_uint64 * max_stamps)()
     n = _I32()
     check(lib().moe_layer_get_trace(h, buf, max_stamps, ctypes.byref(n)), "moe_layer_get_trace")
+    return list(buf)[:n.value]
+
+
+GEMM_STATS = 9
+
+
+def moe_layer_get_gemm_stats(h, max_values: int = 2 * 1024 * GEMM_STATS):
+    buf = (ctypes.c_uint64 * max_values)()
+    n = _I32()
+    check(lib().moe_layer_get_gemm_stats(h, buf, max_values, ctypes.byref(n)), "moe_layer_get_gemm_stats")
     return list(buf)[:n.value]
 
 

@@ -13,9 +13,12 @@
 //
 // Warp roles of a persistent CTA (one per SM):
 //   warp 0      TMA producer: INT4 code tiles (3-D tensor map over the slot
-//               pool: bytes x rows x slot) and token tiles (gate/up: four-row
-//               gathers of x through the permutation; down: 2-D tiles of h,
-//               which is already in expert-sorted order)
+//               pool: bytes x rows x slot; one 128-byte-wide swizzled box
+//               covers four K steps) and token tiles (2-D 256-row boxes of
+//               the expert-sorted activations: x gathered in sorted order
+//               for gate/up, h for down). A 2-D box of 32 KB streams at ~45
+//               bytes per SM-cycle from L2 on this part, small boxes cost
+//               about as much each, so every K step is one large box.
 //   warp 1      TMEM allocation and the single MMA-issuing thread
 //   warps 2-9   dequantisers: codes -> (q - 8) * s in FP16, written in the
 //               128-byte-swizzled K-major layout the MMA reads
@@ -40,11 +43,12 @@ namespace {
 constexpr int BM = 128;  // MMA rows per tile (DUAL: 64 gate + 64 up, interleaved)
 constexpr int BN = 256;  // tokens per tile
 constexpr int BK = 64;   // K per pipeline step (128 bytes of FP16)
-constexpr int kCodeStages = 4;
+constexpr int kCodeK = 4;  // K steps per code tile: 128 bytes of codes per row, one swizzled TMA box
+constexpr int kCodeStages = 2;
 constexpr int kAStages = 3;
 constexpr int kBStages = 4;
 constexpr int kDequantWarps = 8;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each half of the columns
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpDequant0 = 2;
@@ -56,7 +60,7 @@ template <bool DUAL>
 struct Smem {
   static constexpr uint32_t a_tile = BM * BK * 2;      // 16 KB
   static constexpr uint32_t b_tile = BN * BK * 2;      // 32 KB
-  static constexpr uint32_t code_tile = BM * BK / 2;   // 4 KB (DUAL: 64 gate rows then 64 up rows)
+  static constexpr uint32_t code_tile = BM * kCodeK * BK / 2;  // 16 KB (DUAL: 64 gate rows then 64 up rows)
   static constexpr uint32_t off_a = 0;
   static constexpr uint32_t off_b = off_a + kAStages * a_tile;
   static constexpr uint32_t off_codes = off_b + kBStages * b_tile;
@@ -65,7 +69,8 @@ struct Smem {
   static constexpr uint32_t n_bars = 2 * kCodeStages + 2 * kAStages + 2 * kBStages + 4 + 1;
   static constexpr uint32_t off_misc = off_bar + n_bars * 8;
   static constexpr uint32_t off_prefix = off_misc + 64;
-  static constexpr uint32_t bytes = off_prefix + (kMaxSeg + 1) * 4;
+  static constexpr uint32_t off_epi = off_prefix + ((kMaxSeg + 1) * 4 + 15) / 16 * 16;  // [BN] output rows of a tile
+  static constexpr uint32_t bytes = off_epi + BN * 4;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
   static constexpr uint32_t tmem_cols = 512;
   static constexpr uint32_t acc_stride = BN;        // two accumulator buffers of 256 columns
@@ -92,6 +97,29 @@ struct Misc {
   int b_issued;
   int mma_issued;
 };
+
+// barriers of the epilogue warps only (named barrier 2); the second returns
+// whether any epilogue thread passed true
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, %0;" ::"r"(kEpiWarps * 32) : "memory"); }
+__device__ __forceinline__ bool epi_bar_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, 2, %2, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(kEpiWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+// mbar_wait that adds the cycles it spent to *acc (when acc is set)
+__device__ __forceinline__ bool timed_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err,
+                                           unsigned long long* acc) {
+  if (!acc) return mbar_wait(bar, parity, abort_flag, err);
+  const long long t0 = clock64();
+  const bool ok = mbar_wait(bar, parity, abort_flag, err);
+  *acc += (unsigned long long)(clock64() - t0);
+  return ok;
+}
 
 __device__ __forceinline__ int find_segment(const int* prefix, int nseg, int t) {
   int lo = 0, hi = nseg - 1;  // largest s with prefix[s] <= t
@@ -210,83 +238,80 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const int total = misc->total_tiles;
   const uint32_t tbase = misc->tmem_base;
+  unsigned long long* st_cta = a.stats ? a.stats + (size_t)blockIdx.x * kGemmStats : nullptr;
+  const long long t_start = clock64();
   const int nK = a.K / BK;
   volatile int* abort_flag = &misc->abort_flag;
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
-    uint32_t g = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const int s = find_segment(prefix, nseg, t);
-      const int local = t - prefix[s];
-      const int cnt = a.seg_count[s];
-      const int ntl = (cnt + BN - 1) / BN;
-      const int m0 = (local / ntl) * L::units, n0 = (local % ntl) * BN;
-      const int e = a.seg_expert[s];
-      int slot = a.expert_to_slot[e];
-      if (slot < 0 || slot >= a.num_slots) {
-        if (lane == 0) record_error(a.err, MOE_DEV_ERR_BOUNDS);
-        slot = 0;
-      }
-      const int pos0 = a.seg_start[s];
-      int rows[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (DUAL) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int tok = min(n0 + 8 * lane + i, cnt - 1);
-          const int p = pos0 + tok;
-          rows[i] = (p < a.Tk) ? (__ldg(a.perm + p) / a.k) : (p - a.Tk);
+    if (lane == 0) {
+      unsigned long long sw[2] = {0, 0};
+      uint32_t g = 0, gc = 0;  // K steps, code groups (both over all tiles of this CTA)
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int s = find_segment(prefix, nseg, t);
+        const int local = t - prefix[s];
+        const int cnt = a.seg_count[s];
+        const int ntl = (cnt + BN - 1) / BN;
+        const int m0 = (local / ntl) * L::units, n0 = (local % ntl) * BN;
+        const int e = a.seg_expert[s];
+        int slot = a.expert_to_slot[e];
+        if (slot < 0 || slot >= a.num_slots) {
+          record_error(a.err, MOE_DEV_ERR_BOUNDS);
+          slot = 0;
         }
-      }
-      for (int kk = 0; kk < nK; ++kk, ++g) {
-        const int sc = g % kCodeStages, sb = g % kBStages;
-        int good = 1;
-        if (lane == 0) {
-          good = mbar_wait(&B.codes_empty[sc], ((g / kCodeStages) & 1u) ^ 1u, abort_flag, a.err);
-          if (good) {
+        const int pos0 = a.seg_start[s];
+        for (int kk = 0; kk < nK; ++kk, ++g) {
+          if (kk % kCodeK == 0) {
+            // codes of K steps kk .. kk + kCodeK - 1: one box per matrix
+            const int sc = gc % kCodeStages;
+            if (!timed_wait(&B.codes_empty[sc], ((gc / kCodeStages) & 1u) ^ 1u, abort_flag, a.err,
+                            st_cta ? &sw[0] : nullptr)) {
+              ok = false;
+              break;
+            }
             unsigned char* cdst = smem + L::off_codes + (uint32_t)sc * L::code_tile;
             mbar_arrive_expect_tx(&B.codes_full[sc], L::code_tile);
-            tma_load_3d(cdst, &tm_codes0, kk * (BK / 2), m0, slot, &B.codes_full[sc]);
-            if (DUAL) tma_load_3d(cdst + L::code_tile / 2, &tm_codes1, kk * (BK / 2), m0, slot, &B.codes_full[sc]);
-            misc->codes_issued = (int)g + 1;
-            good = mbar_wait(&B.b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err);
-            if (good) mbar_arrive_expect_tx(&B.b_full[sb], L::b_tile);
+            const int cx = (kk / kCodeK) * (kCodeK * BK / 2);
+            tma_load_3d(cdst, &tm_codes0, cx, m0, slot, &B.codes_full[sc]);
+            if (DUAL) tma_load_3d(cdst + L::code_tile / 2, &tm_codes1, cx, m0, slot, &B.codes_full[sc]);
+            ++gc;
+            misc->codes_issued = (int)gc;
           }
+          const int sb = g % kBStages;
+          if (!timed_wait(&B.b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err, st_cta ? &sw[1] : nullptr)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&B.b_full[sb], L::b_tile);
+          tma_load_2d(smem + L::off_b + (uint32_t)sb * L::b_tile, &tm_act, kk * BK, pos0 + n0, &B.b_full[sb]);
+          misc->b_issued = (int)g + 1;
         }
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) {
-          ok = false;
-          break;
-        }
-        unsigned char* bdst = smem + L::off_b + (uint32_t)sb * L::b_tile;
-        if (DUAL) {
-          unsigned char* d0 = bdst + lane * 8 * (BK * 2);
-          tma_gather4(d0, &tm_act, kk * BK, rows[0], rows[1], rows[2], rows[3], &B.b_full[sb]);
-          tma_gather4(d0 + 4 * (BK * 2), &tm_act, kk * BK, rows[4], rows[5], rows[6], rows[7], &B.b_full[sb]);
-        } else if (lane == 0) {
-          tma_load_2d(bdst, &tm_act, kk * BK, pos0 + n0, &B.b_full[sb]);
-        }
-        if (lane == 0) misc->b_issued = (int)g + 1;
-        __syncwarp();
+      }
+      if (st_cta) {
+        st_cta[0] = sw[0];
+        st_cta[1] = sw[1];
       }
     }
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+      unsigned long long sw[3] = {0, 0, 0};
       uint32_t g = 0;
       int j = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++j) {
         const int ab = j & 1;
-        if (!mbar_wait(&B.acc_empty[ab], ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, a.err)) break;
+        if (!timed_wait(&B.acc_empty[ab], ((uint32_t)(j >> 1) & 1u) ^ 1u, abort_flag, a.err, st_cta ? &sw[0] : nullptr))
+          break;
         tc_fence_after();
         const uint32_t d0 = tbase + (uint32_t)ab * L::acc_stride;
         for (int kk = 0; kk < nK; ++kk, ++g) {
           const int sa = g % kAStages, sb = g % kBStages;
-          if (!mbar_wait(&B.a_full[sa], (g / kAStages) & 1u, abort_flag, a.err) ||
-              !mbar_wait(&B.b_full[sb], (g / kBStages) & 1u, abort_flag, a.err)) {
+          if (!timed_wait(&B.a_full[sa], (g / kAStages) & 1u, abort_flag, a.err, st_cta ? &sw[1] : nullptr) ||
+              !timed_wait(&B.b_full[sb], (g / kBStages) & 1u, abort_flag, a.err, st_cta ? &sw[2] : nullptr)) {
             ok = false;
             break;
           }
@@ -305,6 +330,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         mma_commit(&B.acc_full[ab]);
       }
+      if (st_cta) {
+        st_cta[2] = sw[0];
+        st_cta[3] = sw[1];
+        st_cta[4] = sw[2];
+      }
     }
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant
@@ -315,7 +345,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int unit = DUAL ? (r >> 1) : r;
     const bool upper = DUAL && (r & 1);
     const int crow = DUAL ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
-    uint32_t g = 0;
+    uint32_t g = 0, gc = 0;  // K steps, code groups (the producer's order)
+    unsigned long long dw[2] = {0, 0};
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const int s = find_segment(prefix, nseg, t);
@@ -333,21 +364,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // scales of K-step kk are loaded one step ahead (latency off the critical path)
       __half sn = rvalid ? __ldg(sp) : __float2half(0.f);
       for (int kk = 0; kk < nK; ++kk, ++g) {
-        const int sc = g % kCodeStages, sa = g % kAStages;
+        const int sc = gc % kCodeStages, sa = g % kAStages;
         const __half s0 = sn;
         if (kk + 1 < nK && rvalid) sn = __ldg(sp + ((kk + 1) * BK) / a.G);
         int good = 1;
-        if (lane == 0)
-          good = mbar_wait(&B.codes_full[sc], (g / kCodeStages) & 1u, abort_flag, a.err) &&
-                 mbar_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err);
+        if (lane == 0) {
+          const bool rec = st_cta && warp == kWarpDequant0;
+          if (kk % kCodeK == 0)
+            good = timed_wait(&B.codes_full[sc], (gc / kCodeStages) & 1u, abort_flag, a.err, rec ? &dw[0] : nullptr);
+          good = good &&
+                 timed_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err, rec ? &dw[1] : nullptr);
+        }
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           ok = false;
           break;
         }
+        // codes of row crow, K step kk: 16-byte chunk (kk % kCodeK) * 2 + hsel of
+        // the row's 128 bytes, at its 128-byte-swizzle position
         const unsigned char* csrc = smem + L::off_codes + (uint32_t)sc * L::code_tile;
+        const int cc = (kk % kCodeK) * 2 + hsel;
+        const uint4 w = *reinterpret_cast<const uint4*>(csrc + crow * 128 + ((cc ^ (crow & 7)) << 4));
         unsigned char* rowp = smem + L::off_a + (uint32_t)sa * L::a_tile + r * (BK * 2);
-        const uint4 w = *reinterpret_cast<const uint4*>(csrc + crow * (BK / 2) + hsel * 16);
         const __half2 s2 = __half2half2(s0);
         const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -357,16 +395,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
+        const bool group_end = (kk % kCodeK == kCodeK - 1) || (kk == nK - 1);
         if (lane == 0) {
           mbar_arrive(&B.a_full[sa]);
-          mbar_arrive(&B.codes_empty[sc]);
+          if (group_end) mbar_arrive(&B.codes_empty[sc]);
         }
+        if (group_end) ++gc;
       }
+    }
+    if (st_cta && warp == kWarpDequant0 && lane == 0) {
+      st_cta[5] = dw[0];
+      st_cta[6] = dw[1];
     }
   } else {
     // ----------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    // Warp e of the epilogue reads TMEM lanes 32 * (warp % 4) .. + 31 (its
+    // accumulator rows) and columns 128 * (e / 4) .. + 127 (its tokens).
+    const int e = warp - kWarpEpi0, et = tid - kWarpEpi0 * 32;
+    const int q = warp & 3, ch = e >> 2;
     const int row = 32 * q + lane;
+    int* s_f = reinterpret_cast<int*>(smem + L::off_epi);
+    unsigned long long ew = 0;
     int j = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++j) {
       const int s = find_segment(prefix, nseg, t);
@@ -377,39 +426,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int pos0 = a.seg_start[s];
       const int ab = j & 1;
       int good = 1;
-      if (lane == 0) good = mbar_wait(&B.acc_full[ab], (uint32_t)(j >> 1) & 1u, abort_flag, a.err);
+      if (lane == 0)
+        good = timed_wait(&B.acc_full[ab], (uint32_t)(j >> 1) & 1u, abort_flag, a.err,
+                          (st_cta && warp == kWarpEpi0) ? &ew : nullptr);
       good = __shfl_sync(0xffffffffu, good, 0);
-      if (!good) break;
+      if (DUAL) {
+        if (!good) break;
+      } else {
+        // one decision for all epilogue warps (they meet at named barriers);
+        // the previous tile's indices are no longer read past this point
+        if (epi_bar_any(!good)) break;
+        // output row (flat pair index) of every token column of the tile
+        for (int c = et; c < BN; c += kEpiWarps * 32) {
+          const int tok = n0 + c;
+          int f = -1;
+          if (tok < cnt) {
+            const int pos = pos0 + tok;
+            f = (pos < a.Tk) ? __ldg(a.perm + pos) : pos;
+          }
+          s_f[c] = f;
+        }
+        epi_bar();
+      }
       tc_fence_after();
       // DUAL: even lanes own gate unit row/2, odd lanes its up value
       const int gunit = m0 + (DUAL ? (row >> 1) : row);
       const bool rvalid = gunit < a.N;
-      const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * L::acc_stride;
+      const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * L::acc_stride + 128u * ch;
 #pragma unroll 1
-      for (int cb = 0; cb < BN / 32; ++cb) {
+      for (int cb = 0; cb < BN / 64; ++cb) {
         uint32_t v[32];
         tmem_ld32(tacc + cb * 32, v);
         tmem_ld_wait();
+        const int c0 = 128 * ch + cb * 32;
         if (DUAL) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             const float mine = __uint_as_float(v[c]);
             const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-            const int tok = n0 + cb * 32 + c;
-            if (!(lane & 1) && rvalid && tok < cnt) {
-              const float h = silu_f(mine) * other;
-              a.h_out[(size_t)(pos0 + tok) * a.N + gunit] = __float2half_rn(h);
-            }
+            const int tok = n0 + c0 + c;
+            if (!(lane & 1) && rvalid && tok < cnt)
+              a.h_out[(size_t)(pos0 + tok) * a.N + gunit] = __float2half_rn(silu_fast(mine) * other);
           }
         } else {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int tok = n0 + cb * 32 + c;
-            if (rvalid && tok < cnt) {
-              const int pos = pos0 + tok;
-              const int f = (pos < a.Tk) ? __ldg(a.perm + pos) : pos;
-              a.y_out[(size_t)f * a.N + gunit] = __uint_as_float(v[c]);
-            }
+            const int f = s_f[c0 + c];
+            if (rvalid && f >= 0) a.y_out[(size_t)f * a.N + gunit] = __uint_as_float(v[c]);
           }
         }
       }
@@ -417,11 +480,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&B.acc_empty[ab]);
     }
+    if (st_cta && warp == kWarpEpi0 && lane == 0) st_cta[7] = ew;
   }
 
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
+  if (st_cta && tid == 0) st_cta[8] = (unsigned long long)(clock64() - t_start);
   if (misc->abort_flag) {
     if (warp == kWarpProducer && lane == 0) {
       // let issued copies land before shared memory is released
@@ -441,7 +506,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tbase, L::tmem_cols);
 }
 
+// Tokens in expert-sorted order for the gate/up GEMM: xs[pos] = x[perm[pos] /
+// k] for pos < Tk, x[pos - Tk] for the shared expert's segment. A warp per
+// row, 16-byte copies.
+__global__ void __launch_bounds__(256) k_gather_rows(const __half* __restrict__ x, __half* __restrict__ xs,
+                                                      const int32_t* __restrict__ perm, int Tk, int k, int rows,
+                                                      int H) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int h8 = H / 8;
+  for (int pos = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < rows; pos += (gridDim.x * blockDim.x) >> 5) {
+    const int src = pos < Tk ? __ldg(perm + pos) / k : pos - Tk;
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)src * H);
+    uint4* out = reinterpret_cast<uint4*>(xs + (size_t)pos * H);
+    for (int c = lane; c < h8; c += 32) out[c] = __ldg(in + c);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_rows(const __half* x, __half* xs, const int32_t* perm, int Tk, int k, int rows, int H,
+                               int grid, cudaStream_t s, bool pdl) {
+  return launch_ex(k_gather_rows, dim3(grid), dim3(256), 0, s, pdl, x, xs, perm, Tk, k, rows, H);
+}
 
 size_t gemm_smem_bytes(bool dual) { return dual ? Smem<true>::alloc : Smem<false>::alloc; }
 
@@ -479,10 +567,10 @@ bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, i
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)(K / 2), (cuuint64_t)N, (cuuint64_t)num_slots};
   const cuuint64_t strides[2] = {(cuuint64_t)(K / 2), (cuuint64_t)record_bytes};
-  const cuuint32_t box[3] = {BK / 2, (cuuint32_t)box_rows, 1};
+  const cuuint32_t box[3] = {kCodeK * BK / 2, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(pool_section), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -69,7 +69,13 @@ struct GemmArgs {
   __half* h_out;                // DUAL: [P][N]
   float* y_out;                 // single: [Tk + T][N]
   uint32_t* err;
+  unsigned long long* stats;    // nullable: [gridDim][kGemmStats] cycles spent waiting, per role
 };
+// GEMM wait counters per CTA: producer (codes stage free, token stage free),
+// MMA (accumulator free, A stage full, token stage full), dequantiser warp 0
+// (codes landed, A stage free), epilogue warp 0 (accumulator full), and the
+// CTA's total cycles.
+constexpr int kGemmStats = 9;
 
 // Whole-layer decode megakernel (T <= kSmallRouteMaxT, full residency).
 // Tensor-core grouped GEMV over expert segments (decode regime): items of
@@ -207,6 +213,9 @@ size_t gemm_smem_bytes(bool dual);
 bool encode_codes_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes,
                       int box_rows);
 bool encode_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, int box_rows);
+// xs[pos] = x[perm[pos] / k] (pos < Tk) or x[pos - Tk], rows positions of H halves
+cudaError_t launch_gather_rows(const __half* x, __half* xs, const int32_t* perm, int Tk, int k, int rows, int H,
+                               int grid, cudaStream_t s, bool pdl);
 int gemm_tile_n();
 int gemm_tile_k();
 

@@ -53,6 +53,7 @@ struct moe_layer {
   void* ws = nullptr;
   float* logits = nullptr;
   float* logit_part = nullptr;
+  __half* xs = nullptr;          // [P][H] tokens in expert-sorted order (GEMM path)
   int32_t* ids = nullptr;
   float* wts = nullptr;
   int32_t* chunk_hist = nullptr;
@@ -77,6 +78,7 @@ struct moe_layer {
   bool megakernel = true;        // single-launch decode for T <= 16 (full residency)
   bool last_single = false;      // the last profiled forward was one launch
   unsigned long long* trace = nullptr;  // per-CTA phase stamps of the single-launch decode (MOE_TRACE=1)
+  unsigned long long* gemm_stats = nullptr;  // GEMM wait counters (MOE_GEMM_STATS=1): [2][CTAs][kGemmStats]
   uint32_t* ctr = nullptr;       // megakernel counters (zero between launches)
   // prefill (tensor-core) path
   int gemm_min_tokens = 256;
@@ -84,7 +86,7 @@ struct moe_layer {
   moe::CodeMaps pool_maps = {};  // code sections of the caller's pool (full residency)
   moe::TcGemvPlan dec_pg = {}, dec_pd = {};  // GEMV work items: gate/up, down
   CUtensorMap h_map = {};        // h workspace rows
-  CUtensorMap x_map = {};        // tokens of the current forward
+  CUtensorMap xs_map = {};       // tokens in expert-sorted order (xs)
   bool profiling = false;
   cudaEvent_t ev[5] = {};
   moe::Residency* res = nullptr;  // partial residency state

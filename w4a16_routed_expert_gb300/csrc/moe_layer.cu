@@ -103,10 +103,12 @@ size_t workspace_bytes(const moe_layer_config_t& c) {
   b += 4 * align256(4);                 // num_seg, ticket, err, pad
   b += align256(P * I * 2);             // h
   b += align256(P * H * 4);             // ypart
+  if (H % 64 == 0 && I % 64 == 0) b += align256(P * H * 2);  // tokens in sorted order (GEMM path)
   b += 2 * align256(T * H * 2);         // x/out staging
   b += align256(T * k * 4) * 2;         // ids/w staging
   b += align256(2048 * 4);              // megakernel counters
   b += align256(1024 * moe::kTraceStamps * 8);  // phase trace (up to 1024 CTAs)
+  b += align256(2 * 1024 * moe::kGemmStats * 8);  // GEMM wait counters (two launches)
   return b;
 }
 
@@ -188,14 +190,18 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     carve<uint32_t>(p, 1);
     L->hbuf = carve<__half>(p, P * I);
     L->ypart = carve<float>(p, P * H);
+    if (H % 64 == 0 && I % 64 == 0) L->xs = carve<__half>(p, P * H);
     L->x_stage = carve<__half>(p, T * H);
     L->out_stage = carve<__half>(p, T * H);
     L->ids_stage = carve<int32_t>(p, T * k);
     L->w_stage = carve<float>(p, T * k);
     L->ctr = carve<uint32_t>(p, 2048);
-    unsigned long long* tr = carve<unsigned long long>(p, 1024 * 8);
+    unsigned long long* tr = carve<unsigned long long>(p, 1024 * moe::kTraceStamps);
     const char* tr_env = getenv("MOE_TRACE");
     if (tr_env && tr_env[0] == '1') L->trace = tr;
+    unsigned long long* gs = carve<unsigned long long>(p, 2 * 1024 * moe::kGemmStats);
+    const char* gs_env = getenv("MOE_GEMM_STATS");
+    if (gs_env && gs_env[0] == '1') L->gemm_stats = gs;
   }
   // zero the small control words (ticket, error word, segment count)
   e = cudaMemset(L->num_seg, 0, 4 * 256);
@@ -211,8 +217,9 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     if (gm) L->gemm_min_tokens = atoi(gm);
     const int H = config->hidden, I = config->intermediate;
     const size_t P = (size_t)config->max_tokens * (config->top_k + 1);
-    L->gemm_ok = (H % 64 == 0) && (I % 64 == 0) && P < (1u << 31) &&
-                 moe::encode_rows_map(&L->h_map, L->hbuf, I, (int)P, moe::gemm_tile_n());
+    L->gemm_ok = (H % 64 == 0) && (I % 64 == 0) && P < (1u << 31) && L->xs &&
+                 moe::encode_rows_map(&L->h_map, L->hbuf, I, (int)P, moe::gemm_tile_n()) &&
+                 moe::encode_rows_map(&L->xs_map, L->xs, H, (int)P, moe::gemm_tile_n());
     // GEMV work items of about 64 KB of codes for both matrices' passes:
     // two quantisation groups per consumer warp amortise the per-item work
     // (MOE_GEMV_ITEM_BYTES overrides, for tuning)
@@ -286,7 +293,10 @@ moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, 
                           const int32_t* e2s, int num_slots, const SegPtrs& seg, const CodeMaps* maps) {
   const moe_layer_config_t& c = L->cfg;
   const int H = c.hidden, I = c.intermediate, k = c.top_k, G = c.group_size;
-  if (!encode_rows_map(&L->x_map, x, H, T, 1)) return fail(MOE_ERR_CUDA, "token tensor map encoding failed");
+  // the tokens in expert-sorted order, so that every token tile is one 2-D box
+  const int rows = T * k + (c.has_shared_expert ? T : 0);
+  cudaError_t e = launch_gather_rows(x, L->xs, L->perm, T * k, k, rows, H, L->num_sms * 4, s, L->pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "token gather launch");
   GemmArgs ga = {};
   ga.pool = pool;
   ga.record_bytes = (long long)L->lay.record;
@@ -308,7 +318,8 @@ moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, 
   ga.h_out = L->hbuf;
   ga.y_out = nullptr;
   ga.err = L->err;
-  cudaError_t e = launch_gemm(true, maps->gate, maps->up, L->x_map, ga, L->num_sms, s, L->pdl);
+  ga.stats = L->gemm_stats;
+  e = launch_gemm(true, maps->gate, maps->up, L->xs_map, ga, L->num_sms, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[2], s, cudaEventRecordExternal);
   GemmArgs gb = ga;
@@ -319,6 +330,7 @@ moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, 
   gb.ng = (I + G - 1) / G;
   gb.h_out = nullptr;
   gb.y_out = L->ypart;
+  gb.stats = L->gemm_stats ? L->gemm_stats + (size_t)L->num_sms * kGemmStats : nullptr;
   e = launch_gemm(false, maps->down, maps->down, L->h_map, gb, L->num_sms, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[3], s, cudaEventRecordExternal);
@@ -735,6 +747,17 @@ moe_status_t moe_layer_get_trace(moe_layer_t* layer, uint64_t* stamps, int32_t m
   if (e == cudaSuccess) e = cudaMemcpy(stamps, layer->trace, (size_t)n * 8, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "trace read");
   *n_stamps = n;
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_get_gemm_stats(moe_layer_t* layer, uint64_t* values, int32_t max_values, int32_t* n_values) {
+  if (!layer || !values || !n_values) return fail(MOE_ERR_INVALID_ARG, "layer, values and n_values must not be NULL");
+  if (!layer->gemm_stats) return fail(MOE_ERR_INVALID_ARG, "GEMM counters are off (set MOE_GEMM_STATS=1 before create)");
+  const int n = std::min(max_values, 2 * layer->num_sms * moe::kGemmStats);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(values, layer->gemm_stats, (size_t)n * 8, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "GEMM counter read");
+  *n_values = n;
   return MOE_OK;
 }
 

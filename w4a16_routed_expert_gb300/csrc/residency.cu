@@ -19,6 +19,7 @@
 // its own events and its own segment table, so nothing is reused before it
 // has retired; the next forward's synchronisation retires them all.
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -32,6 +33,7 @@ namespace moe {
 
 namespace {
 thread_local const char* g_res_err = "";
+thread_local char g_res_msg[256];
 }
 
 struct Residency {
@@ -98,20 +100,27 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
     st = MOE_ERR_OOM;
   }
   if (st == MOE_OK) {
-    int ro = 0;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&ro, cudaDevAttrHostRegisterReadOnlySupported, dev);
-    const unsigned flags = ro ? cudaHostRegisterReadOnly : cudaHostRegisterDefault;
-    e = cudaHostRegister(const_cast<void*>(host_backing), (size_t)n_records * record_bytes, flags);
-    if (e == cudaSuccess) {
-      r->registered_here = true;
-    } else if (e == cudaErrorHostMemoryAlreadyRegistered) {
-      cudaGetLastError();
-    } else {
-      cudaGetLastError();
-      g_res_err = "registering the host backing failed";
-      st = MOE_ERR_CUDA;
+    // already page-locked (cudaHostAlloc or registered by the caller): use as is
+    cudaPointerAttributes pa = {};
+    const bool pinned = cudaPointerGetAttributes(&pa, host_backing) == cudaSuccess && pa.type == cudaMemoryTypeHost;
+    cudaGetLastError();
+    if (!pinned) {
+      int ro = 0;
+      int dev = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&ro, cudaDevAttrHostRegisterReadOnlySupported, dev);
+      const unsigned flags = ro ? cudaHostRegisterReadOnly : cudaHostRegisterDefault;
+      e = cudaHostRegister(const_cast<void*>(host_backing), (size_t)n_records * record_bytes, flags);
+      if (e == cudaSuccess) {
+        r->registered_here = true;
+      } else if (e == cudaErrorHostMemoryAlreadyRegistered) {
+        cudaGetLastError();
+      } else {
+        cudaGetLastError();
+        snprintf(g_res_msg, sizeof(g_res_msg), "registering the host backing failed: %s", cudaGetErrorString(e));
+        g_res_err = g_res_msg;
+        st = MOE_ERR_CUDA;
+      }
     }
   }
   if (st == MOE_OK && cudaStreamCreateWithFlags(&r->side, cudaStreamNonBlocking) != cudaSuccess) {

@@ -129,10 +129,6 @@ __device__ __forceinline__ void tc_issue_item(const TcGemvArgs& a, const CUtenso
   if (DUAL) bulk_g2s(ss + a.sstride, rec + a.s_off1 + (size_t)r0 * a.ng * 2, sbytes, full, pol);
 }
 
-// SiLU with the hardware exponential and reciprocal (relative error ~1e-6,
-// far inside the layer's FP16 output rounding).
-__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
-
 // K-part partial sums in shared memory: per (consumer warp, matrix) a block
 // of 16 rows x NS tokens, blocks tc_red_block(NS) floats apart. The odd
 // stride puts the K parts of one output in distinct banks for the finish.
