@@ -44,16 +44,17 @@ constexpr int BM = 128;  // MMA rows per tile (DUAL: 64 gate + 64 up, interleave
 constexpr int BN = 256;  // tokens per tile
 constexpr int BK = 64;   // K per pipeline step (128 bytes of FP16)
 constexpr int kCodeK = 4;  // K steps per code tile: 128 bytes of codes per row, one swizzled TMA box
-constexpr int kCodeStages = 2;
+constexpr int kCodeStages = 4;
 constexpr int kAStages = 3;
-constexpr int kBStages = 4;
+constexpr int kBStages = 3;
 constexpr int kDequantWarps = 8;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each half of the columns
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpDequant0 = 2;
 constexpr int kWarpEpi0 = kWarpDequant0 + kDequantWarps;
-constexpr int kGemmThreads = (kWarpEpi0 + kEpiWarps) * 32;
+constexpr int kWarpCodes = kWarpEpi0 + kEpiWarps;  // TMA producer of the code tiles
+constexpr int kGemmThreads = (kWarpCodes + 1) * 32;
 constexpr int kMaxSeg = 1025;
 
 template <bool DUAL>
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&B.codes_empty[i], kDequantWarps);
     }
     for (int i = 0; i < kAStages; ++i) {
-      mbar_init(&B.a_full[i], kDequantWarps);
+      mbar_init(&B.a_full[i], kDequantWarps / 2);
       mbar_init(&B.a_empty[i], 1);
     }
     for (int i = 0; i < kBStages; ++i) {
@@ -244,43 +245,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = &misc->abort_flag;
 
   if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------- producer of the token tiles
     if (lane == 0) {
-      unsigned long long sw[2] = {0, 0};
-      uint32_t g = 0, gc = 0;  // K steps, code groups (both over all tiles of this CTA)
+      unsigned long long sw = 0;
+      uint32_t g = 0;  // K steps over all tiles of this CTA
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const int s = find_segment(prefix, nseg, t);
         const int local = t - prefix[s];
         const int cnt = a.seg_count[s];
         const int ntl = (cnt + BN - 1) / BN;
-        const int m0 = (local / ntl) * L::units, n0 = (local % ntl) * BN;
-        const int e = a.seg_expert[s];
-        int slot = a.expert_to_slot[e];
-        if (slot < 0 || slot >= a.num_slots) {
-          record_error(a.err, MOE_DEV_ERR_BOUNDS);
-          slot = 0;
-        }
+        const int n0 = (local % ntl) * BN;
         const int pos0 = a.seg_start[s];
         for (int kk = 0; kk < nK; ++kk, ++g) {
-          if (kk % kCodeK == 0) {
-            // codes of K steps kk .. kk + kCodeK - 1: one box per matrix
-            const int sc = gc % kCodeStages;
-            if (!timed_wait(&B.codes_empty[sc], ((gc / kCodeStages) & 1u) ^ 1u, abort_flag, a.err,
-                            st_cta ? &sw[0] : nullptr)) {
-              ok = false;
-              break;
-            }
-            unsigned char* cdst = smem + L::off_codes + (uint32_t)sc * L::code_tile;
-            mbar_arrive_expect_tx(&B.codes_full[sc], L::code_tile);
-            const int cx = (kk / kCodeK) * (kCodeK * BK / 2);
-            tma_load_3d(cdst, &tm_codes0, cx, m0, slot, &B.codes_full[sc]);
-            if (DUAL) tma_load_3d(cdst + L::code_tile / 2, &tm_codes1, cx, m0, slot, &B.codes_full[sc]);
-            ++gc;
-            misc->codes_issued = (int)gc;
-          }
           const int sb = g % kBStages;
-          if (!timed_wait(&B.b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err, st_cta ? &sw[1] : nullptr)) {
+          if (!timed_wait(&B.b_empty[sb], ((g / kBStages) & 1u) ^ 1u, abort_flag, a.err, st_cta ? &sw : nullptr)) {
             ok = false;
             break;
           }
@@ -289,10 +268,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           misc->b_issued = (int)g + 1;
         }
       }
-      if (st_cta) {
-        st_cta[0] = sw[0];
-        st_cta[1] = sw[1];
+      if (st_cta) st_cta[1] = sw;
+    }
+  } else if (warp == kWarpCodes) {
+    // -------------------------------------------- producer of the code tiles
+    if (lane == 0) {
+      unsigned long long sw = 0;
+      uint32_t gc = 0;  // code groups over all tiles of this CTA
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int s = find_segment(prefix, nseg, t);
+        const int local = t - prefix[s];
+        const int cnt = a.seg_count[s];
+        const int ntl = (cnt + BN - 1) / BN;
+        const int m0 = (local / ntl) * L::units;
+        const int e = a.seg_expert[s];
+        int slot = a.expert_to_slot[e];
+        if (slot < 0 || slot >= a.num_slots) {
+          record_error(a.err, MOE_DEV_ERR_BOUNDS);
+          slot = 0;
+        }
+        for (int kk = 0; kk < nK; kk += kCodeK, ++gc) {
+          // codes of K steps kk .. kk + kCodeK - 1: one box per matrix
+          const int sc = gc % kCodeStages;
+          if (!timed_wait(&B.codes_empty[sc], ((gc / kCodeStages) & 1u) ^ 1u, abort_flag, a.err,
+                          st_cta ? &sw : nullptr)) {
+            ok = false;
+            break;
+          }
+          unsigned char* cdst = smem + L::off_codes + (uint32_t)sc * L::code_tile;
+          mbar_arrive_expect_tx(&B.codes_full[sc], L::code_tile);
+          const int cx = (kk / kCodeK) * (kCodeK * BK / 2);
+          tma_load_3d(cdst, &tm_codes0, cx, m0, slot, &B.codes_full[sc]);
+          if (DUAL) tma_load_3d(cdst + L::code_tile / 2, &tm_codes1, cx, m0, slot, &B.codes_full[sc]);
+          misc->codes_issued = (int)gc + 1;
+        }
       }
+      if (st_cta) st_cta[0] = sw;
     }
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
@@ -338,14 +350,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant
-    const int dt = tid - kWarpDequant0 * 32;
-    const int r = dt >> 1, hsel = dt & 1;
+    // Two groups of kDequantWarps / 2 warps take alternate K steps (group
+    // par takes the steps kk with kk % 2 == par), so two A stages fill at
+    // once; a thread converts one A row (64 codes) per step.
+    const int par = (warp - kWarpDequant0) / (kDequantWarps / 2);
+    const int r = tid - kWarpDequant0 * 32 - par * (kDequantWarps / 2) * 32;  // A row 0..127
     // A row r: DUAL -> unit r/2 of the gate (even r) or up (odd r) matrix,
     // codes row r/2 or 64 + r/2 of the stage; single -> row r.
     const int unit = DUAL ? (r >> 1) : r;
     const bool upper = DUAL && (r & 1);
     const int crow = DUAL ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
-    uint32_t g = 0, gc = 0;  // K steps, code groups (the producer's order)
+    const bool rec = st_cta && warp == kWarpDequant0 && lane == 0;
+    uint32_t gbase = 0, gc = 0;  // K steps of the previous tiles, code groups (the producer's order)
     unsigned long long dw[2] = {0, 0};
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -361,47 +377,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const __half* sp = reinterpret_cast<const __half*>(a.pool + (size_t)slot * a.record_bytes +
                                                          (upper ? a.s_off1 : a.s_off0)) +
                          (size_t)(m0 + unit) * a.ng;
-      // scales of K-step kk are loaded one step ahead (latency off the critical path)
-      __half sn = rvalid ? __ldg(sp) : __float2half(0.f);
-      for (int kk = 0; kk < nK; ++kk, ++g) {
-        const int sc = gc % kCodeStages, sa = g % kAStages;
-        const __half s0 = sn;
-        if (kk + 1 < nK && rvalid) sn = __ldg(sp + ((kk + 1) * BK) / a.G);
+      const int ngroups = (nK + kCodeK - 1) / kCodeK;
+      for (int grp = 0; grp < ngroups && ok; ++grp, ++gc) {
+        const int sc = gc % kCodeStages;
         int good = 1;
-        if (lane == 0) {
-          const bool rec = st_cta && warp == kWarpDequant0;
-          if (kk % kCodeK == 0)
-            good = timed_wait(&B.codes_full[sc], (gc / kCodeStages) & 1u, abort_flag, a.err, rec ? &dw[0] : nullptr);
-          good = good &&
-                 timed_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err, rec ? &dw[1] : nullptr);
-        }
+        if (lane == 0)
+          good = timed_wait(&B.codes_full[sc], (gc / kCodeStages) & 1u, abort_flag, a.err, rec ? &dw[0] : nullptr);
         good = __shfl_sync(0xffffffffu, good, 0);
         if (!good) {
           ok = false;
           break;
         }
-        // codes of row crow, K step kk: 16-byte chunk (kk % kCodeK) * 2 + hsel of
-        // the row's 128 bytes, at its 128-byte-swizzle position
-        const unsigned char* csrc = smem + L::off_codes + (uint32_t)sc * L::code_tile;
-        const int cc = (kk % kCodeK) * 2 + hsel;
-        const uint4 w = *reinterpret_cast<const uint4*>(csrc + crow * 128 + ((cc ^ (crow & 7)) << 4));
-        unsigned char* rowp = smem + L::off_a + (uint32_t)sa * L::a_tile + r * (BK * 2);
-        const __half2 s2 = __half2half2(s0);
-        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+        const unsigned char* crowp = smem + L::off_codes + (uint32_t)sc * L::code_tile + crow * 128;
+        const int k_end = min(nK, (grp + 1) * kCodeK);
+        for (int kk = grp * kCodeK + par; kk < k_end; kk += 2) {
+          const uint32_t g = gbase + (uint32_t)kk;
+          const int sa = g % kAStages;
+          const __half sv = rvalid ? __ldg(sp + (kk * BK) / a.G) : __float2half(0.f);
+          if (lane == 0)
+            good = timed_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err, rec ? &dw[1] : nullptr);
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+          // codes of K step kk: 16-byte chunks 2 (kk % kCodeK) and + 1 of the
+          // row's 128 bytes, at their 128-byte-swizzle positions
+          const int cc = (kk % kCodeK) * 2;
+          const uint4 w0 = *reinterpret_cast<const uint4*>(crowp + ((cc ^ (crow & 7)) << 4));
+          const uint4 w1 = *reinterpret_cast<const uint4*>(crowp + (((cc + 1) ^ (crow & 7)) << 4));
+          unsigned char* rowp = smem + L::off_a + (uint32_t)sa * L::a_tile + r * (BK * 2);
+          const __half2 s2 = __half2half2(sv);
+          const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = hsel * 4 + i;  // 16-byte chunk (8 halves) of the 128-byte row
-          *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = dequant8(words[i], s2);
+          for (int c = 0; c < 8; ++c)  // 16-byte chunk c (8 halves) of the 128-byte A row
+            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = dequant8(words[c], s2);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&B.a_full[sa]);
         }
-        fence_proxy_async_smem();
+        if (!ok) break;
+        // every dequantiser warp releases the code group once, after its steps
         __syncwarp();
-        const bool group_end = (kk % kCodeK == kCodeK - 1) || (kk == nK - 1);
-        if (lane == 0) {
-          mbar_arrive(&B.a_full[sa]);
-          if (group_end) mbar_arrive(&B.codes_empty[sc]);
-        }
-        if (group_end) ++gc;
+        if (lane == 0) mbar_arrive(&B.codes_empty[sc]);
       }
+      gbase += (uint32_t)nK;
     }
     if (st_cta && warp == kWarpDequant0 && lane == 0) {
       st_cta[5] = dw[0];
