@@ -28,6 +28,8 @@
 // Every cross-CTA wait is a bounded spin; on time-out the CTA records an
 // error, stops, lets its issued copies land and still passes the final
 // ticket, whose last holder resets all counters for the next launch.
+#include <mutex>
+
 #include "route_dev.cuh"
 #include "tcgemv_dev.cuh"
 
@@ -88,7 +90,7 @@ __device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, v
 // the CTA that completed it): out[t][row] = sum_j w[t][j] * y[(t, j)][row]
 // in rank order, then the shared expert, the FP16 rounding and the residual.
 // The same arithmetic, in the same order, as the multi-kernel combine.
-__device__ __forceinline__ void decode_combine_rows(const DecodeArgs& a, const TcGemvArgs& d, int rbi,
+__device__ __noinline__ void decode_combine_rows(const DecodeArgs& a, const TcGemvArgs& d, int rbi,
                                                     const float* s_w, int lane) {
   const int T = a.r.T, H = a.r.H, k = a.r.k, Tk = T * k;
   const int r0 = rbi * d.rb;
@@ -132,7 +134,10 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(const DecodeArgs& a, in
   return L;
 }
 
-template <int NV>
+// NV: router values per lane (E <= 32 NV); TMAX: the largest T of the
+// launch (1, 4 or 16), so that only the loops and routing paths a batch of
+// that size needs are compiled into the instance it runs.
+template <int NV, int TMAX>
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_scan[33];
@@ -178,6 +183,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
     hdr->ncombine = 0;
     fence_mbar_init();
   }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&a.tm_gate);
+    prefetch_tmap(&a.tm_up);
+    prefetch_tmap(&a.tm_down);
+  }
+  // Launched with programmatic stream serialisation (when available): the
+  // next kernel may begin launching now, and nothing above touched global
+  // memory; wait here until the previous kernel has completed and its
+  // writes (the input tokens, this layer's counters) are visible.
+  pdl_trigger();
+  pdl_wait();
   __syncthreads();
   volatile int* abort_flag = &hdr->abort_flag;
   unsigned long long* tr = (tid == 0) ? a.trace : nullptr;
@@ -189,7 +205,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   {
     const int nw = gridDim.x * (kDecodeThreads / 32);
     for (int q = warp * gridDim.x + blockIdx.x; q < E * kLogitParts; q += nw)
-      warp_logit_partial(a.r, q / kLogitParts, q % kLogitParts, a.r.logit_part);
+      warp_logit_partial<TMAX>(a.r, q / kLogitParts, q % kLogitParts, a.r.logit_part);
   }
   __syncthreads();
   trace_mark(tr, 1);
@@ -218,7 +234,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
     L.seg_count = s_scount;
     L.num_seg = s_nseg;
     // the ring is idle until routing is done: block top-k buffer
-    route_finish_cta<NV>(L, s_scratch, s_scan, a.r.logit_part, tr, reinterpret_cast<float*>(ring));
+    route_finish_cta<NV, TMAX == 1>(L, s_scratch, s_scan, a.r.logit_part, tr, reinterpret_cast<float*>(ring));
     __syncthreads();
     trace_mark(tr, 4);
     nseg = *s_nseg;
@@ -480,22 +496,69 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   }
 }
 
-template <int NV>
-cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s) {
+template <int NV, int TMAX>
+cudaError_t launch_decode_t(const DecodeArgs& a, int grid, cudaStream_t s, bool pdl) {
   const size_t smem = decode_smem_bytes(a, a.stages);
-  cudaError_t e = ensure_smem(k_decode<NV>, smem);
+  cudaError_t e = ensure_smem(k_decode<NV, TMAX>, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kDecodeThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode<NV>, a);
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k_decode<NV, TMAX>, a);
+}
+
+template <int NV>
+cudaError_t launch_decode_nv(const DecodeArgs& a, int grid, cudaStream_t s, bool pdl) {
+  if (a.r.T <= 1) return launch_decode_t<NV, 1>(a, grid, s, pdl);
+  if (a.r.T <= 4) return launch_decode_t<NV, 4>(a, grid, s, pdl);
+  return launch_decode_t<NV, kSmallRouteMaxT>(a, grid, s, pdl);
+}
+
+// Whether a cooperative launch also accepts programmatic stream
+// serialisation on this device: probed once per process with an empty
+// cooperative kernel on a private stream (never inside a stream capture).
+__global__ void k_coop_pdl_probe() {
+  pdl_trigger();
+  pdl_wait();
+}
+bool coop_pdl_probe_once() {
+  static int state = -1;  // -1 unknown, 0 no, 1 yes
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (state >= 0) return state == 1;
+  state = 0;
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_coop_pdl_probe);
+  if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, k_coop_pdl_probe);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) state = 1;
+  cudaGetLastError();
+  cudaStreamDestroy(st);
+  return state == 1;
 }
 
 }  // namespace
@@ -519,12 +582,15 @@ TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes) {
   return p;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s) {
-  if (a.r.E <= 64) return launch_decode_t<2>(a, grid, s);
-  if (a.r.E <= 128) return launch_decode_t<4>(a, grid, s);
-  if (a.r.E <= 256) return launch_decode_t<8>(a, grid, s);
-  if (a.r.E <= 512) return launch_decode_t<16>(a, grid, s);
-  return launch_decode_t<32>(a, grid, s);
+bool decode_pdl_supported() { return coop_pdl_probe_once(); }
+
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s, bool pdl) {
+  if (a.r.T < 1 || a.r.T > kSmallRouteMaxT) return cudaErrorInvalidValue;
+  if (a.r.E <= 64) return launch_decode_nv<2>(a, grid, s, pdl);
+  if (a.r.E <= 128) return launch_decode_nv<4>(a, grid, s, pdl);
+  if (a.r.E <= 256) return launch_decode_nv<8>(a, grid, s, pdl);
+  if (a.r.E <= 512) return launch_decode_nv<16>(a, grid, s, pdl);
+  return launch_decode_nv<32>(a, grid, s, pdl);
 }
 
 }  // namespace moe

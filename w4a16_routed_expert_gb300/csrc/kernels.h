@@ -15,6 +15,9 @@ namespace moe {
 constexpr int kRouteChunkTokens = 32;
 // Largest T handled by the fused single-launch routing kernel.
 constexpr int kSmallRouteMaxT = 16;
+// Most K parts the large-batch router logits are split into (partial-logit
+// planes in the logits workspace).
+constexpr int kRouterSplitMax = 8;
 
 // Routing workspace and outputs (all device pointers).
 // global-timer stamps per CTA written by the traced single-launch decode:
@@ -31,7 +34,8 @@ struct RouteArgs {
   int T, H, E, k;
   int renorm;
   int has_shared;
-  float* logits;        // [T][E]
+  float* logits;        // [T][E], or [nsplit][T][E] partial planes (large path)
+  int nsplit;           // large path: planes in logits, summed in order plus the bias; 0: final logits
   float* logit_part;    // [T][E][16] partial logits (single-launch decode), or nullptr
   int32_t* ids;         // [T][k] workspace copy
   float* w;             // [T][k] workspace copy
@@ -199,6 +203,8 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 
 cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_route_large(const RouteArgs& a, cudaStream_t s, bool pdl);
+// K parts of the large-batch router logits for this shape (1..kRouterSplitMax)
+int router_split(int T, int E, int H, int num_sms);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl);
 constexpr int kDecodeMaxStages = 8;  // ring stages of the single-launch decode
 // dynamic shared memory the ring kernels size themselves to: the 227 KB
@@ -206,7 +212,10 @@ constexpr int kDecodeMaxStages = 8;  // ring stages of the single-launch decode
 // reservation
 constexpr size_t kSmemBudget = 227 * 1024 - 2048;
 size_t decode_smem_bytes(const DecodeArgs& a, int stages);
-cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s, bool pdl);
+// whether the decode launch may add programmatic stream serialisation to its
+// cooperative launch on this device (probed once, outside any capture)
+bool decode_pdl_supported();
 cudaError_t launch_gemm(bool dual, const CUtensorMap& codes0, const CUtensorMap& codes1, const CUtensorMap& act,
                         const GemmArgs& a, int grid, cudaStream_t s, bool pdl);
 size_t gemm_smem_bytes(bool dual);

@@ -49,6 +49,7 @@ struct moe_layer {
   Layout lay;
   int n_records = 0;
   bool pdl = true;
+  bool decode_pdl = false;  // the cooperative decode launch also takes programmatic serialisation
   // workspace (one allocation)
   void* ws = nullptr;
   float* logits = nullptr;

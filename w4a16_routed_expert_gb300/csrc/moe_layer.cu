@@ -92,7 +92,7 @@ size_t workspace_bytes(const moe_layer_config_t& c) {
   const size_t nchunks = (T + moe::kRouteChunkTokens - 1) / moe::kRouteChunkTokens;
   const size_t P = T * k + T;  // sorted positions incl. the shared segment
   size_t b = 0;
-  b += align256(T * E * 4);             // logits
+  b += align256(moe::kRouterSplitMax * T * E * 4);  // logits (partial planes on the large path)
   b += align256(std::min<size_t>(T, moe::kSmallRouteMaxT) * E * 16 * 4);  // logit partials
   b += 2 * align256(T * k * 4);         // ids, wts
   b += 2 * align256(nchunks * E * 4);   // chunk_hist, chunk_base
@@ -152,6 +152,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
   L->pdl = !(pdl_env && pdl_env[0] == '0');
   const char* mk_env = getenv("MOE_MEGAKERNEL");
   L->megakernel = !(mk_env && mk_env[0] == '0');
+  // probed here, at create time, so that no capture sees a rejected launch
+  L->decode_pdl = L->pdl && moe::decode_pdl_supported();
   cudaError_t e = cudaGetDevice(&L->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
   if (e != cudaSuccess) {
@@ -171,7 +173,7 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     const size_t nchunks = (T + moe::kRouteChunkTokens - 1) / moe::kRouteChunkTokens;
     const size_t P = T * k + T;
     char* p = static_cast<char*>(L->ws);
-    L->logits = carve<float>(p, T * E);
+    L->logits = carve<float>(p, moe::kRouterSplitMax * T * E);
     L->logit_part = carve<float>(p, std::min<size_t>(T, moe::kSmallRouteMaxT) * E * 16);
     L->ids = carve<int32_t>(p, T * k);
     L->wts = carve<float>(p, T * k);
@@ -534,7 +536,7 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   a.stages = (int)std::min<size_t>(kDecodeMaxStages, (kSmemBudget - fixed) / a.slot_bytes);
   if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
   if (L->trace) cudaMemsetAsync(L->trace, 0, (size_t)L->num_sms * moe::kTraceStamps * 8, s);
-  cudaError_t e = launch_decode(a, L->num_sms, s);
+  cudaError_t e = launch_decode(a, L->num_sms, s, L->pdl && L->decode_pdl);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
   L->last_single = true;
@@ -593,6 +595,7 @@ moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_us
   ra.ticket = L->ticket;
   ra.err = L->err;
   const bool small = T <= moe::kSmallRouteMaxT && (size_t)T * c.hidden * 2 <= 200 * 1024;
+  if (!small) ra.nsplit = moe::router_split(T, c.num_experts, c.hidden, L->num_sms);
   if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
   L->last_single = false;
   cudaError_t e = small ? moe::launch_route_small(ra, s, L->pdl) : moe::launch_route_large(ra, s, L->pdl);

@@ -8,15 +8,17 @@
 // definition in include/moe_layer.h: FP32 logits from FP16 x and FP32 router
 // weights, FP32 softmax, selection decided on the FP32 logits.
 //
-// Two launch shapes produce identical outputs:
+// Two launch shapes:
 //  * small T (<= kSmallRouteMaxT): one kernel; CTAs split the experts, each
 //    warp computes one expert's logits for all tokens, and the last CTA to
 //    finish (atomic ticket, no spinning) runs top-k, the histogram, the scan
 //    and the stable scatter for the whole batch;
-//  * large T: a tiled logits kernel, a top-k kernel per 64-token chunk that
-//    also writes the chunk's expert histogram (its last CTA turns the
-//    histograms into offsets and per-chunk bases), then a scatter kernel per
-//    chunk.
+//  * large T: a logits kernel split over K (partial planes summed in order
+//    by the next kernel), a top-k kernel per chunk of tokens that also
+//    writes the chunk's expert histogram (its last CTA turns the histograms
+//    into offsets and per-chunk bases), then a scatter kernel per chunk.
+// The selection is the same rule on both; the logits' FP32 summation order
+// differs between them.
 #include <cfloat>
 #include <cmath>
 
@@ -26,7 +28,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kRouteThreads = 256;
 
 // Router logits for T <= kSmallRouteMaxT tokens: one CTA per expert, warp p
 // computes partial p of the row; the partials are summed in order (the same
@@ -73,96 +74,127 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
 }
 
 // ------------------------------------------------------------ large path
-// Logits tile: 32 tokens x 64 experts per CTA (128 threads, 4 x 4 outputs
-// each), K in steps of 32 staged through shared memory; FP32 FMA.
-__global__ void __launch_bounds__(128) k_router_logits_tiled(RouteArgs a) {
-  __shared__ __align__(16) float xs[32][32 + 4];  // [k][token]
-  __shared__ __align__(16) float ws[32][64 + 4];  // [k][expert]
+// Router logits, split over K: CTA (bx, by, p) computes the partial dot
+// products of 128 tokens x 64 experts over K part p (32-wide K chunks
+// [p * nch / P, (p + 1) * nch / P)) in FP32 and writes plane p of the logits
+// workspace ([P][T][E]); the top-k kernel sums the planes in order and adds
+// the bias. Each thread holds 8 tokens x 4 experts; the next K chunk is
+// loaded into registers while the current one is multiplied.
+constexpr int kLgTok = 128;
+constexpr int kLgExp = 64;
+constexpr int kLgK = 32;
+constexpr int kLgThreads = 256;
+
+__global__ void __launch_bounds__(kLgThreads) k_router_logits_split(RouteArgs a) {
+  __shared__ __align__(16) float xs[kLgK][kLgTok + 4];  // [k][token]
+  __shared__ __align__(16) float ws[kLgK][kLgExp + 4];  // [k][expert]
   const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * 32, e0 = blockIdx.y * 64;
-  const int ty = tid >> 4, tx = tid & 15;  // tokens 4*ty.., experts 4*tx..
-  const int T = a.T, H = a.H, E = a.E;
+  const int t0 = blockIdx.x * kLgTok, e0 = blockIdx.y * kLgExp, p = blockIdx.z;
+  const int T = a.T, H = a.H, E = a.E, P = a.nsplit;
+  const int nch = H / kLgK;
+  const int c0 = (int)((long long)p * nch / P), c1 = (int)((long long)(p + 1) * nch / P);
+  const int ty = tid >> 4, tx = tid & 15;  // tokens 8 ty .. 8 ty + 7, experts 4 tx .. 4 tx + 3
+  // loader roles: x row lt (16 halves at kq), router row le (8 floats at kw)
+  const int lt = tid >> 1, kq = (tid & 1) * 16;
+  const int le = tid >> 2, kw = (tid & 3) * 8;
+  const bool xrow = t0 + lt < T, wrow = e0 + le < E;
+  const uint4* xsrc = reinterpret_cast<const uint4*>(a.x + (size_t)(xrow ? t0 + lt : 0) * H + kq);
+  const float4* wsrc = reinterpret_cast<const float4*>(a.wr + (size_t)(wrow ? e0 + le : 0) * H + kw);
   pdl_wait();
-  float acc[4][4];
+  float acc[8][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-  for (int k0 = 0; k0 < H; k0 += 32) {
-    {  // x tile: 32 tokens x 32 k = 1024 halves, 8 per thread
-      const int tt = tid >> 2, kk = (tid & 3) * 8;
-      const int t = t0 + tt;
-      uint4 raw = make_uint4(0, 0, 0, 0);
-      if (t < T) raw = __ldg(reinterpret_cast<const uint4*>(a.x + (size_t)t * H + k0 + kk));
-      const __half2* hp = reinterpret_cast<const __half2*>(&raw);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float2 v = __half22float2(hp[u]);
-        xs[kk + 2 * u][tt] = v.x;
-        xs[kk + 2 * u + 1][tt] = v.y;
-      }
+  uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
+  float4 wr0 = make_float4(0.f, 0.f, 0.f, 0.f), wr1 = wr0;
+  auto load = [&](int c) {
+    const int o = c * kLgK;
+    if (xrow) {
+      xr0 = __ldg(xsrc + o / 8);
+      xr1 = __ldg(xsrc + o / 8 + 1);
     }
+    if (wrow) {
+      wr0 = __ldg(wsrc + o / 4);
+      wr1 = __ldg(wsrc + o / 4 + 1);
+    }
+  };
+  if (c0 < c1) load(c0);
+  for (int c = c0; c < c1; ++c) {
+    {
+      const uint32_t hx[8] = {xr0.x, xr0.y, xr0.z, xr0.w, xr1.x, xr1.y, xr1.z, xr1.w};
 #pragma unroll
-    for (int rep = 0; rep < 4; ++rep) {  // router tile: 64 experts x 32 k, 16 floats per thread
-      const int idx = rep * 128 + tid;
-      const int ee = idx >> 3, kk = (idx & 7) * 4;
-      const int e = e0 + ee;
-      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (e < E) w = __ldg(reinterpret_cast<const float4*>(a.wr + (size_t)e * H + k0 + kk));
-      ws[kk + 0][ee] = w.x;
-      ws[kk + 1][ee] = w.y;
-      ws[kk + 2][ee] = w.z;
-      ws[kk + 3][ee] = w.w;
+      for (int u = 0; u < 8; ++u) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hx[u]));
+        xs[kq + 2 * u][lt] = f.x;
+        xs[kq + 2 * u + 1][lt] = f.y;
+      }
+      const float wv[8] = {wr0.x, wr0.y, wr0.z, wr0.w, wr1.x, wr1.y, wr1.z, wr1.w};
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ws[kw + u][le] = wv[u];
     }
     __syncthreads();
+    if (c + 1 < c1) load(c + 1);
 #pragma unroll 8
-    for (int kk = 0; kk < 32; ++kk) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
+    for (int kk = 0; kk < kLgK; ++kk) {
+      const float4 xa = *reinterpret_cast<const float4*>(&xs[kk][8 * ty]);
+      const float4 xb = *reinterpret_cast<const float4*>(&xs[kk][8 * ty + 4]);
       const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
       const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], wa[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], wa[j], acc[i][j]);
     }
     __syncthreads();
   }
+  float* plane = a.logits + (size_t)p * T * E;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + 4 * ty + i;
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + 8 * ty + i;
     if (t >= T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int e = e0 + 4 * tx + j;
-      if (e < E) a.logits[(size_t)t * E + e] = acc[i][j] + (a.bias ? __ldg(a.bias + e) : 0.f);
+      if (e < E) plane[(size_t)t * E + e] = acc[i][j];
     }
   }
 }
 
+// Softmax, top-k and the expert histogram of one chunk of kRouteChunkTokens
+// tokens (one warp per token). The last CTA to finish turns the chunk
+// histograms into per-expert totals, offsets, the segment list and each
+// chunk's per-expert base relative to its expert's offset (staged through
+// shared memory a slab of experts at a time, so no thread walks a chain of
+// dependent global loads).
+constexpr int kTopkThreads = 512;
+constexpr int kFinishInts = 8192;  // shared ints for the staged histograms (at least one column)
+__host__ __device__ inline int finish_stage_ints(int nchunks) { return nchunks > kFinishInts ? nchunks : kFinishInts; }
+
 template <int NV>
-__global__ void __launch_bounds__(kRouteThreads) k_topk_hist(RouteArgs a) {
+__global__ void __launch_bounds__(kTopkThreads) k_topk_hist(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int s_scan[33];
   __shared__ int s_last;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int nwarps = kTopkThreads / 32;
   const int T = a.T, E = a.E, k = a.k;
   const int c = blockIdx.x;
   const int tbeg = c * kRouteChunkTokens;
   const int tend = min(T, tbeg + kRouteChunkTokens);
-  int32_t* s_ids = reinterpret_cast<int32_t*>(smem);           // [64*k]
-  int* s_hist = s_ids + kRouteChunkTokens * k;                  // [E]
-  int* s_off = s_hist + E;                                       // [E+1] (last CTA)
+  int32_t* s_ids = reinterpret_cast<int32_t*>(smem);  // [chunk tokens * k]
+  int* s_hist = s_ids + kRouteChunkTokens * k;        // [E]
+  int* s_off = s_hist + E;                             // [E+1]
+  int* s_stage = s_off + E + 1;                        // [finish_stage_ints] (last CTA)
 
   pdl_wait();
-  for (int i = tid; i < E; i += kRouteThreads) s_hist[i] = 0;
-  for (int t = tbeg + warp; t < tend; t += kRouteThreads / 32)
-    warp_softmax_topk<NV>(a, t, s_ids + (t - tbeg) * k);
+  for (int i = tid; i < E; i += kTopkThreads) s_hist[i] = 0;
+  for (int t = tbeg + warp; t < tend; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + (t - tbeg) * k);
   __syncthreads();
-  for (int f = tid; f < (tend - tbeg) * k; f += kRouteThreads) atomicAdd(&s_hist[s_ids[f]], 1);
+  for (int f = tid; f < (tend - tbeg) * k; f += kTopkThreads) atomicAdd(&s_hist[s_ids[f]], 1);
   __syncthreads();
-  for (int i = tid; i < E; i += kRouteThreads) a.chunk_hist[(size_t)c * E + i] = s_hist[i];
+  for (int i = tid; i < E; i += kTopkThreads) a.chunk_hist[(size_t)c * E + i] = s_hist[i];
 
   __threadfence();
   __syncthreads();
@@ -172,19 +204,23 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_hist(RouteArgs a) {
   __threadfence();
 
   const int nchunks = gridDim.x;
-  // per-expert totals and per-chunk exclusive bases (relative to the expert):
-  // one warp per expert, lane i scans a contiguous block of chunks, then a
-  // warp exclusive scan of the block totals
-  {
-    const int lane = tid & 31;
-    const int per = (nchunks + 31) / 32;
-    for (int e = warp; e < E; e += kRouteThreads / 32) {
-      const int c0 = lane * per;
+  const int slab = max(1, min(E, finish_stage_ints(nchunks) / nchunks));
+  const int per = (nchunks + 31) / 32;
+  for (int e0 = 0; e0 < E; e0 += slab) {
+    const int ns = min(slab, E - e0);
+    // stage hist[:, e0 .. e0 + ns) (independent loads, all in flight together)
+    for (int i = tid; i < nchunks * ns; i += kTopkThreads) {
+      const int cc = i / ns, j = i - cc * ns;
+      s_stage[i] = __ldcg(a.chunk_hist + (size_t)cc * E + e0 + j);
+    }
+    __syncthreads();
+    // one warp per expert column: lane l sums chunks [l * per, (l + 1) * per),
+    // a warp exclusive scan gives each lane its base
+    for (int j = warp; j < ns; j += nwarps) {
+      const int cb = lane * per;
       int local = 0;
-      for (int i = 0; i < per; ++i) {
-        const int cc = c0 + i;
-        if (cc < nchunks) local += __ldcg(a.chunk_hist + (size_t)cc * E + e);
-      }
+      for (int q = 0; q < per; ++q)
+        if (cb + q < nchunks) local += s_stage[(cb + q) * ns + j];
       int incl = local;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -192,21 +228,18 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_hist(RouteArgs a) {
         if (lane >= o) incl += y;
       }
       int run = incl - local;
-      for (int i = 0; i < per; ++i) {
-        const int cc = c0 + i;
-        if (cc < nchunks) {
-          const int h = __ldcg(a.chunk_hist + (size_t)cc * E + e);
-          a.chunk_base[(size_t)cc * E + e] = run;
-          run += h;
+      for (int q = 0; q < per; ++q)
+        if (cb + q < nchunks) {
+          a.chunk_base[(size_t)(cb + q) * E + e0 + j] = run;
+          run += s_stage[(cb + q) * ns + j];
         }
-      }
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
-      if (lane == 0) {
-        s_hist[e] = total;
-        s_off[e] = total;
-        a.counts[e] = total;
-      }
+      if (lane == 31) s_hist[e0 + j] = incl;
     }
+    __syncthreads();
+  }
+  for (int i = tid; i < E; i += kTopkThreads) {
+    s_off[i] = s_hist[i];
+    a.counts[i] = s_hist[i];
   }
   __syncthreads();
   block_exclusive_scan(s_off, E, s_scan);
@@ -214,25 +247,26 @@ __global__ void __launch_bounds__(kRouteThreads) k_topk_hist(RouteArgs a) {
     s_off[E] = T * k;
     a.offsets[E] = T * k;
   }
-  for (int e = tid; e < E; e += kRouteThreads) a.offsets[e] = s_off[e];
+  for (int e = tid; e < E; e += kTopkThreads) a.offsets[e] = s_off[e];
   __syncthreads();
-  for (int i = tid; i < nchunks * E; i += kRouteThreads) a.chunk_base[i] += s_off[i % E];
   if (warp == 0) warp_segments(a, s_hist, s_off);
   if (tid == 0) *a.ticket = 0u;
 }
 
+// Stable scatter of one chunk's (token, rank) pairs: expert e's pairs of
+// chunk c start at offsets[e] + chunk_base[c][e].
 __global__ void __launch_bounds__(32) k_scatter(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int lane = threadIdx.x;
   const int c = blockIdx.x;
   const int E = a.E, k = a.k;
   int* cur = reinterpret_cast<int*>(smem);                           // [E]
-  int32_t* s_ids = cur + E;                                          // [64*k]
+  int32_t* s_ids = cur + E;                                          // [chunk tokens * k]
   pdl_wait();
-  for (int e = lane; e < E; e += 32) cur[e] = a.chunk_base[(size_t)c * E + e];
+  for (int e = lane; e < E; e += 32) cur[e] = __ldcg(a.chunk_base + (size_t)c * E + e) + __ldcg(a.offsets + e);
   const int fbeg = c * kRouteChunkTokens * k;
   const int fend = min(a.T * k, fbeg + kRouteChunkTokens * k);
-  for (int f = fbeg + lane; f < fend; f += 32) s_ids[f - fbeg] = a.ids[f];
+  for (int f = fbeg + lane; f < fend; f += 32) s_ids[f - fbeg] = __ldcg(a.ids + f);
   __syncwarp();
   warp_stable_scatter(a, s_ids, fbeg, fend, cur);
 }
@@ -248,14 +282,15 @@ cudaError_t launch_route_small_nv(const RouteArgs& a, cudaStream_t s, bool pdl) 
 
 template <int NV>
 cudaError_t launch_route_large_nv(const RouteArgs& a, cudaStream_t s, bool pdl) {
-  dim3 g1((a.T + 31) / 32, (a.E + 63) / 64);
-  cudaError_t e = launch_ex(k_router_logits_tiled, g1, dim3(128), 0, s, pdl, a);
+  dim3 g1((a.T + kLgTok - 1) / kLgTok, (a.E + kLgExp - 1) / kLgExp, a.nsplit);
+  cudaError_t e = launch_ex(k_router_logits_split, g1, dim3(kLgThreads), 0, s, pdl, a);
   if (e != cudaSuccess) return e;
   const int nchunks = (a.T + kRouteChunkTokens - 1) / kRouteChunkTokens;
-  const size_t smem2 = ((size_t)kRouteChunkTokens * a.k + 2 * (size_t)a.E + 1) * sizeof(int);
+  const size_t smem2 =
+      ((size_t)kRouteChunkTokens * a.k + 2 * (size_t)a.E + 1 + finish_stage_ints(nchunks)) * sizeof(int);
   e = ensure_smem(k_topk_hist<NV>, smem2);
   if (e != cudaSuccess) return e;
-  e = launch_ex(k_topk_hist<NV>, dim3(nchunks), dim3(kRouteThreads), smem2, s, pdl, a);
+  e = launch_ex(k_topk_hist<NV>, dim3(nchunks), dim3(kTopkThreads), smem2, s, pdl, a);
   if (e != cudaSuccess) return e;
   const size_t smem3 = ((size_t)a.E + (size_t)kRouteChunkTokens * a.k) * sizeof(int);
   e = ensure_smem(k_scatter, smem3);
@@ -273,7 +308,16 @@ cudaError_t launch_route_small(const RouteArgs& a, cudaStream_t s, bool pdl) {
   return launch_route_small_nv<32>(a, s, pdl);
 }
 
+int router_split(int T, int E, int H, int num_sms) {
+  const int tiles = ((T + kLgTok - 1) / kLgTok) * ((E + kLgExp - 1) / kLgExp);
+  const int nch = H / kLgK;
+  int p = 1;
+  while (p < kRouterSplitMax && tiles * p < num_sms && nch >= 4 * p) p *= 2;
+  return p;
+}
+
 cudaError_t launch_route_large(const RouteArgs& a, cudaStream_t s, bool pdl) {
+  if (a.nsplit < 1 || a.nsplit > kRouterSplitMax || a.H % kLgK) return cudaErrorInvalidValue;
   if (a.E <= 64) return launch_route_large_nv<2>(a, s, pdl);
   if (a.E <= 128) return launch_route_large_nv<4>(a, s, pdl);
   if (a.E <= 256) return launch_route_large_nv<8>(a, s, pdl);

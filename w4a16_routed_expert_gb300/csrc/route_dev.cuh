@@ -64,20 +64,23 @@ __device__ __forceinline__ int block_exclusive_scan(int* data, int n, int* scrat
 constexpr int kLogitParts = 16;
 
 // Partial p of expert e's logits for every token, written to part[t][e][p].
+// TMAX: the largest T the caller passes (the token loop is unrolled to it;
+// every token's FMA chain is the same whatever TMAX is).
+template <int TMAX = kSmallRouteMaxT>
 __device__ __forceinline__ void warp_logit_partial(const RouteArgs& a, int e, int p, float* part) {
   const int lane = threadIdx.x & 31;
   const int T = a.T, H = a.H, E = a.E;
   const int h4b = (p * (H / 4)) / kLogitParts, h4e = ((p + 1) * (H / 4)) / kLogitParts;
-  float acc[kSmallRouteMaxT];
+  float acc[TMAX];
 #pragma unroll
-  for (int t = 0; t < kSmallRouteMaxT; ++t) acc[t] = 0.f;
+  for (int t = 0; t < TMAX; ++t) acc[t] = 0.f;
   const float4* wr4 = reinterpret_cast<const float4*>(a.wr + (size_t)e * H) + h4b;
   const uint2* x2 = reinterpret_cast<const uint2*>(a.x) + h4b;
 #pragma unroll 2
   for (int h4 = lane; h4 < h4e - h4b; h4 += 32) {
     const float4 wv = __ldg(wr4 + h4);
 #pragma unroll
-    for (int t = 0; t < kSmallRouteMaxT; ++t) {
+    for (int t = 0; t < TMAX; ++t) {
       if (t < T) {
         const uint2 raw = __ldg(x2 + (size_t)t * (H / 4) + h4);
         const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
@@ -90,7 +93,7 @@ __device__ __forceinline__ void warp_logit_partial(const RouteArgs& a, int e, in
     }
   }
 #pragma unroll
-  for (int t = 0; t < kSmallRouteMaxT; ++t)
+  for (int t = 0; t < TMAX; ++t)
     if (t < T) {
       const float v = warp_sum(acc[t]);
       if (lane == 0) part[((size_t)t * E + e) * kLogitParts + p] = v;
@@ -113,6 +116,21 @@ __device__ __forceinline__ float logit_from_parts(const RouteArgs& a, const floa
   return v + (a.bias ? __ldg(a.bias + e) : 0.f);
 }
 
+// Logit (t, e) of the large-batch path from its nsplit K-part planes
+// ([p][T][E], read through L2): summed in order p = 0..nsplit-1, then the bias.
+__device__ __forceinline__ float logit_from_planes(const RouteArgs& a, int t, int e) {
+  const size_t plane = (size_t)a.T * a.E;
+  const float* q = a.logits + (size_t)t * a.E + e;
+  float u[kRouterSplitMax];
+#pragma unroll
+  for (int p = 0; p < kRouterSplitMax; ++p) u[p] = p < a.nsplit ? __ldcg(q + p * plane) : 0.f;
+  float v = 0.f;
+#pragma unroll
+  for (int p = 0; p < kRouterSplitMax; ++p)
+    if (p < a.nsplit) v += u[p];
+  return v + (a.bias ? __ldg(a.bias + e) : 0.f);
+}
+
 // One warp: softmax over the E logits of token t and selection of the top k
 // (largest logit first, lower id first among equal logits). NV = values held
 // per lane (E <= 32 * NV). Writes ids / weights to the workspace, the user
@@ -127,7 +145,14 @@ __device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (e < E) ? (part ? logit_from_parts(a, part, t, e) : __ldcg(L + e)) : -INFINITY;
+    if (e >= E)
+      v[i] = -INFINITY;
+    else if (part)
+      v[i] = logit_from_parts(a, part, t, e);
+    else if (a.nsplit > 0)
+      v[i] = logit_from_planes(a, t, e);
+    else
+      v[i] = __ldcg(L + e);
   }
   float m = -INFINITY;
 #pragma unroll
@@ -429,32 +454,36 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
 // memory; s_scan: 33 ints of shared memory; fbuf (optional, used when
 // E <= 128): T*E + 2T + T*k floats of shared memory for the block-wide
 // top-k.
+// TINY_ONLY: the caller guarantees T * k <= 32 (only that path is compiled).
+// fbuf must be given when NV <= 4.
 template <int NV>
+__device__ __forceinline__ void cta_softmax_topk(const RouteArgs& a, const float* part, float* fbuf,
+                                                 int32_t* s_ids) {
+  if constexpr (NV <= 4) {
+    block_softmax_topk<NV>(a, part, fbuf, s_ids);
+  } else {
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int t = warp; t < a.T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * a.k, part);
+  }
+}
+
+template <int NV, bool TINY_ONLY = false>
 __device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* scratch, int* s_scan,
-                                                 const float* part = nullptr, unsigned long long* tr = nullptr,
-                                                 float* fbuf = nullptr) {
+                                                 const float* part, unsigned long long* tr, float* fbuf) {
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k;
   int32_t* s_ids = scratch;
-  const bool block_topk = NV <= 4 && fbuf != nullptr;
-  if (T * k <= 32) {
+  if (TINY_ONLY || T * k <= 32) {
     int32_t* s_sorted = s_ids + 32 + E + 1;
-    if (block_topk)
-      block_softmax_topk<NV>(a, part, fbuf, s_ids);
-    else
-      for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
+    cta_softmax_topk<NV>(a, part, fbuf, s_ids);
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
     finish_tiny(a, s_ids, s_sorted);
-  } else {
+  } else if constexpr (!TINY_ONLY) {
     int* s_counts = s_ids + T * k;
     int* s_off = s_counts + E;
     int* s_cur = s_off + E + 1;
-    if (block_topk)
-      block_softmax_topk<NV>(a, part, fbuf, s_ids);
-    else
-      for (int t = warp; t < T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
+    cta_softmax_topk<NV>(a, part, fbuf, s_ids);
     for (int i = tid; i < E; i += blockDim.x) s_counts[i] = 0;
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
