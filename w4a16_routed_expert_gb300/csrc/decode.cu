@@ -381,6 +381,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
     int b_seg = -1, b_tb = -1, b_gu = -1;  // token tile the B buffer holds
     int ready_seg = -1;
     int ti = 0;
+    if (n_it > 0 && ng_it > 0) {
+      // the first item's token fragments while its codes are still in flight
+      const int sgi0 = fg / nrb_g;
+      tc_build_b<false>(g, sgi0, 0, min(kTcMaxTok, s_scount[sgi0]), NS, Bs, Cs, tid);
+      b_seg = sgi0;
+      b_tb = 0;
+      b_gu = 1;
+      tc_bar();
+    }
     for (int it = 0; it < n_it; ++it) {
       const int st = it % S;
       const uint32_t ph = (uint32_t)(it / S) & 1u;

@@ -15,8 +15,8 @@
 //    and the stable scatter for the whole batch;
 //  * large T: a logits kernel split over K (partial planes summed in order
 //    by the next kernel), a top-k kernel per chunk of tokens that also
-//    writes the chunk's expert histogram (its last CTA turns the histograms
-//    into offsets and per-chunk bases), then a scatter kernel per chunk.
+//    writes the chunk's expert histogram, then a scatter kernel per chunk
+//    that derives its own bases from the whole histogram.
 // The selection is the same rule on both; the logits' FP32 summation order
 // differs between them.
 #include <cfloat>
@@ -163,21 +163,13 @@ __global__ void __launch_bounds__(kLgThreads) k_router_logits_split(RouteArgs a)
 }
 
 // Softmax, top-k and the expert histogram of one chunk of kRouteChunkTokens
-// tokens (one warp per token). The last CTA to finish turns the chunk
-// histograms into per-expert totals, offsets, the segment list and each
-// chunk's per-expert base relative to its expert's offset (staged through
-// shared memory a slab of experts at a time, so no thread walks a chain of
-// dependent global loads).
+// tokens (one warp per token).
 constexpr int kTopkThreads = 512;
-constexpr int kFinishInts = 8192;  // shared ints for the staged histograms (at least one column)
-__host__ __device__ inline int finish_stage_ints(int nchunks) { return nchunks > kFinishInts ? nchunks : kFinishInts; }
 
 template <int NV>
 __global__ void __launch_bounds__(kTopkThreads) k_topk_hist(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  __shared__ int s_scan[33];
-  __shared__ int s_last;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   constexpr int nwarps = kTopkThreads / 32;
   const int T = a.T, E = a.E, k = a.k;
   const int c = blockIdx.x;
@@ -185,9 +177,6 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_hist(RouteArgs a) {
   const int tend = min(T, tbeg + kRouteChunkTokens);
   int32_t* s_ids = reinterpret_cast<int32_t*>(smem);  // [chunk tokens * k]
   int* s_hist = s_ids + kRouteChunkTokens * k;        // [E]
-  int* s_off = s_hist + E;                             // [E+1]
-  int* s_stage = s_off + E + 1;                        // [finish_stage_ints] (last CTA)
-
   pdl_wait();
   for (int i = tid; i < E; i += kTopkThreads) s_hist[i] = 0;
   for (int t = tbeg + warp; t < tend; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + (t - tbeg) * k);
@@ -195,80 +184,68 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_hist(RouteArgs a) {
   for (int f = tid; f < (tend - tbeg) * k; f += kTopkThreads) atomicAdd(&s_hist[s_ids[f]], 1);
   __syncthreads();
   for (int i = tid; i < E; i += kTopkThreads) a.chunk_hist[(size_t)c * E + i] = s_hist[i];
-
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  const int nchunks = gridDim.x;
-  const int slab = max(1, min(E, finish_stage_ints(nchunks) / nchunks));
-  const int per = (nchunks + 31) / 32;
-  for (int e0 = 0; e0 < E; e0 += slab) {
-    const int ns = min(slab, E - e0);
-    // stage hist[:, e0 .. e0 + ns) (independent loads, all in flight together)
-    for (int i = tid; i < nchunks * ns; i += kTopkThreads) {
-      const int cc = i / ns, j = i - cc * ns;
-      s_stage[i] = __ldcg(a.chunk_hist + (size_t)cc * E + e0 + j);
-    }
-    __syncthreads();
-    // one warp per expert column: lane l sums chunks [l * per, (l + 1) * per),
-    // a warp exclusive scan gives each lane its base
-    for (int j = warp; j < ns; j += nwarps) {
-      const int cb = lane * per;
-      int local = 0;
-      for (int q = 0; q < per; ++q)
-        if (cb + q < nchunks) local += s_stage[(cb + q) * ns + j];
-      int incl = local;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      int run = incl - local;
-      for (int q = 0; q < per; ++q)
-        if (cb + q < nchunks) {
-          a.chunk_base[(size_t)(cb + q) * E + e0 + j] = run;
-          run += s_stage[(cb + q) * ns + j];
-        }
-      if (lane == 31) s_hist[e0 + j] = incl;
-    }
-    __syncthreads();
-  }
-  for (int i = tid; i < E; i += kTopkThreads) {
-    s_off[i] = s_hist[i];
-    a.counts[i] = s_hist[i];
-  }
-  __syncthreads();
-  block_exclusive_scan(s_off, E, s_scan);
-  if (tid == 0) {
-    s_off[E] = T * k;
-    a.offsets[E] = T * k;
-  }
-  for (int e = tid; e < E; e += kTopkThreads) a.offsets[e] = s_off[e];
-  __syncthreads();
-  if (warp == 0) warp_segments(a, s_hist, s_off);
-  if (tid == 0) *a.ticket = 0u;
 }
 
-// Stable scatter of one chunk's (token, rank) pairs: expert e's pairs of
-// chunk c start at offsets[e] + chunk_base[c][e].
-__global__ void __launch_bounds__(32) k_scatter(RouteArgs a) {
+// Stable scatter of chunk c's (token, rank) pairs. Every chunk CTA reads the
+// whole histogram (independent loads, all in flight together) for its
+// experts' totals and the pairs of earlier chunks; expert e's pairs of chunk
+// c start at offsets[e] + (pairs of e in chunks < c). CTA 0 also writes the
+// counts, offsets and the segment list.
+constexpr int kScatterThreads = 256;
+
+__global__ void __launch_bounds__(kScatterThreads) k_scatter(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int lane = threadIdx.x;
-  const int c = blockIdx.x;
+  __shared__ int s_scan[33];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int c = blockIdx.x, nchunks = gridDim.x;
   const int E = a.E, k = a.k;
-  int* cur = reinterpret_cast<int*>(smem);                           // [E]
-  int32_t* s_ids = cur + E;                                          // [chunk tokens * k]
+  int* s_before = reinterpret_cast<int*>(smem);  // [E]
+  int* s_tot = s_before + E;                     // [E]
+  int* s_off = s_tot + E;                        // [E + 1]
+  int32_t* s_ids = s_off + E + 1;                // [chunk tokens * k]
   pdl_wait();
-  for (int e = lane; e < E; e += 32) cur[e] = __ldcg(a.chunk_base + (size_t)c * E + e) + __ldcg(a.offsets + e);
+  for (int i = tid; i < E; i += kScatterThreads) {
+    s_before[i] = 0;
+    s_tot[i] = 0;
+  }
   const int fbeg = c * kRouteChunkTokens * k;
   const int fend = min(a.T * k, fbeg + kRouteChunkTokens * k);
-  for (int f = fbeg + lane; f < fend; f += 32) s_ids[f - fbeg] = __ldcg(a.ids + f);
-  __syncwarp();
-  warp_stable_scatter(a, s_ids, fbeg, fend, cur);
+  for (int f = fbeg + tid; f < fend; f += kScatterThreads) s_ids[f - fbeg] = __ldcg(a.ids + f);
+  __syncthreads();
+  // (expert, part) per thread: tpe threads split an expert's chunks
+  const int tpe = E >= kScatterThreads ? 1 : kScatterThreads / E;
+  const int per_pass = kScatterThreads / tpe;
+  for (int e0 = 0; e0 < E; e0 += per_pass) {
+    const int e = e0 + tid / tpe, part = tid % tpe;
+    if (tid / tpe < per_pass && e < E) {
+      const int cb = (int)((long long)part * nchunks / tpe), ce = (int)((long long)(part + 1) * nchunks / tpe);
+      int before = 0, tot = 0;
+#pragma unroll 8
+      for (int cc = cb; cc < ce; ++cc) {
+        const int v = __ldcg(a.chunk_hist + (size_t)cc * E + e);
+        tot += v;
+        before += cc < c ? v : 0;
+      }
+      if (tot) atomicAdd(&s_tot[e], tot);
+      if (before) atomicAdd(&s_before[e], before);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < E; i += kScatterThreads) s_off[i] = s_tot[i];
+  __syncthreads();
+  block_exclusive_scan(s_off, E, s_scan);
+  if (tid == 0) s_off[E] = a.T * k;
+  for (int i = tid; i < E; i += kScatterThreads) s_before[i] += s_off[i];  // cursors
+  __syncthreads();
+  if (warp == 0) warp_stable_scatter(a, s_ids, fbeg, fend, s_before);
+  if (c == 0) {
+    for (int i = tid; i < E; i += kScatterThreads) {
+      a.counts[i] = s_tot[i];
+      a.offsets[i] = s_off[i];
+    }
+    if (tid == 0) a.offsets[E] = a.T * k;
+    if (warp == 1) warp_segments(a, s_tot, s_off);
+  }
 }
 
 template <int NV>
@@ -286,16 +263,15 @@ cudaError_t launch_route_large_nv(const RouteArgs& a, cudaStream_t s, bool pdl) 
   cudaError_t e = launch_ex(k_router_logits_split, g1, dim3(kLgThreads), 0, s, pdl, a);
   if (e != cudaSuccess) return e;
   const int nchunks = (a.T + kRouteChunkTokens - 1) / kRouteChunkTokens;
-  const size_t smem2 =
-      ((size_t)kRouteChunkTokens * a.k + 2 * (size_t)a.E + 1 + finish_stage_ints(nchunks)) * sizeof(int);
+  const size_t smem2 = ((size_t)kRouteChunkTokens * a.k + (size_t)a.E) * sizeof(int);
   e = ensure_smem(k_topk_hist<NV>, smem2);
   if (e != cudaSuccess) return e;
   e = launch_ex(k_topk_hist<NV>, dim3(nchunks), dim3(kTopkThreads), smem2, s, pdl, a);
   if (e != cudaSuccess) return e;
-  const size_t smem3 = ((size_t)a.E + (size_t)kRouteChunkTokens * a.k) * sizeof(int);
+  const size_t smem3 = ((size_t)3 * a.E + 1 + (size_t)kRouteChunkTokens * a.k) * sizeof(int);
   e = ensure_smem(k_scatter, smem3);
   if (e != cudaSuccess) return e;
-  return launch_ex(k_scatter, dim3(nchunks), dim3(32), smem3, s, pdl, a);
+  return launch_ex(k_scatter, dim3(nchunks), dim3(kScatterThreads), smem3, s, pdl, a);
 }
 
 }  // namespace
