@@ -188,6 +188,31 @@ def algorithmic(shape, T, eu):
     return b, f, dict(gate_up_per_expert=gate_up, down_per_expert=down)
 
 
+# Sources each measured kernel is built from: a DRAM-traffic figure recorded
+# under profiles/ is reported only while these files are unchanged.
+KERNEL_SOURCES = {
+    "decode": ["decode.cu", "tcgemv_dev.cuh", "route_dev.cuh", "common.cuh", "kernels.h"],
+    "gemv": ["gemv.cu", "tcgemv_dev.cuh", "common.cuh", "kernels.h"],
+    "gemm": ["gemm.cu", "tc.cuh", "common.cuh", "kernels.h"],
+}
+
+
+def kernel_traffic(workload, kern, tensor_path):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch of the
+    dominant kernel, from one ncu capture recorded in profiles/traffic.json,
+    or None when the kernel's sources changed since the capture."""
+    family = "gemm" if tensor_path else ("decode" if kern == "layer" else "gemv")
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as ftr:
+            ent = json.load(ftr).get(workload, {}).get(kern)
+        files = [f"w4a16_routed_expert_gb300/csrc/{f}" for f in KERNEL_SOURCES[family]]
+        if ent and ent.get("source_sha") == source_hash(*files):
+            return ent["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
 def source_hash(*files):
     h = hashlib.sha256()
     for fn in files:
@@ -331,16 +356,7 @@ def run_ours(args):
         kern = "gate_up" if stage[1] >= stage[2] else "down"
         kern_ms = stage[1] if kern == "gate_up" else stage[2]
     tensor_path = T >= args.gemm_min_tokens and shape.hidden % 64 == 0 and shape.intermediate % 64 == 0
-    traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as ftr:
-            tr = json.load(ftr)
-        src = "gemm.cu" if tensor_path else "gemv.cu"
-        ent = tr.get(args.workload, {}).get(kern)
-        if ent and ent.get("source_sha") == source_hash(f"w4a16_routed_expert_gb300/csrc/{src}"):
-            traffic = ent["dram_bytes_per_launch"]
-    except Exception:
-        traffic = None
+    traffic = kernel_traffic(args.workload, kern, tensor_path)
     if tensor_path:
         achieved = f[kern] / (kern_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
@@ -400,7 +416,7 @@ def run_ours(args):
     return {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded; INT4 codes quantised from N(0,0.02) weights)",
+        "dtype": "f16", "data": "synthetic (seeded; INT4 codes quantised from N(0,0.02) weights)",
         "config": {"workload": args.workload, "description": desc, "hidden": shape.hidden,
                    "intermediate": shape.intermediate, "experts": shape.num_experts, "top_k": shape.top_k,
                    "shared_expert": shape.has_shared, "group_size": shape.group_size,
@@ -434,7 +450,7 @@ def _mk_layer(MoELayer, torch, dev, lay, max_tokens, add_residual=False, partial
 
 def _common(args, world, desc, shape, T, extra_cfg):
     return {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded; INT4 codes quantised from N(0,0.02) weights)",
             "config": dict({"workload": args.workload, "description": desc, "hidden": shape.hidden,
                             "intermediate": shape.intermediate, "experts": shape.num_experts,

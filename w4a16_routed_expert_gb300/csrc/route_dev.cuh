@@ -475,12 +475,7 @@ __device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* sc
   int32_t* s_ids = scratch;
   if (TINY_ONLY || T * k <= 32) {
     int32_t* s_sorted = s_ids + 32 + E + 1;
-    if constexpr (TINY_ONLY) {
-      // one token per warp: no block-wide phases for a batch this small
-      for (int t = warp; t < T; t += blockDim.x >> 5) warp_softmax_topk<NV>(a, t, s_ids + t * k, part);
-    } else {
-      cta_softmax_topk<NV>(a, part, fbuf, s_ids);
-    }
+    cta_softmax_topk<NV>(a, part, fbuf, s_ids);
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
     finish_tiny(a, s_ids, s_sorted);
