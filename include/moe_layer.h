@@ -9,7 +9,9 @@
  *   logits  L[t][e] = sum_h x[t][h] * Wr[e][h] (+ bias[e])        FP32
  *   p[t]    = softmax over all E experts of L[t]                  FP32
  *   ids[t]  = the top_k experts of L[t], ties to the lower id,
- *             in rank order (descending logit, then ascending id)
+ *             in rank order (descending logit, then ascending id);
+ *             a NaN logit ranks below every number (inputs with NaN or
+ *             Inf give a well-defined selection, never a stalled launch)
  *   w[t][j] = p[t][ids[t][j]]  (divided by sum_j p[t][ids[t][j]] when
  *             renormalising)
  *   y_e(x)  = Wd_e (silu(Wg_e x) * (Wu_e x)),  silu(z) = z / (1 + e^-z),

@@ -1,0 +1,70 @@
+"""Non-finite inputs: a token whose hidden state holds NaN or Inf still gets a
+well-defined selection (NaN logits rank below every number, ties to the
+lower id), so every CTA that routes it agrees and the launch completes
+without a device-side wait giving up. Finite tokens of the same batch are
+unaffected (checked against the oracle)."""
+import time
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+from w4a16_routed_expert_gb300 import capi, synth  # noqa: E402
+
+import gpu_harness as GH  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    capi.lib()
+
+
+@pytest.fixture(scope="module")
+def olmoe_layer():
+    return synth.make_layer(synth.OLMOE, seed=11)
+
+
+def _poison(x, rows, kind):
+    x = x.copy()
+    for r in rows:
+        if kind == "nan":
+            x[r, ::7] = np.float16(np.nan)
+        elif kind == "inf":
+            x[r, 3] = np.float16(np.inf)
+            x[r, 9] = np.float16(-np.inf)
+        else:  # overflowing magnitudes: logits become +-inf or nan
+            x[r, :] = np.float16(60000.0)
+    return x
+
+
+@pytest.mark.parametrize("T", [1, 4, 16, 40])
+@pytest.mark.parametrize("kind", ["nan", "inf", "huge"])
+def test_non_finite_tokens_complete_and_route_validly(olmoe_layer, T, kind):
+    shape = synth.OLMOE
+    x = synth.make_tokens(shape.hidden, T, seed=100 + T)
+    bad = [0] if T == 1 else [0, T - 1]
+    xp = _poison(x, bad, kind)
+    ml = GH.upload(olmoe_layer, max_tokens=T)
+    for rep in range(2):  # twice in a row: the launch leaves its counters clean
+        t0 = time.perf_counter()
+        g = GH.run(ml, xp)  # raises on MOE_ERR_TIMEOUT
+        assert time.perf_counter() - t0 < 1.0, "launch took longer than any device wait should"
+        ids = g["ids"]
+        assert ids.min() >= 0 and ids.max() < shape.num_experts
+        for t in range(T):
+            assert len(set(ids[t].tolist())) == shape.top_k, f"token {t}: repeated expert"
+        assert int(g["counts"].sum()) == T * shape.top_k
+    ml.close()
+    good = [t for t in range(T) if t not in bad]
+    if good:
+        ref_ml = GH.upload(olmoe_layer, max_tokens=T)
+        sub = GH.run(ref_ml, x)  # same tokens, all finite
+        ref_ml.close()
+        ref_ids = sub["ids"][good]
+        assert np.array_equal(g["ids"][good], ref_ids)
+        assert np.array_equal(g["out"][good], sub["out"][good])

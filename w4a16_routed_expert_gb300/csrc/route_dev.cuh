@@ -131,6 +131,11 @@ __device__ __forceinline__ float logit_from_planes(const RouteArgs& a, int t, in
   return v + (a.bias ? __ldg(a.bias + e) : 0.f);
 }
 
+// Selection key of a logit: NaN ranks below every number (as -inf), so the
+// order (key descending, id ascending) is total for any input and every CTA
+// that routes the same logits derives the same selection.
+__device__ __forceinline__ float route_key(float v) { return v != v ? -INFINITY : v; }
+
 // One warp: softmax over the E logits of token t and selection of the top k
 // (largest logit first, lower id first among equal logits). NV = values held
 // per lane (E <= 32 * NV). Writes ids / weights to the workspace, the user
@@ -148,11 +153,11 @@ __device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int
     if (e >= E)
       v[i] = -INFINITY;
     else if (part)
-      v[i] = logit_from_parts(a, part, t, e);
+      v[i] = route_key(logit_from_parts(a, part, t, e));
     else if (a.nsplit > 0)
-      v[i] = logit_from_planes(a, t, e);
+      v[i] = route_key(logit_from_planes(a, t, e));
     else
-      v[i] = __ldcg(L + e);
+      v[i] = route_key(__ldcg(L + e));
   }
   float m = -INFINITY;
 #pragma unroll
@@ -382,7 +387,7 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
   float* sp = den + T;    // [T][k] probabilities by rank
   for (int i = tid; i < n; i += blockDim.x) {
     const int t = i / E, e = i - t * E;
-    lg[i] = part ? logit_from_parts(a, part, t, e) : __ldcg(a.logits + i);
+    lg[i] = route_key(part ? logit_from_parts(a, part, t, e) : __ldcg(a.logits + i));
   }
   for (int i = tid; i < T * k; i += blockDim.x) {
     s_sel[i] = 0;  // defined even if NaN logits leave a rank unfilled
