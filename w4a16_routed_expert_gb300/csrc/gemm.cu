@@ -378,6 +378,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                                          (upper ? a.s_off1 : a.s_off0)) +
                          (size_t)(m0 + unit) * a.ng;
       const int ngroups = (nK + kCodeK - 1) / kCodeK;
+      // this row's scale for the group's next K step, loaded one step ahead
+      // so its latency overlaps the current step's conversion
+      __half sv_next = (rvalid && par < nK) ? __ldg(sp + (par * BK) / a.G) : __float2half(0.f);
       for (int grp = 0; grp < ngroups && ok; ++grp, ++gc) {
         const int sc = gc % kCodeStages;
         int good = 1;
@@ -393,7 +396,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kk = grp * kCodeK + par; kk < k_end; kk += 2) {
           const uint32_t g = gbase + (uint32_t)kk;
           const int sa = g % kAStages;
-          const __half sv = rvalid ? __ldg(sp + (kk * BK) / a.G) : __float2half(0.f);
+          const __half sv = sv_next;
+          if (rvalid && kk + 2 < nK) sv_next = __ldg(sp + ((kk + 2) * BK) / a.G);
           if (lane == 0)
             good = timed_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err, rec ? &dw[1] : nullptr);
           good = __shfl_sync(0xffffffffu, good, 0);
