@@ -255,6 +255,7 @@ def test_single_launch_decode_matches_multi_kernel_path(shape, seed, T, monkeypa
     experts with the same work items, so every output is bit-identical."""
     lay = synth.make_layer(shape, seed=seed)
     x = synth.make_tokens(shape.hidden, T, seed=seed)
+    monkeypatch.setenv("MOE_MEGAKERNEL_MAX_T", "16")  # the one-launch path for every T here
     mk = GH.upload(lay, max_tokens=T)
     a = GH.run(mk, x)
     b2 = GH.run(mk, x)

@@ -76,13 +76,14 @@ struct moe_layer {
   int32_t* ids_stage = nullptr;
   float* w_stage = nullptr;
   int last_T = 0;
-  bool megakernel = true;        // single-launch decode for T <= 16 (full residency)
+  bool megakernel = true;        // single-launch decode (full residency)
+  int megakernel_max_tokens = 4;  // largest T it takes (<= 16); measured faster than the multi-kernel path up to 4
   bool last_single = false;      // the last profiled forward was one launch
   unsigned long long* trace = nullptr;  // per-CTA phase stamps of the single-launch decode (MOE_TRACE=1)
   unsigned long long* gemm_stats = nullptr;  // GEMM wait counters (MOE_GEMM_STATS=1): [2][CTAs][kGemmStats]
   uint32_t* ctr = nullptr;       // megakernel counters (zero between launches)
   // prefill (tensor-core) path
-  int gemm_min_tokens = 256;
+  int gemm_min_tokens = 48;  // tensor-core GEMM from this T (below it the grouped GEMV is faster)
   bool gemm_ok = false;         // shapes suit the GEMM (H, I multiples of 64)
   moe::CodeMaps pool_maps = {};  // code sections of the caller's pool (full residency)
   moe::TcGemvPlan dec_pg = {}, dec_pd = {};  // GEMV work items: gate/up, down

@@ -152,6 +152,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
   L->pdl = !(pdl_env && pdl_env[0] == '0');
   const char* mk_env = getenv("MOE_MEGAKERNEL");
   L->megakernel = !(mk_env && mk_env[0] == '0');
+  if (const char* mt = getenv("MOE_MEGAKERNEL_MAX_T"))
+    L->megakernel_max_tokens = std::max(1, std::min(moe::kSmallRouteMaxT, atoi(mt)));
   // probed here, at create time, so that no capture sees a rejected launch
   L->decode_pdl = L->pdl && moe::decode_pdl_supported();
   cudaError_t e = cudaGetDevice(&L->device);
@@ -621,7 +623,7 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
   // programmatic dependent launch only on explicitly created streams
   const bool pdl_saved = layer->pdl;
   if (s == nullptr) layer->pdl = false;
-  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->megakernel && T <= moe::kSmallRouteMaxT) {
+  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->megakernel && T <= layer->megakernel_max_tokens) {
     moe_status_t sd = moe::enqueue_decode(layer, xh, T, oh, topk_ids, topk_w, s);
     if (sd != MOE_ERR_UNSUPPORTED) {
       layer->pdl = pdl_saved;
