@@ -320,11 +320,7 @@ def run_ours(args):
     el_ms = start.elapsed_time(end)
     for l in layers:
         l.sync()  # raises if any device-side wait of the timed launches gave up
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([el_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el_ms = float(t.item())
+    el_ms = _max_over_ranks(torch, dev, world, el_ms)
     # keep the GPU loaded long enough for the clock sampler to see it
     soak_t0 = time.perf_counter()
     while time.perf_counter() - soak_t0 < max(0.0, 1.5 - (t_wall1 - t_wall0)):
@@ -337,7 +333,7 @@ def run_ours(args):
     clocks["window"] = "timed region" if soak_t1 - soak_t0 < 0.01 else "timed region + untimed replay of the same graph"
 
     ms_per_step = el_ms / K
-    value = T * world / (ms_per_step / 1e3)
+    value = replica_throughput(T, world, ms_per_step)
 
     # per-stage CUDA events (profiling graph of the same R forwards)
     for l in layers:
@@ -410,13 +406,8 @@ def run_ours(args):
     e1.record()
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": T * K * world / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms = _max_over_ranks(torch, dev, world, e0.elapsed_time(e1))
+    e2e = {"value": replica_throughput(T, world, e2e_ms / K), "unit": "tokens/s",
            "h2d_bytes_per_step": T * shape.hidden * 2,
            "d2h_bytes_per_step": T * shape.hidden * 2 + T * shape.top_k * 8,
            "path": "moe_layer_forward_host (pinned host x -> device, forward, out/ids/weights -> host)"}
@@ -473,7 +464,15 @@ def _common(args, world, desc, shape, T, extra_cfg):
                             "parallelism": "replicas" if world > 1 else "single GPU"}, **extra_cfg)}
 
 
+def replica_throughput(tokens_per_rank, world, ms_per_step):
+    """Whole-job tokens/s of `world` independent replicas, each processing
+    tokens_per_rank tokens per step, timed by the slowest rank."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 def _max_over_ranks(torch, dev, world, v):
+    """The slowest rank's time (every rank gets it). The data path has no
+    collective: this is the only exchange between replicas."""
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([v], dtype=torch.float64, device=dev)
@@ -621,7 +620,7 @@ def run_stack(args):
         "layers": STACK_LAYERS, "l2": f"inputs larger than L2: {STACK_LAYERS} layers hold "
         f"{STACK_LAYERS * lays[0].records.nbytes / 1e9:.2f} GB of experts"})
     res.update({
-        "value": T * world / (ms_per_step / 1e3), "ms_per_step": ms_per_step,
+        "value": replica_throughput(T, world, ms_per_step), "ms_per_step": ms_per_step,
         "roofline": roofline,
         "layer_roofline": {"bytes_per_step": step_bytes, "achieved_gbs": step_bytes / (ms_per_step / 1e3) / 1e9,
                            "hbm_frac": step_bytes / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
@@ -629,7 +628,7 @@ def run_stack(args):
         "stage_ms": ({"layer (single launch)": st[4], "total": st[4]} if single else
                      {"route": st[0], "gate_up": st[1], "down": st[2], "combine": st[3], "total": st[4]}),
         "cpu_baseline": cpu_base,
-        "e2e": {"value": T * K * world / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": T * shape.hidden * 2,
+        "e2e": {"value": replica_throughput(T, world, e2e_ms / K), "unit": "tokens/s", "h2d_bytes_per_step": T * shape.hidden * 2,
                 "d2h_bytes_per_step": T * shape.hidden * 2,
                 "path": "host x -> device, 16 x moe_layer_forward, last output -> host"},
         "clocks": clocks,
@@ -732,7 +731,7 @@ def run_partial(args):
     res = _common(args, world, desc, shape, T, {"slots": PARTIAL_SLOTS, "l2": "expert copies stream from host "
                                                 "memory every step (pool of 32 of 128 experts)"})
     res.update({
-        "value": T * world / (ms_per_step / 1e3), "ms_per_step": ms_per_step,
+        "value": replica_throughput(T, world, ms_per_step), "ms_per_step": ms_per_step,
         "roofline": {"bound": "h2d", "kernel": "expert record copies (host -> device)", "achieved": h2d_gbs,
                      "peak": h2d_peak, "unit": "GB/s", "frac": h2d_gbs / h2d_peak,
                      "peak_source": "measured in this run: pinned 1 GiB host -> device copies",
@@ -742,7 +741,7 @@ def run_partial(args):
                       "d2h_expert_bytes": int(st.d2h_expert_bytes)},
         "layer_roofline": {"flops_per_step": flops, "achieved_tflops": flops / (ms_per_step / 1e3) / 1e12},
         "cpu_baseline": cpu_base,
-        "e2e": {"value": T * K * world / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": {"value": replica_throughput(T, world, e2e_ms / K), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * shape.hidden * 2,
                 "d2h_bytes_per_step": T * shape.hidden * 2 + T * shape.top_k * 8,
                 "path": "moe_layer_forward_host"},
