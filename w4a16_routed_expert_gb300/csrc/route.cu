@@ -74,92 +74,123 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
 }
 
 // ------------------------------------------------------------ large path
-// Router logits, split over K: CTA (bx, by, p) computes the partial dot
-// products of 128 tokens x 64 experts over K part p (32-wide K chunks
-// [p * nch / P, (p + 1) * nch / P)) in FP32 and writes plane p of the logits
-// workspace ([P][T][E]); the top-k kernel sums the planes in order and adds
-// the bias. Each thread holds 8 tokens x 4 experts; the next K chunk is
-// loaded into registers while the current one is multiplied.
-constexpr int kLgTok = 128;
+// Router logits on the tensor cores, split over K. CTA (bx, by, p) computes
+// the partial dot products of 64 tokens x 64 experts over K part p (32-wide
+// K chunks [p * nch / P, (p + 1) * nch / P)) and writes plane p of the
+// logits workspace ([P][T][E]); the top-k kernel sums the planes in order
+// and adds the bias.
+//
+// x is FP16, so each product x * w is exact in FP32 once w is; the FP32
+// router weight is split as w = hi + lo * 2^-11 with hi = fp16(w) and
+// lo = fp16((w - hi) * 2^11) (together ~22 significant bits), and
+// mma.sync m16n8k16 accumulates sum x * hi and sum x * lo separately in
+// FP32; the plane gets acc_hi + acc_lo * 2^-11. Warp w holds tokens
+// 16 w .. 16 w + 15 and all 64 experts (8 n-tiles of 8). The next K chunk
+// is loaded into registers while the current one is multiplied.
+constexpr int kLgTok = 64;
 constexpr int kLgExp = 64;
 constexpr int kLgK = 32;
-constexpr int kLgThreads = 256;
+constexpr int kLgThreads = 128;
+constexpr int kLgStride = kLgK + 8;  // halves per staged row: 80 bytes, conflict-free fragment reads
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
 __global__ void __launch_bounds__(kLgThreads) k_router_logits_split(RouteArgs a) {
-  __shared__ __align__(16) float xs[kLgK][kLgTok + 4];  // [k][token]
-  __shared__ __align__(16) float ws[kLgK][kLgExp + 4];  // [k][expert]
-  const int tid = threadIdx.x;
+  __shared__ __align__(16) __half xs[kLgTok][kLgStride];  // [token][k]
+  __shared__ __align__(16) __half wh[kLgExp][kLgStride];  // [expert][k], hi part
+  __shared__ __align__(16) __half wl[kLgExp][kLgStride];  // [expert][k], lo part x 2^11
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
   const int t0 = blockIdx.x * kLgTok, e0 = blockIdx.y * kLgExp, p = blockIdx.z;
   const int T = a.T, H = a.H, E = a.E, P = a.nsplit;
   const int nch = H / kLgK;
   const int c0 = (int)((long long)p * nch / P), c1 = (int)((long long)(p + 1) * nch / P);
-  const int ty = tid >> 4, tx = tid & 15;  // tokens 8 ty .. 8 ty + 7, experts 4 tx .. 4 tx + 3
-  // loader roles: x row lt (16 halves at kq), router row le (8 floats at kw)
-  const int lt = tid >> 1, kq = (tid & 1) * 16;
-  const int le = tid >> 2, kw = (tid & 3) * 8;
-  const bool xrow = t0 + lt < T, wrow = e0 + le < E;
-  const uint4* xsrc = reinterpret_cast<const uint4*>(a.x + (size_t)(xrow ? t0 + lt : 0) * H + kq);
-  const float4* wsrc = reinterpret_cast<const float4*>(a.wr + (size_t)(wrow ? e0 + le : 0) * H + kw);
+  // loader roles: x row lx (16 halves at kx); router row lw (16 floats at kw)
+  const int lx = tid >> 1, kx = (tid & 1) * 16;
+  const int lw = tid >> 1, kw = (tid & 1) * 16;
+  const bool xrow = t0 + lx < T, wrow = e0 + lw < E;
+  const uint4* xsrc = reinterpret_cast<const uint4*>(a.x + (size_t)(xrow ? t0 + lx : 0) * H + kx);
+  const float4* wsrc = reinterpret_cast<const float4*>(a.wr + (size_t)(wrow ? e0 + lw : 0) * H + kw);
   pdl_wait();
-  float acc[8][4];
+  float ah[8][4], al[8][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int n = 0; n < 8; ++n)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int i = 0; i < 4; ++i) ah[n][i] = al[n][i] = 0.f;
   uint4 xr0 = make_uint4(0u, 0u, 0u, 0u), xr1 = xr0;
-  float4 wr0 = make_float4(0.f, 0.f, 0.f, 0.f), wr1 = wr0;
-  auto load = [&](int c) {
-    const int o = c * kLgK;
+  float4 wr[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) wr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto load = [&](int ch) {
+    const int o = ch * kLgK;
     if (xrow) {
       xr0 = __ldg(xsrc + o / 8);
       xr1 = __ldg(xsrc + o / 8 + 1);
     }
     if (wrow) {
-      wr0 = __ldg(wsrc + o / 4);
-      wr1 = __ldg(wsrc + o / 4 + 1);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) wr[i] = __ldg(wsrc + o / 4 + i);
     }
   };
   if (c0 < c1) load(c0);
-  for (int c = c0; c < c1; ++c) {
+  for (int ch = c0; ch < c1; ++ch) {
     {
-      const uint32_t hx[8] = {xr0.x, xr0.y, xr0.z, xr0.w, xr1.x, xr1.y, xr1.z, xr1.w};
+      *reinterpret_cast<uint4*>(&xs[lx][kx]) = xr0;
+      *reinterpret_cast<uint4*>(&xs[lx][kx + 8]) = xr1;
+      __align__(16) __half hh[16], hl[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hx[u]));
-        xs[kq + 2 * u][lt] = f.x;
-        xs[kq + 2 * u + 1][lt] = f.y;
+      for (int i = 0; i < 4; ++i) {
+        const float v[4] = {wr[i].x, wr[i].y, wr[i].z, wr[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __half h = __float2half_rn(v[j]);
+          hh[4 * i + j] = h;
+          hl[4 * i + j] = __float2half_rn((v[j] - __half2float(h)) * 2048.f);
+        }
       }
-      const float wv[8] = {wr0.x, wr0.y, wr0.z, wr0.w, wr1.x, wr1.y, wr1.z, wr1.w};
-#pragma unroll
-      for (int u = 0; u < 8; ++u) ws[kw + u][le] = wv[u];
+      *reinterpret_cast<uint4*>(&wh[lw][kw]) = *reinterpret_cast<const uint4*>(&hh[0]);
+      *reinterpret_cast<uint4*>(&wh[lw][kw + 8]) = *reinterpret_cast<const uint4*>(&hh[8]);
+      *reinterpret_cast<uint4*>(&wl[lw][kw]) = *reinterpret_cast<const uint4*>(&hl[0]);
+      *reinterpret_cast<uint4*>(&wl[lw][kw + 8]) = *reinterpret_cast<const uint4*>(&hl[8]);
     }
     __syncthreads();
-    if (c + 1 < c1) load(c + 1);
-#pragma unroll 8
-    for (int kk = 0; kk < kLgK; ++kk) {
-      const float4 xa = *reinterpret_cast<const float4*>(&xs[kk][8 * ty]);
-      const float4 xb = *reinterpret_cast<const float4*>(&xs[kk][8 * ty + 4]);
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
-      const float xv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-      const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+    if (ch + 1 < c1) load(ch + 1);
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
+    for (int kb = 0; kb < kLgK; kb += 16) {
+      const int r = 16 * warp + g;
+      const uint32_t a0 = *reinterpret_cast<const uint32_t*>(&xs[r][kb + 2 * c]);
+      const uint32_t a1 = *reinterpret_cast<const uint32_t*>(&xs[r + 8][kb + 2 * c]);
+      const uint32_t a2 = *reinterpret_cast<const uint32_t*>(&xs[r][kb + 2 * c + 8]);
+      const uint32_t a3 = *reinterpret_cast<const uint32_t*>(&xs[r + 8][kb + 2 * c + 8]);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], wa[j], acc[i][j]);
+      for (int n = 0; n < 8; ++n) {
+        const int ew = 8 * n + g;
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t*>(&wh[ew][kb + 2 * c]);
+        const uint32_t bh1 = *reinterpret_cast<const uint32_t*>(&wh[ew][kb + 2 * c + 8]);
+        const uint32_t bl0 = *reinterpret_cast<const uint32_t*>(&wl[ew][kb + 2 * c]);
+        const uint32_t bl1 = *reinterpret_cast<const uint32_t*>(&wl[ew][kb + 2 * c + 8]);
+        mma_f16_16816(ah[n], a0, a1, a2, a3, bh0, bh1);
+        mma_f16_16816(al[n], a0, a1, a2, a3, bl0, bl1);
+      }
     }
     __syncthreads();
   }
+  // D fragment: rows g / g + 8 (tokens), columns 2c / 2c + 1 (experts)
   float* plane = a.logits + (size_t)p * T * E;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int t = t0 + 8 * ty + i;
-    if (t >= T) continue;
+  for (int n = 0; n < 8; ++n)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + 4 * tx + j;
-      if (e < E) plane[(size_t)t * E + e] = acc[i][j];
+    for (int i = 0; i < 4; ++i) {
+      const int t = t0 + 16 * warp + g + ((i & 2) ? 8 : 0);
+      const int e = e0 + 8 * n + 2 * c + (i & 1);
+      if (t < T && e < E) plane[(size_t)t * E + e] = ah[n][i] + al[n][i] * (1.f / 2048.f);
     }
-  }
 }
 
 // Softmax, top-k and the expert histogram of one chunk of kRouteChunkTokens
@@ -288,7 +319,7 @@ int router_split(int T, int E, int H, int num_sms) {
   const int tiles = ((T + kLgTok - 1) / kLgTok) * ((E + kLgExp - 1) / kLgExp);
   const int nch = H / kLgK;
   int p = 1;
-  while (p < kRouterSplitMax && tiles * p < num_sms && nch >= 4 * p) p *= 2;
+  while (p < kRouterSplitMax && tiles * p < 3 * num_sms && nch >= 4 * p) p *= 2;
   return p;
 }
 
