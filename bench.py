@@ -746,7 +746,9 @@ def run_partial(args):
                 "d2h_bytes_per_step": T * shape.hidden * 2 + T * shape.top_k * 8,
                 "path": "moe_layer_forward_host"},
         "clocks": sampler.summary(t0, t1),
-        "gpu_launches": None,
+        # routing, then per wave of resident experts the expert kernels, then the combine
+        "gpu_launches": int(round(K * ((1 if T <= 16 else 3) + (s1.waves - s0.waves) / K * (
+            3 if T >= args.gemm_min_tokens else 2) + 1))),
     })
     return res
 
