@@ -1,0 +1,61 @@
+"""The bench's roofline arithmetic against closed-form sizes of the layer:
+algorithmic bytes (every selected expert's record read once, the router
+weights, x in and out) and FLOPs (2 H E per token for the router, 6 H I per
+(token, expert) pair for gate/up/down), plus its launch and throughput
+accounting. CPU only."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from w4a16_routed_expert_gb300 import synth  # noqa: E402
+
+
+def _payload(H, I, G):
+    """Codes + scales of one expert record (no alignment padding)."""
+    return 3 * H * I // 2 + 2 * I * (-(-H // G)) * 2 + H * (-(-I // G)) * 2
+
+
+def test_olmoe_batch1_layer_bytes():
+    s = synth.OLMOE
+    b, f, per = bench.algorithmic(s, 1, 8)
+    assert _payload(2048, 1024, 128) == 3_244_032
+    assert b["layer"] == 8 * 3_244_032 + 64 * 2048 * 4 + 2 * 2048 * 2 == 26_484_736
+    assert per["gate_up_per_expert"] == 2_162_688 and per["down_per_expert"] == 1_081_344
+    assert f["layer"] == 2 * 2048 * 64 + 8 * 6 * 2048 * 1024
+
+
+def test_prefill_flops_make_it_tensor_bound():
+    s = synth.OLMOE
+    b, f, _ = bench.algorithmic(s, 8192, 64)
+    assert f["layer"] == 2 * 8192 * 2048 * 64 + 8192 * 8 * 6 * 2048 * 1024
+    assert f["gate_up"] == 8192 * 8 * 4 * 2048 * 1024 and f["down"] == 8192 * 8 * 2 * 2048 * 1024
+    # about 827 GFLOP against about 0.2 GB: the FLOPs set the roofline time
+    assert abs(f["layer"] / 1e9 - 826.8) < 1.0
+    peaks = bench._peaks()
+    assert f["layer"] / (peaks["bf16_tflops"] * 1e12) > b["layer"] / (peaks["hbm_gbs"] * 1e9)
+
+
+def test_many_experts_batch1_includes_shared_expert_and_router():
+    s = synth.MANY_EXPERTS
+    b, f, _ = bench.algorithmic(s, 1, 10)
+    rec = _payload(2048, 512, 128)
+    assert rec == 1_622_016
+    assert b["layer"] == 11 * rec + 512 * 2048 * 4 + 2 * 2048 * 2
+    assert f["layer"] == 2 * 2048 * 512 + 11 * 6 * 2048 * 512
+
+
+@pytest.mark.parametrize("T,gmin,expect", [(8, 48, 4), (16, 48, 4), (17, 48, 6), (47, 48, 6), (48, 48, 7),
+                                           (8192, 48, 7)])
+def test_multi_kernel_launch_count(T, gmin, expect):
+    # routing (1 kernel up to 16 tokens, else 3) + experts (2 GEMV or gather + 2 GEMM) + combine
+    assert bench.launches_per_multi_kernel_forward(T, gmin) == expect
+
+
+def test_replica_throughput():
+    assert bench.replica_throughput(1, 1, 0.025) == pytest.approx(40_000.0)
+    assert bench.replica_throughput(16, 4, 0.1) == pytest.approx(640_000.0)
