@@ -59,6 +59,7 @@ WORKLOADS = {
 STACK_LAYERS = 16
 PARTIAL_SLOTS = 32
 DEFAULT_WORKLOAD = "olmoe-decode-t1"
+PREFILL_WORKLOAD = "olmoe-prefill-t8192"
 
 
 def _peaks():
@@ -231,37 +232,115 @@ def source_hash(*files):
     return h.hexdigest()[:16]
 
 
-def run_ours(args):
-    import torch
+def _bench_tokens(shape, T, rank, R):
+    """The R token batches a rank's timed steps rotate over."""
+    return [synth.make_tokens(shape.hidden, T, seed=1000 * (rank + 1) + r) for r in range(R)]
 
-    from w4a16_routed_expert_gb300 import build as B
-    from w4a16_routed_expert_gb300 import capi
-    from w4a16_routed_expert_gb300.layer import MoELayer
 
-    world, rank, local = _dist()
-    shape, T, seed, desc = WORKLOADS[args.workload]
-    lay = synth.make_layer(shape, seed=seed)
-
-    cpu_base = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sdesc, el = oracle_sample(lay, shape, T, seed, args.cpu_seconds)
-        cpu_base = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sdesc}
-
-    if not os.path.exists(capi.LIB_PATH):
-        B.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    props = torch.cuda.get_device_properties(dev)
-    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2**20
+def _rotation(shape, T, lay, l2_bytes):
+    """Copies of the expert table the steps rotate over: a copy is not
+    revisited before at least twice the L2 capacity of other expert bytes."""
     rec = lay.records.shape[1]
     max_eu = min(shape.num_experts, T * shape.top_k) + (1 if shape.has_shared else 0)
     touched = max_eu * rec
-    R = int(min(16, max(2, math.ceil(2 * l2 / touched) + 1)))
+    return int(min(16, max(2, math.ceil(2 * l2_bytes / touched) + 1)))
 
+
+PARITY_MAX_ROWS = 64
+
+
+def _parity_rows(T):
+    """Tokens of the bench's first batch whose outputs the parity record
+    compares: all of them up to 64, else 64 spread over the batch."""
+    if T <= PARITY_MAX_ROWS:
+        return np.arange(T)
+    return np.unique(np.linspace(0, T - 1, PARITY_MAX_ROWS).round().astype(np.int64))
+
+
+def cpu_leg(args, lay, shape, T, seed, x_check, time_it=True):
+    """The CPU-baseline leg: the oracle, as it stands, timed on bounded samples
+    of the workload on one host core and then on all of them (a child
+    process whose BLAS may use every core), plus the oracle's result for the
+    bench's own first batch (routing of every token, outputs of up to 64
+    tokens), which the parity record compares with the GPU's."""
+    from oracle import moe_oracle as O
+    base = None
+    if time_it:
+        v, sdesc, _ = oracle_sample(lay, shape, T, seed, args.cpu_seconds)
+        base = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sdesc,
+                "host_cores": os.cpu_count()}
+        allc = _all_core_sample(args.workload, args.cpu_seconds)
+        if allc is not None:
+            base["all_cores"] = allc
+    kw = dict(H=shape.hidden, I=shape.intermediate, E=shape.num_experts, k=shape.top_k, G=shape.group_size,
+              renormalize=shape.renormalize, has_shared=shape.has_shared)
+    rows = _parity_rows(T)
+    ref = O.moe_forward(x_check, lay.router_w, lay.router_bias, lay.records, lay.expert_to_slot,
+                        tokens=rows, **kw)
+    near = O.near_tie_tokens(ref["logits"], shape.top_k, 1e-3)
+    return base, dict(ids=ref["ids"], out=ref["out"], rows=rows, near=near)
+
+
+def _all_core_sample(workload, seconds):
+    """The same bounded oracle sample in a child process whose BLAS threads
+    are not limited (all host cores); None if the child fails."""
+    env = dict(os.environ)
+    n = str(os.cpu_count() or 1)
+    for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = n
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", "--workload", workload,
+                            "--cpu-seconds", str(seconds)], capture_output=True, text=True, env=env,
+                           timeout=max(120.0, 6 * seconds))
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+
+
+def cpu_worker(args):
+    shape, T, seed, _ = WORKLOADS[args.workload]
+    lay = synth.make_layer(shape, seed=seed if not args.workload.startswith("olmoe-stack")
+                           else synth.stack_layer_seed(seed, 0))
+    v, desc, _ = oracle_sample(lay, shape, T, seed, args.cpu_seconds)
+    scale = STACK_LAYERS if args.workload.startswith("olmoe-stack") else 1
+    print(json.dumps({"value": v / scale, "unit": "tokens/s", "cores": os.cpu_count(),
+                      "blas_threads": int(os.environ.get("OPENBLAS_NUM_THREADS", "0") or 0), "sample": desc}))
+
+
+def parity_record(shape, ref, ids, out):
+    """The GPU's routing of the bench's first batch against the oracle's
+    (bit-exact ids on tokens decided beyond the 1e-3 near-tie margin) and its
+    outputs on the compared rows (|gpu - oracle| <= 2e-3 max(1, |oracle|) on
+    decided tokens). Near-tie tokens are counted, not compared."""
+    near = set(int(t) for t in ref["near"])
+    T = ids.shape[0]
+    decided = np.array([t for t in range(T) if t not in near], dtype=np.int64)
+    ids_ok = bool(np.array_equal(ids[decided], ref["ids"][decided])) if decided.size else True
+    rows = ref["rows"]
+    keep = [i for i, t in enumerate(rows) if int(t) not in near]
+    got = out[rows[keep]].astype(np.float64)
+    exp = ref["out"][keep]
+    ratio = float((np.abs(got - exp) / (2e-3 * np.maximum(1.0, np.abs(exp)))).max()) if keep else 0.0
+    return {"tokens_routed": int(T), "ids_bit_exact_on_decided": ids_ok, "near_ties": len(near),
+            "rows_compared": len(keep), "max_err_over_bound": ratio,
+            "pass": bool(ids_ok and ratio <= 1.0 and np.isfinite(got).all()),
+            "acceptance": "ids bit-exact where the k-th and (k+1)-th logits differ by > 1e-3; "
+                          "outputs within 2e-3 max(1, |oracle|)"}
+
+
+def measure(args, workload, K, W, lay, xs_np, ref, l2):
+    """Times K steps (one whole forward each, replayed from a CUDA graph) of
+    the workload on this rank's GPU and returns its result block."""
+    import torch
+
+    from w4a16_routed_expert_gb300.layer import MoELayer
+
+    world, rank, local = _dist()
+    shape, T, seed, desc = WORKLOADS[workload]
+    dev = torch.device("cuda", local)
+    R = len(xs_np)
     pools, routers, biases, e2ss, layers, xs, outs = [], [], [], [], [], [], []
     for r in range(R):
         pools.append(torch.from_numpy(lay.records).to(dev))
@@ -272,10 +351,9 @@ def run_ours(args):
                                top_k=shape.top_k, group_size=shape.group_size, renormalize=shape.renormalize,
                                has_shared=shape.has_shared, max_tokens=T, router_w=routers[r],
                                router_bias=biases[r], pool=pools[r], expert_to_slot=e2ss[r]))
-        xs.append(torch.from_numpy(synth.make_tokens(shape.hidden, T, seed=1000 * (rank + 1) + r)).to(dev))
+        xs.append(torch.from_numpy(xs_np[r]).to(dev))
         outs.append(torch.empty_like(xs[-1]))
 
-    K, W = args.steps, args.warmup
     launches_per_forward = launches_per_multi_kernel_forward(T, args.gemm_min_tokens)
     for i in range(max(W, R)):
         layers[i % R].forward(xs[i % R], out=outs[i % R])
@@ -335,7 +413,9 @@ def run_ours(args):
     ms_per_step = el_ms / K
     value = replica_throughput(T, world, ms_per_step)
 
-    # per-stage CUDA events (profiling graph of the same R forwards)
+    # per-stage CUDA events (profiling graph of the same R forwards): the
+    # events between launches serialise them, so these times are used for
+    # the split between stages and for the multi-kernel dominant kernel only
     for l in layers:
         l.set_profiling(True)
     g_prof = capture(R)
@@ -358,28 +438,32 @@ def run_ours(args):
     eu = eu_sum / nprof
     peaks = _peaks()
     b, f, per = algorithmic(shape, T, eu)
-    if single_launch:  # the decode megakernel: one launch per forward
-        kern, kern_ms = "layer", stage[4]
+    if single_launch:
+        # the step is this one launch: its duration is the timed step (the
+        # events of the profiling graph would add a launch gap to it)
+        kern, kern_ms, ksrc = "layer", ms_per_step, "timed step (one launch per step)"
     else:
         kern = "gate_up" if stage[1] >= stage[2] else "down"
-        kern_ms = stage[1] if kern == "gate_up" else stage[2]
+        kern_ms = min(stage[1] if kern == "gate_up" else stage[2], ms_per_step)
+        ksrc = "CUDA events around the kernel in a profiling replay of the same forwards"
     tensor_path = T >= args.gemm_min_tokens and shape.hidden % 64 == 0 and shape.intermediate % 64 == 0
-    traffic = kernel_traffic(args.workload, kern, tensor_path)
+    traffic = kernel_traffic(workload, kern, tensor_path)
     if tensor_path:
         achieved = f[kern] / (kern_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
         roofline = {"bound": "tensor", "kernel": f"k_gemm ({kern.replace('_', '/')})", "achieved": achieved,
                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                    "peak_source": peaks["source"] + " bf16 dense (fp16 runs at the bf16 rate)",
+                    "peak_source": peaks["source"] + " bf16 dense burst (fp16 runs at the bf16 rate)",
                     "traffic": traffic, "algorithmic_flops_per_launch": f[kern],
-                    "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms, "active_experts": eu}
+                    "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms, "kernel_time": ksrc,
+                    "active_experts": eu}
     else:
         achieved = b[kern] / (kern_ms / 1e3) / 1e9
         kname = "k_decode (whole layer, one launch)" if single_launch else f"k_gemv ({kern.replace('_', '/')})"
         roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                     "peak_source": peaks["source"], "traffic": traffic,
-                    "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms,
+                    "algorithmic_bytes_per_launch": b[kern], "avg_launch_ms": kern_ms, "kernel_time": ksrc,
                     "active_experts": eu}
     layer_bytes_gbs = b["layer"] / (ms_per_step / 1e3) / 1e9
     layer_tflops = f["layer"] / (ms_per_step / 1e3) / 1e12
@@ -389,52 +473,123 @@ def run_ours(args):
                   "roofline_ms": max(b["layer"] / (peaks["hbm_gbs"] * 1e9), f["layer"] / (peaks["bf16_tflops"] * 1e12)) * 1e3}
     layer_roof["frac_of_roofline"] = layer_roof["roofline_ms"] / ms_per_step
 
+    # parity of the bench's own first batch against the oracle's result
+    parity = None
+    if ref is not None:
+        ids_t = torch.empty((T, shape.top_k), dtype=torch.int32, device=dev)
+        w_t = torch.empty((T, shape.top_k), dtype=torch.float32, device=dev)
+        o_t = torch.empty_like(xs[0])
+        layers[0].forward(xs[0], out=o_t, ids=ids_t, w=w_t)
+        layers[0].sync()
+        parity = parity_record(shape, ref, ids_t.cpu().numpy().astype(np.int64), o_t.float().cpu().numpy())
+
+    res = {"ms_per_step": ms_per_step, "value": value, "roofline": roofline, "layer_roofline": layer_roof,
+           "stage_ms": ({"layer (single launch, profiling replay)": stage[4], "total": stage[4]} if single_launch
+                        else {"route": stage[0], "gate_up": stage[1], "down": stage[2], "combine": stage[3],
+                              "total": stage[4]}),
+           "clocks": clocks, "parity": parity,
+           "gpu_launches": K * (1 if single_launch else launches_per_forward),
+           "l2": f"inputs larger than L2: steps rotate over {R} device copies of the "
+                 f"{lay.records.nbytes / 1e6:.1f} MB expert table and {R} token batches"}
+    res["_layers"] = layers
+    res["_xs"] = xs
+    return res
+
+
+def run_ours(args):
+    import torch
+
+    from w4a16_routed_expert_gb300 import build as B
+    from w4a16_routed_expert_gb300 import capi
+
+    world, rank, local = _dist()
+    shape, T, seed, desc = WORKLOADS[args.workload]
+    lay = synth.make_layer(shape, seed=seed)
+    l2_guess = 126 * 2**20
+    R = _rotation(shape, T, lay, l2_guess)
+    xs_np = _bench_tokens(shape, T, rank, R)
+    with_prefill = args.workload == DEFAULT_WORKLOAD and not args.no_prefill
+    pshape, pT, pseed, pdesc = WORKLOADS[PREFILL_WORKLOAD]
+    pxs_np = _bench_tokens(pshape, pT, rank, _rotation(pshape, pT, lay, l2_guess)) if with_prefill else None
+
+    cpu_base, ref, pref = None, None, None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_base, ref = cpu_leg(args, lay, shape, T, seed, xs_np[0])
+        if with_prefill:
+            _, pref = cpu_leg(args, lay, pshape, pT, pseed, pxs_np[0], time_it=False)
+
+    if not os.path.exists(capi.LIB_PATH):
+        B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    K, W = args.steps, args.warmup
+    main = measure(args, args.workload, K, W, lay, xs_np, ref, l2_guess)
+    layers, xs = main.pop("_layers"), main.pop("_xs")
+
     # end to end through the C ABI with host buffers (pinned), copies inside
+    R = len(xs)
     xh = [x.cpu().pin_memory() for x in xs]
-    oh = [torch.empty_like(x) .pin_memory() for x in xh]
+    oh = [torch.empty_like(x).pin_memory() for x in xh]
     ih = [torch.empty((T, shape.top_k), dtype=torch.int32).pin_memory() for _ in xs]
     wh = [torch.empty((T, shape.top_k), dtype=torch.float32).pin_memory() for _ in xs]
     for i in range(R):
         layers[i].forward_host(xh[i], oh[i], ih[i], wh[i])
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
     torch.cuda.synchronize()
     e0.record()
     for i in range(K):
         layers[i % R].forward_host(xh[i % R], oh[i % R], ih[i % R], wh[i % R])
     e1.record()
     torch.cuda.synchronize()
-    barrier()
+    if world > 1:
+        dist.barrier()
     e2e_ms = _max_over_ranks(torch, dev, world, e0.elapsed_time(e1))
     e2e = {"value": replica_throughput(T, world, e2e_ms / K), "unit": "tokens/s",
            "h2d_bytes_per_step": T * shape.hidden * 2,
            "d2h_bytes_per_step": T * shape.hidden * 2 + T * shape.top_k * 8,
            "path": "moe_layer_forward_host (pinned host x -> device, forward, out/ids/weights -> host)"}
-
     for l in layers:
         l.close()
+    del layers, xs
+    torch.cuda.empty_cache()
+
+    prefill = None
+    if with_prefill:
+        pK = max(20, min(K, 200))
+        pm = measure(args, PREFILL_WORKLOAD, pK, W, lay, pxs_np, pref, l2_guess)
+        for l in pm.pop("_layers"):
+            l.close()
+        pm.pop("_xs")
+        prefill = dict({"workload": PREFILL_WORKLOAD, "description": pdesc, "tokens_per_step": pT,
+                        "steps": pK, "warmup": W, "unit": "tokens/s"}, **pm)
+
     if rank != 0:
         return None
-    return {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+    res = {
+        "metric": METRIC, "value": main["value"], "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": main["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded; INT4 codes quantised from N(0,0.02) weights)",
         "config": {"workload": args.workload, "description": desc, "hidden": shape.hidden,
                    "intermediate": shape.intermediate, "experts": shape.num_experts, "top_k": shape.top_k,
                    "shared_expert": shape.has_shared, "group_size": shape.group_size,
                    "renormalize": shape.renormalize, "tokens_per_step": T, "global_batch": T * world,
                    "arithmetic": "INT4 codes (zero point 8) x FP16 scales x FP16 activations, FP32 accumulation",
-                   "l2": f"inputs larger than L2: steps rotate over {R} device copies of the "
-                         f"{lay.records.nbytes / 1e6:.1f} MB expert table and {R} token batches",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": roofline, "layer_roofline": layer_roof,
-        "stage_ms": ({"layer (single launch)": stage[4], "total": stage[4]} if single_launch else
-                     {"route": stage[0], "gate_up": stage[1], "down": stage[2], "combine": stage[3],
-                      "total": stage[4]}),
-        "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": K * (1 if single_launch else launches_per_forward),
+                   "l2": main["l2"], "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": main["roofline"], "layer_roofline": main["layer_roofline"], "stage_ms": main["stage_ms"],
+        "parity": main["parity"], "cpu_baseline": cpu_base, "e2e": e2e, "clocks": main["clocks"],
+        "gpu_launches": main["gpu_launches"],
     }
+    if prefill is not None:
+        res["prefill"] = prefill
+    return res
 
 
 def _mk_layer(MoELayer, torch, dev, lay, max_tokens, add_residual=False, partial_slots=None):
@@ -787,7 +942,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "description": desc, "tokens_per_step": T},
-        "cpu_baseline": {"kind": "oracle", "cores": 1, "value": value, "unit": "tokens/s",
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "host_cores": os.cpu_count(), "value": value, "unit": "tokens/s",
                          "sample": descs[0] + (f" of one layer, scaled to the {STACK_LAYERS}-layer stack"
                                                if layers_per_step > 1 else "")},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -803,11 +958,17 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the 8192-token prefill block of the default decode run")
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--gemm-min-tokens", type=int, default=48,
                     help="batch size from which the library takes the tensor-core path (its default)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.cpu_worker:
+        cpu_worker(args)
+        return
     if args.impl == "reference":
         res = run_reference(args)
     elif args.workload.startswith("olmoe-stack"):

@@ -39,6 +39,9 @@
  *  - Every call returns a moe_status_t; nothing aborts and no C++ exception
  *    crosses the ABI. moe_layer_last_error() describes the last failure of
  *    the calling thread.
+ *  - The pages publish no interface (Horizon RunMap report, "Scope of the
+ *    published results": the runtime source stays private). Each entry point
+ *    below cites the passage that defines the operation it performs.
  *  - Device pointers passed in are borrowed: the caller owns them and they
  *    must stay valid until moe_layer_destroy.
  *  - moe_layer_forward is asynchronous on the given CUDA stream (NULL = the
@@ -62,7 +65,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 typedef enum {
   MOE_OK = 0,
@@ -140,14 +143,21 @@ size_t moe_record_bytes(int32_t hidden, int32_t intermediate, int32_t group_size
 moe_status_t moe_record_section(int32_t hidden, int32_t intermediate, int32_t group_size,
                                 int32_t section, size_t* offset, size_t* bytes);
 
-/* Validates the configuration, records the borrowed pointers and allocates
+/* Horizon RunMap report, "The complete execution path", step 1 (the routed
+ * experts loaded once as compact INT4 + FP16-scale tensors into the pool the
+ * kernels read) and F51 Nitro-MoE, "Layer 1 - expert persistence cache" (a
+ * fixed pool of slots addressed through expert_to_slot).
+ * Validates the configuration, records the borrowed pointers and allocates
  * the workspace for max_tokens tokens on the current CUDA device. Fails with
  * INVALID_ARG / UNSUPPORTED / OOM / CAPACITY; *out is NULL on failure. No
  * allocation happens in moe_layer_forward afterwards. */
 moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_weights_t* weights,
                               moe_layer_t** out);
 
-/* One forward of T tokens on `stream` (a cudaStream_t, NULL = default).
+/* Horizon RunMap report, "The complete execution path", steps 2-3 (routing
+ * selects each token's experts, the custom kernels run them on FP16
+ * activations) and moe-stream, "Method" (top-8 of 64 experts per token).
+ * One forward of T tokens on `stream` (a cudaStream_t, NULL = default).
  *   x        device FP16 [T][H], read only
  *   out      device FP16 [T][H]; must not overlap x
  *   topk_ids device int32 [T][k] or NULL; rank order
@@ -214,7 +224,9 @@ moe_status_t moe_layer_get_gemm_stats(moe_layer_t* layer, uint64_t* values, int3
 /* Copies the handle's counters into *stats. */
 moe_status_t moe_layer_get_stats(const moe_layer_t* layer, moe_layer_stats_t* stats);
 
-/* Frees the workspace (and, in PARTIAL mode, the pool and the host
+/* Horizon RunMap report, "Partial-residency contract": the pool and its
+ * host registration end with the handle.
+ * Frees the workspace (and, in PARTIAL mode, the pool and the host
  * registration). NULL is accepted and returns MOE_OK. Call after the last
  * forward has completed. */
 moe_status_t moe_layer_destroy(moe_layer_t* layer);
@@ -233,8 +245,10 @@ moe_status_t moe_layer_destroy(moe_layer_t* layer);
  * Limits: 0 <= T <= 16, 1 <= E <= 1024, 1 <= k <= min(32, E), H a multiple
  * of 32 in 128..4096; anything else returns MOE_ERR_INVALID_ARG with a
  * message. The first call on a device (with that device current) looks up
- * the scratch array's address and caches it: make that first call before any
- * stream capture. All calls share the array and it keeps the last call's
+ * the scratch array's address and caches it with the id of the device's
+ * current context: make that first call before any stream capture. After a
+ * device reset the context id changes and the next call looks the address
+ * up again. All calls share the array and it keeps the last call's
  * contents; calls that overlap on the GPU race. Asynchronous on `stream`;
  * results are valid once it is synchronised. Calls no allocating routine. */
 moe_status_t moe_route_topk_static(const void* x, int32_t T, int32_t H, const float* router_w,
@@ -242,8 +256,10 @@ moe_status_t moe_route_topk_static(const void* x, int32_t T, int32_t H, const fl
                                    int32_t* topk_ids, float* topk_w, void* stream);
 
 /* Message of the calling thread's last failed call ("" if none). The pointer
- * stays valid until the thread's next call into the library. */
-const char* moe_layer_last_error(void);
+ * stays valid until the thread's next call into the library. `layer` may be
+ * NULL: the message is kept per thread, not per handle, because a create
+ * that fails has no handle to attach it to. */
+const char* moe_layer_last_error(const moe_layer_t* layer);
 
 #ifdef __cplusplus
 }

@@ -10,7 +10,8 @@ layer, each step written in the order the layer defines it:
 
 1. router logits ``L = x W_r^T (+ b)``                       -> router_logits
 2. softmax over all E experts                                -> softmax_rows
-3. top-k, ties to the lowest expert id, rank order            -> select_topk
+3. top-k, ties to the lowest expert id, rank order; NaN logits rank as -inf
+                                                              -> select_topk
 4. routing weights (softmax value, optionally renormalised)   -> routing_weights
 5. counting-sort permutation by expert                        -> counting_sort
 6. expert FFN ``y = W_d (silu(W_g x) * (W_u x))`` on dequantised INT4 weights
@@ -67,8 +68,8 @@ def unpack_codes(raw: np.ndarray, N: int, K: int) -> np.ndarray:
 
     Byte b of a row holds code k = 2b in its low four bits and k = 2b + 1 in
     its high four bits."""
-    raw = np.asarray(raw, dtype=np.uint8).reshape(N, K // 2).astype(np.int64)
-    q = np.empty((N, K), dtype=np.int64)
+    raw = np.asarray(raw, dtype=np.uint8).reshape(N, K // 2)
+    q = np.empty((N, K), dtype=np.uint8)
     q[:, 0::2] = raw % 16
     q[:, 1::2] = raw // 16
     return q
@@ -78,8 +79,10 @@ def dequantize(q: np.ndarray, scales: np.ndarray, G: int) -> np.ndarray:
     """w[n, k] = (q[n, k] - 8) * s[n, k // G] in float64."""
     N, K = q.shape
     s = np.asarray(scales, dtype=np.float16).astype(np.float64)
-    group_of_k = np.arange(K) // G
-    return (q.astype(np.float64) - 8.0) * s[:, group_of_k]
+    w = np.asarray(q).astype(np.float64) - 8.0
+    for gi in range(s.shape[1]):
+        w[:, gi * G:(gi + 1) * G] *= s[:, gi:gi + 1]
+    return w
 
 
 def expert_matrices(record: np.ndarray, H: int, I: int, G: int):
@@ -117,10 +120,21 @@ def softmax_rows(L: np.ndarray) -> np.ndarray:
     return z / z.sum(axis=1, keepdims=True)
 
 
+def selection_key(L: np.ndarray) -> np.ndarray:
+    """Key a logit is ranked by: the logit itself, with NaN ranked below
+    every number (as -inf). The pages say nothing about non-finite values;
+    this reading keeps the order (key descending, id ascending) total for
+    any input."""
+    L = np.asarray(L, dtype=np.float64)
+    return np.where(np.isnan(L), -np.inf, L)
+
+
 def select_topk(L: np.ndarray, k: int) -> np.ndarray:
-    """k rounds of selection: each round takes the largest remaining logit,
-    the lowest expert id among equal logits. Result in rank order."""
-    T, E = L.shape
+    """k rounds of selection: each round takes the largest remaining key
+    (selection_key), the lowest expert id among equal keys. Result in rank
+    order."""
+    K = selection_key(L)
+    T, E = K.shape
     ids = np.empty((T, k), dtype=np.int64)
     for t in range(T):
         taken = np.zeros(E, dtype=bool)
@@ -129,7 +143,7 @@ def select_topk(L: np.ndarray, k: int) -> np.ndarray:
             for e in range(E):
                 if taken[e]:
                     continue
-                if best < 0 or L[t, e] > L[t, best]:
+                if best < 0 or K[t, e] > K[t, best]:
                     best = e
             ids[t, j] = best
             taken[best] = True
@@ -137,17 +151,11 @@ def select_topk(L: np.ndarray, k: int) -> np.ndarray:
 
 
 def select_topk_fast(L: np.ndarray, k: int) -> np.ndarray:
-    """Same selection as select_topk, vectorised over tokens (np.argmax
-    returns the first, i.e. lowest, index among equal maxima)."""
-    work = np.array(L, dtype=np.float64, copy=True)
-    T = work.shape[0]
-    ids = np.empty((T, k), dtype=np.int64)
-    rows = np.arange(T)
-    for j in range(k):
-        best = np.argmax(work, axis=1)
-        ids[:, j] = best
-        work[rows, best] = -np.inf
-    return ids
+    """Same selection as select_topk, vectorised over tokens: a stable sort
+    of the negated keys keeps equal keys in ascending id order (every key is
+    a number or -inf, so the negation is exact)."""
+    order = np.argsort(-selection_key(L), axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
 
 
 def routing_weights(p: np.ndarray, ids: np.ndarray, renormalize: bool) -> np.ndarray:

@@ -16,3 +16,20 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return os.path.join(ROOT, "tests", "golden")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Near-tie tokens of every GPU parity comparison, reported separately
+    from the pass/fail result (their routing is checked against the oracle
+    recomputed with the GPU's ids instead)."""
+    mod = sys.modules.get("gpu_harness")
+    reps = getattr(mod, "REPORTS", None) if mod else None
+    if not reps:
+        return
+    tr = terminalreporter
+    tr.write_sep("-", "parity comparisons: near ties reported separately")
+    for r in reps:
+        tr.write_line(f"{r['test']}: tokens {r['tokens']}, rows compared {r['rows_compared']}, "
+                      f"near ties {r['near_ties']}, worst err/bound {r['worst_ratio']:.3f}")
+    tr.write_line(f"total near-tie tokens: {sum(r['near_ties'] for r in reps)} "
+                  f"over {sum(r['tokens'] for r in reps)} routed tokens")

@@ -20,6 +20,10 @@ from w4a16_routed_expert_gb300.layer import MoELayer
 TOL = 2e-3
 TIE_EPS = 1e-3
 _STREAM = None
+# one entry per compare() call of the session: test id, tokens compared,
+# near-tie tokens (reported separately; the routing check skips them), worst
+# error over its bound. Printed at the end of the run (tests/conftest.py).
+REPORTS = []
 
 
 def stream():
@@ -104,4 +108,8 @@ def compare(lay: synth.Layer, x_np: np.ndarray, g: dict, tokens=None, tol: float
     worst = float((err / bound).max()) if err.size else 0.0
     assert np.isfinite(got).all(), "non-finite outputs"
     assert (err <= bound).all(), f"max err/bound {worst:.3f}, max abs err {err.max():.3e}"
-    return dict(near_ties=len(near), worst_ratio=worst, max_abs_err=float(err.max()) if err.size else 0.0)
+    rep = dict(tokens=int(T), rows_compared=int(len(toks)), near_ties=len(near), worst_ratio=worst,
+               max_abs_err=float(err.max()) if err.size else 0.0)
+    import os
+    REPORTS.append(dict(test=os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], **rep))
+    return rep

@@ -59,3 +59,35 @@ def test_multi_kernel_launch_count(T, gmin, expect):
 def test_replica_throughput():
     assert bench.replica_throughput(1, 1, 0.025) == pytest.approx(40_000.0)
     assert bench.replica_throughput(16, 4, 0.1) == pytest.approx(640_000.0)
+
+
+def test_parity_record_flags_planted_errors():
+    """The bench's parity record against hand-made GPU results: exact ids
+    and outputs within the bound pass; a wrong id on a decided token, or an
+    output off by more than the bound, fails; near-tie tokens are counted and
+    not compared."""
+    import numpy as np
+    shape = synth.OLMOE
+    ids = np.tile(np.arange(8), (4, 1))
+    out = np.ones((4, 16))
+    ref = dict(ids=ids.copy(), out=out.copy(), rows=np.arange(4), near=np.array([2]))
+    ok = bench.parity_record(shape, ref, ids.copy(), out + 1e-3)
+    assert ok["pass"] and ok["near_ties"] == 1 and ok["rows_compared"] == 3
+    assert ok["max_err_over_bound"] == pytest.approx(0.5)
+    bad_ids = ids.copy()
+    bad_ids[1, 0] = 9
+    assert not bench.parity_record(shape, ref, bad_ids, out)["pass"]
+    near_ids = ids.copy()
+    near_ids[2, 0] = 9  # token 2 is a near tie: not compared
+    assert bench.parity_record(shape, ref, near_ids, out)["pass"]
+    bad_out = out.copy()
+    bad_out[3, 5] += 3e-3
+    assert not bench.parity_record(shape, ref, ids, bad_out)["pass"]
+
+
+def test_parity_rows_cover_small_batches_and_sample_large_ones():
+    import numpy as np
+    assert bench._parity_rows(1).tolist() == [0]
+    assert bench._parity_rows(64).tolist() == list(range(64))
+    r = bench._parity_rows(8192)
+    assert len(r) == 64 and r[0] == 0 and r[-1] == 8191 and (np.diff(r) > 0).all()

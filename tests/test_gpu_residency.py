@@ -85,3 +85,25 @@ def test_capacity_shortfall_fails_at_create():
     with pytest.raises(capi.MoEError) as ei:
         _partial(lay, 3, 4)
     assert ei.value.status == capi.MOE_ERR_CAPACITY
+
+
+def test_partial_residency_full_size_every_row():
+    """The 2880-wide layer at its full size (128 experts, top-4 renormalised,
+    32 resident slots filled from host backing of all 128 experts), 256
+    tokens: every demanded expert is copied in over several waves. Every
+    output row and the whole routing against the oracle."""
+    shape = synth.GPTOSS_LIKE
+    T = 256
+    lay = synth.make_layer(shape, seed=4)
+    x = synth.make_tokens(shape.hidden, T, seed=4)
+    ml, host = _partial(lay, 32, T)
+    g = GH.run(ml, x)
+    st = ml.stats()
+    ml.close()
+    rep = GH.compare(lay, x, g)
+    assert rep["rows_compared"] == T
+    demanded = int((g["counts"] > 0).sum())
+    assert st.expert_hits + st.expert_misses == demanded
+    assert st.waves >= -(-demanded // 32)
+    assert st.h2d_bytes == st.expert_misses * lay.records.shape[1]
+    assert st.d2h_expert_bytes == 0

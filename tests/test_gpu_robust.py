@@ -1,8 +1,10 @@
 """Non-finite inputs: a token whose hidden state holds NaN or Inf still gets a
 well-defined selection (NaN logits rank below every number, ties to the
 lower id), so every CTA that routes it agrees and the launch completes
-without a device-side wait giving up. Finite tokens of the same batch are
-unaffected (checked against the oracle)."""
+without a device-side wait giving up. The selection of the poisoned tokens
+is checked against the oracle's selection under the same reading; their
+outputs are non-finite and outside parity. Finite tokens of the same batch
+are unaffected."""
 import time
 
 import numpy as np
@@ -12,6 +14,7 @@ torch = pytest.importorskip("torch")
 
 pytestmark = pytest.mark.gpu
 
+from oracle import moe_oracle as O  # noqa: E402
 from w4a16_routed_expert_gb300 import capi, synth  # noqa: E402
 
 import gpu_harness as GH  # noqa: E402
@@ -42,6 +45,28 @@ def _poison(x, rows, kind):
     return x
 
 
+def _check_poisoned_selection(lay, xp, bad, ids):
+    """The poisoned tokens' ids against the oracle's selection (NaN ranked as
+    -inf, equal keys to the lower id) on its FP64 logits. Equal infinite keys
+    are exact ties on both sides; finite keys whose gap at ranks 0..k is
+    within the FP32 rounding of the logits (1e-5 of the largest |x_h w_eh|
+    sum, at least 1e-3) are near ties and skipped."""
+    k = lay.shape.top_k
+    with np.errstate(all="ignore"):
+        L = O.router_logits(xp[bad], lay.router_w)
+        mag = np.abs(xp[bad].astype(np.float64)) @ np.abs(lay.router_w.astype(np.float64)).T
+        keys = O.selection_key(L)
+        srt = -np.sort(-keys, axis=1)[:, :k + 1]
+        gaps = srt[:, :-1] - srt[:, 1:]
+    ref = O.select_topk(L, k)
+    for i, t in enumerate(bad):
+        m = mag[i][np.isfinite(mag[i])]
+        eps = max(1e-3, 1e-5 * (m.max() if m.size else 0.0))
+        if np.any(np.isfinite(gaps[i]) & (gaps[i] <= eps)):
+            continue
+        assert ids[t].tolist() == ref[i].tolist(), (t, ids[t].tolist(), ref[i].tolist())
+
+
 @pytest.mark.parametrize("T", [1, 4, 16, 40])
 @pytest.mark.parametrize("kind", ["nan", "inf", "huge"])
 def test_non_finite_tokens_complete_and_route_validly(olmoe_layer, T, kind, monkeypatch):
@@ -60,6 +85,7 @@ def test_non_finite_tokens_complete_and_route_validly(olmoe_layer, T, kind, monk
         for t in range(T):
             assert len(set(ids[t].tolist())) == shape.top_k, f"token {t}: repeated expert"
         assert int(g["counts"].sum()) == T * shape.top_k
+        _check_poisoned_selection(olmoe_layer, xp, bad, g["ids"])
     ml.close()
     good = [t for t in range(T) if t not in bad]
     if good:

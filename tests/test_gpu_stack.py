@@ -1,7 +1,8 @@
 """Stacked layers with a residual stream (16 OLMoE-shaped layers):
 x_{l+1} = fp16(x_l + fp16(layer_l(x_l))), next step's input = last output +
-N(0, 0.1). Checked teacher-forced: every checked layer against the oracle fed
-the GPU's own input to that layer."""
+N(0, 0.1) (the literal recipe, finite over the steps run here). Checked
+teacher-forced: every layer and every token against the oracle fed the GPU's
+own input to that layer."""
 import numpy as np
 import pytest
 
@@ -29,7 +30,7 @@ def stack_layers():
     return [synth.make_layer(synth.OLMOE, seed=synth.stack_layer_seed(2, l)) for l in range(LAYERS)]
 
 
-@pytest.mark.parametrize("T,steps,checked", [(1, 2, range(LAYERS)), (64, 1, (0, 15))])
+@pytest.mark.parametrize("T,steps,checked", [(1, 2, range(LAYERS)), (64, 1, range(LAYERS))])
 def test_stack_teacher_forced(stack_layers, T, steps, checked):
     shape = synth.OLMOE
     mls = [GH.upload(lay, max_tokens=T, add_residual=True) for lay in stack_layers]
@@ -42,9 +43,8 @@ def test_stack_teacher_forced(stack_layers, T, steps, checked):
             xout = g["out"].astype(np.float16)
             if l in checked:
                 lay = stack_layers[l]
-                sample = None if T <= 16 else [0, 1, T // 2, T - 1]
-                ref = O.moe_forward(xin, lay.router_w, None, lay.records, lay.expert_to_slot, tokens=sample, **kw)
-                toks = np.arange(T) if sample is None else np.array(sample)
+                ref = O.moe_forward(xin, lay.router_w, None, lay.records, lay.expert_to_slot, **kw)
+                toks = np.arange(T)
                 near = set(O.near_tie_tokens(ref["logits"], shape.top_k).tolist())
                 for i, t in enumerate(toks):
                     if int(t) in near:

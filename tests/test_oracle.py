@@ -158,6 +158,25 @@ def test_topk_against_full_sort_with_ties():
         assert np.array_equal(O.select_topk_fast(L, k), ref)
 
 
+def test_topk_non_finite_logits_hand_worked():
+    # NaN ranks below every number (as -inf); equal keys go to the lower id.
+    # Row 0 keys: [-inf, 1, -inf, 1, -inf, 3] -> 5, then 1 and 3 (tie, lower
+    # id first), then the lowest id among the -inf keys, 0.
+    # Row 1: every logit NaN -> all keys equal -> ids 0, 1, 2, 3.
+    # Row 2: +inf beats every number; -inf and NaN tie below them.
+    nan, inf = np.nan, np.inf
+    L = np.array([[nan, 1.0, nan, 1.0, -inf, 3.0],
+                  [nan, nan, nan, nan, nan, nan],
+                  [-inf, nan, inf, 0.5, inf, -2.0]])
+    expect = [[5, 1, 3, 0], [0, 1, 2, 3], [2, 4, 3, 5]]
+    assert O.select_topk(L, 4).tolist() == expect
+    assert O.select_topk_fast(L, 4).tolist() == expect
+    # the fast path must not re-take an entry when every remaining key is -inf
+    L2 = np.array([[-inf, -inf, 7.0, -inf]])
+    assert O.select_topk_fast(L2, 4).tolist() == [[2, 0, 1, 3]]
+    assert O.select_topk(L2, 4).tolist() == [[2, 0, 1, 3]]
+
+
 def test_softmax_and_silu_against_library():
     rng = np.random.default_rng(1)
     L = rng.normal(0, 3, size=(20, 33))

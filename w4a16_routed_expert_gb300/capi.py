@@ -79,7 +79,7 @@ PROTOTYPES = {
     "moe_layer_get_gemm_stats": (_I32, [_P, ctypes.POINTER(ctypes.c_uint64), _I32, ctypes.POINTER(_I32)]),
     "moe_layer_get_profile": (_I32, [_P, ctypes.POINTER(moe_layer_profile_t)]),
     "moe_layer_destroy": (_I32, [_P]),
-    "moe_layer_last_error": (ctypes.c_char_p, []),
+    "moe_layer_last_error": (ctypes.c_char_p, [ctypes.c_void_p]),
     "moe_route_topk_static": (_I32, [_P, _I32, _I32, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
     # include/moe_residency.h
     "moe_slot_planner_create": (_P, [_I32, _I32]),
@@ -149,7 +149,7 @@ def lib() -> ctypes.CDLL:
 
 
 def last_error() -> str:
-    return lib().moe_layer_last_error().decode()
+    return lib().moe_layer_last_error(None).decode()
 
 
 def check(status: int, where: str) -> None:

@@ -9,7 +9,8 @@
 #include <mutex>
 #include <new>
 #include <string>
-#include <unordered_map>
+#include <map>
+#include <utility>
 
 #include "layer_internal.h"
 #include "residency.h"
@@ -134,7 +135,10 @@ moe_status_t moe_record_section(int32_t hidden, int32_t intermediate, int32_t gr
   return MOE_OK;
 }
 
-const char* moe_layer_last_error(void) { return g_last_error.c_str(); }
+const char* moe_layer_last_error(const moe_layer_t* layer) {
+  (void)layer;
+  return g_last_error.c_str();
+}
 
 moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_weights_t* weights,
                               moe_layer_t** out) {
@@ -779,17 +783,24 @@ moe_status_t moe_layer_get_stats(const moe_layer_t* layer, moe_layer_stats_t* st
 namespace moe {
 
 cudaError_t ensure_smem_ptr(const void* kern, size_t bytes) {
+  // The attribute applies to the device current when it is set, so the
+  // record is kept per (device, kernel): a process that uses several GPUs
+  // opts every one of them in.
   static std::mutex mu;
-  static std::unordered_map<const void*, size_t> set_bytes;
+  static std::map<std::pair<int, const void*>, size_t> set_bytes;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  auto it = set_bytes.find(kern);
+  const auto key = std::make_pair(dev, kern);
+  auto it = set_bytes.find(key);
   if (it != set_bytes.end() && it->second >= bytes) return cudaSuccess;
   if (bytes <= 48 * 1024 && it == set_bytes.end()) {
-    set_bytes[kern] = 48 * 1024;
+    set_bytes[key] = 48 * 1024;
     return cudaSuccess;
   }
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) set_bytes[kern] = bytes;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) set_bytes[key] = bytes;
   return e;
 }
 

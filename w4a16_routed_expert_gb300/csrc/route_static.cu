@@ -13,8 +13,11 @@
 // All calls on a device share it and it keeps the last call's contents: calls
 // that overlap on the GPU (different streams, or threads without ordering)
 // race on it. Set-up: the first call on a device, with that device current,
-// looks up the array's device address (cudaGetSymbolAddress) and caches it;
-// make that first call before any stream capture.
+// looks up the array's device address (cudaGetSymbolAddress) and caches it
+// together with the unique id of the device's current context; make that
+// first call before any stream capture. A device reset (cudaDeviceReset)
+// ends the context and the array may come back at another address: a call
+// that finds a different context id looks the address up again.
 #include <mutex>
 
 #include "layer_internal.h"
@@ -34,6 +37,34 @@ static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchByt
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
+
+// Unique id of the calling thread's current context (0 if unavailable), via
+// the driver entry points (no link-time dependence on the driver library).
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    looked_up = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+    cudaGetLastError();
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS) return id;
+  return 0;
+}
 
 moe_status_t fail_static(moe_status_t st, const char* msg) { return set_error(st, "%s", msg); }
 
@@ -79,7 +110,8 @@ extern "C" moe_status_t moe_route_topk_static(const void* x, int32_t T, int32_t 
   unsigned char* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_scratch_addr[dev] || ctx != g_scratch_ctx[dev]) {
       void* p = nullptr;
       e = cudaGetSymbolAddress(&p, g_route_scratch);
       if (e != cudaSuccess || !p) {
@@ -87,6 +119,8 @@ extern "C" moe_status_t moe_route_topk_static(const void* x, int32_t T, int32_t 
         return fail_static(MOE_ERR_CUDA, "moe_route_topk_static: cudaGetSymbolAddress of the scratch failed");
       }
       g_scratch_addr[dev] = p;
+      // the lookup made the device's primary context current if it was not
+      g_scratch_ctx[dev] = current_context_id();
     }
     base = static_cast<unsigned char*>(g_scratch_addr[dev]);
   }
