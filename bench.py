@@ -193,16 +193,22 @@ def algorithmic(shape, T, eu):
 # under profiles/ is reported only while these files are unchanged.
 KERNEL_SOURCES = {
     "decode": ["decode.cu", "tcgemv_dev.cuh", "route_dev.cuh", "common.cuh", "kernels.h"],
+    "decode1": ["decode1.cu", "tcgemv_dev.cuh", "route_dev.cuh", "common.cuh", "kernels.h"],
     "gemv": ["gemv.cu", "tcgemv_dev.cuh", "common.cuh", "kernels.h"],
     "gemm": ["gemm.cu", "tc.cuh", "common.cuh", "kernels.h"],
 }
 
 
-def kernel_traffic(workload, kern, tensor_path):
+def kernel_traffic(workload, kern, tensor_path, tokens=0):
     """dram__bytes_read.sum + dram__bytes_write.sum per launch of the
     dominant kernel, from one ncu capture recorded in profiles/traffic.json,
     or None when the kernel's sources changed since the capture."""
-    family = "gemm" if tensor_path else ("decode" if kern == "layer" else "gemv")
+    if tensor_path:
+        family = "gemm"
+    elif kern == "layer":
+        family = "decode1" if tokens == 1 else "decode"
+    else:
+        family = "gemv"
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as ftr:
             ent = json.load(ftr).get(workload, {}).get(kern)
@@ -447,7 +453,7 @@ def measure(args, workload, K, W, lay, xs_np, ref, l2):
         kern_ms = min(stage[1] if kern == "gate_up" else stage[2], ms_per_step)
         ksrc = "CUDA events around the kernel in a profiling replay of the same forwards"
     tensor_path = T >= args.gemm_min_tokens and shape.hidden % 64 == 0 and shape.intermediate % 64 == 0
-    traffic = kernel_traffic(workload, kern, tensor_path)
+    traffic = kernel_traffic(workload, kern, tensor_path, T)
     if tensor_path:
         achieved = f[kern] / (kern_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
@@ -459,7 +465,11 @@ def measure(args, workload, K, W, lay, xs_np, ref, l2):
                     "active_experts": eu}
     else:
         achieved = b[kern] / (kern_ms / 1e3) / 1e9
-        kname = "k_decode (whole layer, one launch)" if single_launch else f"k_gemv ({kern.replace('_', '/')})"
+        if single_launch:
+            kname = ("k_decode1 (batch-1 whole layer, one launch)" if T == 1
+                     else "k_decode (whole layer, one launch)")
+        else:
+            kname = f"k_gemv ({kern.replace('_', '/')})"
         roofline = {"bound": "hbm", "kernel": kname, "achieved": achieved,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                     "peak_source": peaks["source"], "traffic": traffic,
@@ -743,7 +753,8 @@ def run_stack(args):
     peaks = _peaks()
     b, f, _ = algorithmic(shape, T, eu)
     if single:
-        kern, kms, kname = "layer", st[4], "k_decode (whole layer, one launch)"
+        kern, kms = "layer", st[4]
+        kname = "k_decode1 (batch-1 whole layer, one launch)" if T == 1 else "k_decode (whole layer, one launch)"
     else:
         kern = "gate_up" if st[1] >= st[2] else "down"
         kms = st[1] if kern == "gate_up" else st[2]

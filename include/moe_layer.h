@@ -197,18 +197,25 @@ moe_status_t moe_layer_sync(moe_layer_t* layer, void* stream);
 moe_status_t moe_layer_set_profiling(moe_layer_t* layer, int32_t enable);
 moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* profile);
 
-/* Tracing of the single-launch decode path: when the handle was created
- * with the environment variable MOE_TRACE=1, every CTA of that kernel writes
- * 32 global-timer stamps (ns) per forward: 0 entry, 1 own logit partials
- * written, 2 all partials seen, 3 top-k done, 4 routing done, 5 first
- * gate/up item started, 6 last gate/up item done, 7 first down item started,
- * 8 consumers done, 9 finisher done, 10 all warps done, 11 exit, 12 first
- * down wait entered, 13 its counter seen, 14 its activations staged, 15
- * unused; then for the CTA's first 8 work items, item i's bytes landed
- * (16 + 2i) and item i computed (17 + 2i), as seen by consumer warp 0 (0 if
- * not reached). Synchronises the device and copies min(max_stamps,
- * 32 * CTAs) stamps, CTA-major, into host memory; *n_stamps receives the
- * count. */
+/* Tracing of the single-launch decode kernels: when the handle was created
+ * with the environment variable MOE_TRACE=1, every CTA of those kernels
+ * writes 32 global-timer stamps (ns) per forward (0 where not reached).
+ * Batch-1 kernel (one token): 0 entry, 1 past the dependency on the previous
+ * launch, 2 own logits published, 3 all logits seen, 4 per-group candidates
+ * ranked, 5 selection done, 6 gate/up copies issued, 7 routing weights done,
+ * 8 down copies issued, 9..12 gate/up tiles 0..3 landed, 13..16 tiles 0..3
+ * computed (consumer warp 0), 17 the CTA's h written, 18 every CTA's h
+ * seen, 19 / 21 down inputs staged by consumer warp 0 / the last consumer
+ * warp, 20 / 22 their down work done, 23 all down partials done, 24 output
+ * rows written, 25 exit. Small-batch kernel (2..16 tokens): 0 entry, 1 own
+ * logit partials written, 2 all partials seen, 3 top-k done, 4 routing
+ * done, 5 first gate/up item started, 6 last gate/up item done, 7 first down
+ * item started, 8 consumers done, 9 finisher done, 10 all warps done, 11
+ * exit, 12 first down wait entered, 13 its counter seen, 14 its activations
+ * staged; then for the CTA's first 8 work items, item i's bytes landed
+ * (16 + 2i) and item i computed (17 + 2i), as seen by consumer warp 0.
+ * Synchronises the device and copies min(max_stamps, 32 * CTAs) stamps,
+ * CTA-major, into host memory; *n_stamps receives the count. */
 moe_status_t moe_layer_get_trace(moe_layer_t* layer, uint64_t* stamps, int32_t max_stamps, int32_t* n_stamps);
 
 /* Wait counters of the tensor-core GEMM path: when the handle was created

@@ -257,6 +257,7 @@ def test_single_launch_decode_matches_multi_kernel_path(shape, seed, T, monkeypa
     experts with the same work items, so every output is bit-identical."""
     lay = synth.make_layer(shape, seed=seed)
     x = synth.make_tokens(shape.hidden, T, seed=seed)
+    monkeypatch.setenv("MOE_DECODE1", "0")  # batch 1 too: this compares the two kernels below
     monkeypatch.setenv("MOE_MEGAKERNEL_MAX_T", "16")  # the one-launch path for every T here
     mk = GH.upload(lay, max_tokens=T)
     a = GH.run(mk, x)
@@ -271,3 +272,46 @@ def test_single_launch_decode_matches_multi_kernel_path(shape, seed, T, monkeypa
         assert np.array_equal(a[key], b2[key]), key  # repeatable across launches (counters reset)
     for key in ("out", "ids", "w", "perm", "inv_perm", "counts", "offsets"):
         assert np.array_equal(a[key], b[key]), key
+
+
+BATCH1_CASES = [
+    ("olmoe", synth.OLMOE, 60, "quantized"),
+    ("many-experts", synth.MANY_EXPERTS, 61, "quantized"),
+    ("tiny-uniform", synth.TINY, 62, "uniform"),
+    ("shared-G64", synth.LayerShape(512, 384, 16, 3, 64, False, has_shared=True), 63, "uniform"),
+    ("k1-E1", synth.LayerShape(256, 256, 1, 1, 128, True), 64, "uniform"),
+    ("E1024-k32", synth.LayerShape(256, 128, 1024, 32, 64, True, router_std=0.2), 65, "uniform"),
+]
+
+
+@pytest.mark.parametrize("name,shape,seed,codes", BATCH1_CASES, ids=[c[0] for c in BATCH1_CASES])
+def test_batch1_kernel_matches_oracle_and_the_other_paths(name, shape, seed, codes, monkeypatch):
+    """One token takes the batch-1 kernel (every CTA's share of the bytes
+    requested at once, the combine local to each CTA): against the oracle,
+    repeatable bit for bit across launches, the same routing bits as the
+    single-launch small-batch kernel and the multi-kernel path (the logits
+    and the softmax use the same FP32 arithmetic), and outputs that agree
+    with theirs within the layer tolerance (the per-group partial sums are
+    added in another order)."""
+    lay = synth.make_layer(shape, seed=seed, codes=codes)
+    ml = GH.upload(lay, max_tokens=4)
+    for call in range(3):
+        x = synth.make_tokens(shape.hidden, 1, seed=seed * 10 + call)
+        a = GH.run(ml, x)
+        a2 = GH.run(ml, x)
+        GH.compare(lay, x, a)
+        for key in ("out", "ids", "w", "perm", "inv_perm", "counts", "offsets"):
+            assert np.array_equal(a[key], a2[key]), key
+        for env in ({"MOE_DECODE1": "0"}, {"MOE_DECODE1": "0", "MOE_MEGAKERNEL": "0"}):
+            for kv in env.items():
+                monkeypatch.setenv(*kv)
+            other = GH.upload(lay, max_tokens=4)
+            b = GH.run(other, x)
+            other.close()
+            for kv in env:
+                monkeypatch.delenv(kv)
+            for key in ("ids", "w", "perm", "inv_perm", "counts", "offsets"):
+                assert np.array_equal(a[key], b[key]), (env, key)
+            err = np.abs(a["out"] - b["out"])
+            assert (err <= GH.TOL * np.maximum(1, np.abs(b["out"]))).all(), (env, err.max())
+    ml.close()

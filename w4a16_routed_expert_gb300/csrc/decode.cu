@@ -52,40 +52,6 @@ struct DecodeHdr {
 };
 static_assert(sizeof(DecodeHdr) <= kHdrBytes, "decode header exceeds its reserved bytes");
 
-// Release-ordered increment (fire and forget): the caller's prior writes, and
-// those it has observed (e.g. through an mbarrier), are visible before it.
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t* p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Bounded spin until *p >= target. False on time-out (error recorded).
-__device__ __forceinline__ bool wait_count(const uint32_t* p, uint32_t target, volatile int* abort_flag,
-                                           uint32_t* err) {
-  if (ld_acquire(p) >= target) return true;
-  const long long t0 = clock64();
-  while (true) {
-    __nanosleep(64);
-    if (ld_acquire(p) >= target) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kSpinLimitCycles) {
-      record_error(err, MOE_DEV_ERR_TIMEOUT);
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
 // Weighted combine of down row block rbi by one warp (the signalling warp of
 // the CTA that completed it): out[t][row] = sum_j w[t][j] * y[(t, j)][row]
 // in rank order, then the shared expert, the FP16 rounding and the residual.

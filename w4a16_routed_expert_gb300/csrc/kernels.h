@@ -216,6 +216,41 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t s, bool pd
 // whether the decode launch may add programmatic stream serialisation to its
 // cooperative launch on this device (probed once, outside any capture)
 bool decode_pdl_supported();
+
+// Batch-1 whole-layer decode (T == 1, fully resident table): every CTA's
+// share of the selected experts' bytes fits its shared memory, so all of it
+// is requested at once. Work comes in units of 16 rows: gate/up units of
+// the (selected expert, intermediate row) space and down units of the output
+// rows. ctr[0] (logits published) and ctr[1] (gate/up done) are epoch
+// counters that every CTA increments exactly once per launch, wrapping at
+// ctr_mod (a multiple of the grid); they start at zero.
+struct Decode1Args {
+  RouteArgs r;                  // T == 1; logits [E]; routing outputs published by CTA 0
+  const uint8_t* pool;          // slot pool base
+  long long record_bytes;
+  const int32_t* expert_to_slot;
+  int num_slots;
+  long long off_q[3];           // code sections: gate, up, down
+  long long off_s[3];           // scale sections: gate, up, down
+  int I;                        // intermediate
+  int G;                        // group size
+  __half* h;                    // [nseg][I] SwiGLU activations, by sorted position
+  __half* out;                  // [H]
+  const __half* x_res;          // residual input or nullptr
+  uint32_t* ctr;
+  uint32_t ctr_mod;
+  unsigned long long* trace;    // nullable: [gridDim][kTraceStamps]
+  int nseg_max;                 // k + has_shared
+  int max_units_g;              // most gate/up tiles of a CTA (decode1_max_tiles)
+  int max_units_d;              // ceil(H / 16 / grid)
+  int max_rows_rt;              // router rows per CTA: ceil(E / grid)
+};
+// Most gate/up tiles (16 rows, 8 at an expert's end) any CTA of the grid
+// gets when nseg experts' I rows are split in 8-row granules.
+int decode1_max_tiles(int nseg, int I, int grid);
+// Dynamic shared memory of k_decode1 for these arguments (0: does not fit).
+size_t decode1_smem_bytes(const Decode1Args& a);
+cudaError_t launch_decode1(const Decode1Args& a, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_gemm(bool dual, const CUtensorMap& codes0, const CUtensorMap& codes1, const CUtensorMap& act,
                         const GemmArgs& a, int grid, cudaStream_t s, bool pdl);
 size_t gemm_smem_bytes(bool dual);

@@ -76,12 +76,14 @@ struct moe_layer {
   int32_t* ids_stage = nullptr;
   float* w_stage = nullptr;
   int last_T = 0;
+  bool decode1 = true;           // batch-1 decode kernel (full residency, T == 1)
   bool megakernel = true;        // single-launch decode (full residency)
   int megakernel_max_tokens = 4;  // largest T it takes (<= 16); measured faster than the multi-kernel path up to 4
   bool last_single = false;      // the last profiled forward was one launch
   unsigned long long* trace = nullptr;  // per-CTA phase stamps of the single-launch decode (MOE_TRACE=1)
   unsigned long long* gemm_stats = nullptr;  // GEMM wait counters (MOE_GEMM_STATS=1): [2][CTAs][kGemmStats]
   uint32_t* ctr = nullptr;       // megakernel counters (zero between launches)
+  uint32_t* ctr1 = nullptr;      // batch-1 decode epoch counters (zero at create)
   // prefill (tensor-core) path
   int gemm_min_tokens = 48;  // tensor-core GEMM from this T (below it the grouped GEMV is faster)
   bool gemm_ok = false;         // shapes suit the GEMM (H, I multiples of 64)
@@ -115,6 +117,10 @@ bool encode_pool_maps(const moe_layer* L, const uint8_t* pool, int num_slots, Co
 // Single-launch decode; MOE_ERR_UNSUPPORTED when no variant fits the shapes.
 moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, int32_t* ids_user, float* w_user,
                             cudaStream_t s);
+// Batch-1 decode (T == 1); MOE_ERR_UNSUPPORTED when a CTA's share does not
+// fit its shared memory.
+moe_status_t enqueue_decode1(moe_layer* L, const __half* x, __half* out, int32_t* ids_user, float* w_user,
+                             cudaStream_t s);
 // Enqueue the weighted combine of the expert outputs into out.
 moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s);
 // Record the calling thread's error message; returns st.

@@ -108,6 +108,7 @@ size_t workspace_bytes(const moe_layer_config_t& c) {
   b += 2 * align256(T * H * 2);         // x/out staging
   b += align256(T * k * 4) * 2;         // ids/w staging
   b += align256(2048 * 4);              // megakernel counters
+  b += align256(64 * 4);                // batch-1 decode epoch counters
   b += align256(1024 * moe::kTraceStamps * 8);  // phase trace (up to 1024 CTAs)
   b += align256(2 * 1024 * moe::kGemmStats * 8);  // GEMM wait counters (two launches)
   return b;
@@ -154,6 +155,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
   L->n_records = config->num_experts + config->has_shared_expert;
   const char* pdl_env = getenv("MOE_PDL");
   L->pdl = !(pdl_env && pdl_env[0] == '0');
+  const char* d1_env = getenv("MOE_DECODE1");
+  L->decode1 = !(d1_env && d1_env[0] == '0');
   const char* mk_env = getenv("MOE_MEGAKERNEL");
   L->megakernel = !(mk_env && mk_env[0] == '0');
   if (const char* mt = getenv("MOE_MEGAKERNEL_MAX_T"))
@@ -204,6 +207,7 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     L->ids_stage = carve<int32_t>(p, T * k);
     L->w_stage = carve<float>(p, T * k);
     L->ctr = carve<uint32_t>(p, 2048);
+    L->ctr1 = carve<uint32_t>(p, 64);
     unsigned long long* tr = carve<unsigned long long>(p, 1024 * moe::kTraceStamps);
     const char* tr_env = getenv("MOE_TRACE");
     if (tr_env && tr_env[0] == '1') L->trace = tr;
@@ -214,6 +218,7 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
   // zero the small control words (ticket, error word, segment count)
   e = cudaMemset(L->num_seg, 0, 4 * 256);
   if (e == cudaSuccess) e = cudaMemset(L->ctr, 0, 2048 * 4);
+  if (e == cudaSuccess) e = cudaMemset(L->ctr1, 0, 64 * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(L->ws);
@@ -235,8 +240,10 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     if (const char* ib = getenv("MOE_GEMV_ITEM_BYTES")) item_bytes = std::max(4096, std::min(131072, atoi(ib)));
     L->dec_pg = moe::plan_tcgemv(I, H, config->group_size, true, item_bytes);
     L->dec_pd = moe::plan_tcgemv(H, I, config->group_size, false, item_bytes);
-    if (config->residency == MOE_RESIDENCY_FULL)
-      moe::encode_pool_maps(L, static_cast<const uint8_t*>(weights->slot_pool), config->num_slots, &L->pool_maps);
+    if (config->residency == MOE_RESIDENCY_FULL) {
+      const uint8_t* pool = static_cast<const uint8_t*>(weights->slot_pool);
+      moe::encode_pool_maps(L, pool, config->num_slots, &L->pool_maps);
+    }
   }
   if (config->residency == MOE_RESIDENCY_PARTIAL) {
     st = moe::residency_create(L->cfg, L->lay.record, L->n_records, weights->host_backing, &L->res);
@@ -549,6 +556,67 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   return MOE_OK;
 }
 
+moe_status_t enqueue_decode1(moe_layer* L, const __half* x, __half* out, int32_t* ids_user, float* w_user,
+                             cudaStream_t s) {
+  const moe_layer_config_t& c = L->cfg;
+  const int H = c.hidden, I = c.intermediate, E = c.num_experts, k = c.top_k;
+  const int grid = L->num_sms;
+  if (grid < 1) return MOE_ERR_UNSUPPORTED;
+  Decode1Args a = {};
+  RouteArgs& r = a.r;
+  r.x = x;
+  r.wr = L->w.router_w;
+  r.bias = L->w.router_bias;
+  r.T = 1;
+  r.H = H;
+  r.E = E;
+  r.k = k;
+  r.renorm = c.renormalize;
+  r.has_shared = c.has_shared_expert;
+  r.logits = L->logits;
+  r.ids = L->ids;
+  r.w = L->wts;
+  r.ids_user = ids_user;
+  r.w_user = w_user;
+  r.counts = L->counts;
+  r.offsets = L->offsets;
+  r.perm = L->perm;
+  r.inv_perm = L->inv_perm;
+  r.seg_expert = L->seg_expert;
+  r.seg_start = L->seg_start;
+  r.seg_count = L->seg_count;
+  r.num_seg = L->num_seg;
+  r.err = L->err;
+  a.pool = static_cast<const uint8_t*>(L->w.slot_pool);
+  a.record_bytes = (long long)L->lay.record;
+  a.expert_to_slot = L->w.expert_to_slot;
+  a.num_slots = c.num_slots;
+  for (int i = 0; i < 3; ++i) {
+    a.off_q[i] = (long long)L->lay.off[i];
+    a.off_s[i] = (long long)L->lay.off[3 + i];
+  }
+  a.I = I;
+  a.G = c.group_size;
+  a.h = L->hbuf;
+  a.out = out;
+  a.x_res = c.add_residual ? x : nullptr;
+  a.ctr = L->ctr1;
+  a.ctr_mod = (uint32_t)grid * 1024u;
+  a.trace = L->trace;
+  a.nseg_max = k + c.has_shared_expert;
+  a.max_units_g = decode1_max_tiles(a.nseg_max, I, grid);
+  a.max_units_d = (H / 16 + grid - 1) / grid;
+  a.max_rows_rt = (E + grid - 1) / grid;
+  if (decode1_smem_bytes(a) == 0) return MOE_ERR_UNSUPPORTED;
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
+  // (every CTA rewrites its stamps on every launch: no clearing launch)
+  cudaError_t e = launch_decode1(a, grid, s, L->pdl && L->decode_pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "batch-1 decode launch");
+  if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
+  L->last_single = true;
+  return MOE_OK;
+}
+
 moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s) {
   const moe_layer_config_t& c = L->cfg;
   CombineArgs ca = {};
@@ -627,6 +695,17 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
   // programmatic dependent launch only on explicitly created streams
   const bool pdl_saved = layer->pdl;
   if (s == nullptr) layer->pdl = false;
+  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->decode1 && T == 1) {
+    moe_status_t sd = moe::enqueue_decode1(layer, xh, oh, topk_ids, topk_w, s);
+    if (sd != MOE_ERR_UNSUPPORTED) {
+      layer->pdl = pdl_saved;
+      if (sd != MOE_OK) return sd;
+      layer->last_T = T;
+      layer->stats.forward_calls += 1;
+      layer->stats.tokens += (uint64_t)T;
+      return MOE_OK;
+    }
+  }
   if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->megakernel && T <= layer->megakernel_max_tokens) {
     moe_status_t sd = moe::enqueue_decode(layer, xh, T, oh, topk_ids, topk_w, s);
     if (sd != MOE_ERR_UNSUPPORTED) {
