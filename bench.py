@@ -602,7 +602,8 @@ def run_ours(args):
     return res
 
 
-def _mk_layer(MoELayer, torch, dev, lay, max_tokens, add_residual=False, partial_slots=None):
+def _mk_layer(MoELayer, torch, dev, lay, max_tokens, add_residual=False, partial_slots=None, spare_slots=0,
+              cache_policy=0):
     s = lay.shape
     kw = dict(hidden=s.hidden, intermediate=s.intermediate, num_experts=s.num_experts, top_k=s.top_k,
               group_size=s.group_size, renormalize=s.renormalize, has_shared=s.has_shared, max_tokens=max_tokens,
@@ -611,7 +612,8 @@ def _mk_layer(MoELayer, torch, dev, lay, max_tokens, add_residual=False, partial
               add_residual=add_residual)
     if partial_slots:
         host = torch.from_numpy(lay.records[lay.expert_to_slot]).pin_memory()
-        return MoELayer(num_slots=partial_slots, host_backing=host, **kw)
+        return MoELayer(num_slots=partial_slots, host_backing=host, spare_slots=spare_slots,
+                        cache_policy=cache_policy, **kw)
     return MoELayer(pool=torch.from_numpy(lay.records).to(dev),
                     expert_to_slot=torch.from_numpy(lay.expert_to_slot.astype(np.int32)).to(dev), **kw)
 
@@ -828,7 +830,9 @@ def run_partial(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    ml = _mk_layer(MoELayer, torch, dev, lay, T, partial_slots=PARTIAL_SLOTS)
+    published = PARTIAL_SLOTS - args.partial_spares
+    ml = _mk_layer(MoELayer, torch, dev, lay, T, partial_slots=published, spare_slots=args.partial_spares,
+                   cache_policy=args.partial_policy)
     xs = [torch.from_numpy(synth.make_tokens(shape.hidden, T, seed=1000 * (rank + 1) + r)).to(dev) for r in range(4)]
     out = torch.empty_like(xs[0])
     # live peak of pinned host -> device copies (the bound of this workload)
@@ -894,7 +898,10 @@ def run_partial(args):
         return None
     pairs = T * shape.top_k
     flops = 2 * T * shape.hidden * shape.num_experts + pairs * 6 * shape.hidden * shape.intermediate
-    res = _common(args, world, desc, shape, T, {"slots": PARTIAL_SLOTS, "l2": "expert copies stream from host "
+    res = _common(args, world, desc, shape, T, {"slots": PARTIAL_SLOTS, "published_slots": published,
+                                                "spare_slots": args.partial_spares,
+                                                "cache_policy": ["lru", "lfu", "lru-freq"][args.partial_policy],
+                                                "l2": "expert copies stream from host "
                                                 "memory every step (pool of 32 of 128 experts)"})
     res.update({
         "value": replica_throughput(T, world, ms_per_step), "ms_per_step": ms_per_step,
@@ -904,7 +911,9 @@ def run_partial(args):
                      "traffic": None, "h2d_bytes_per_step": h2d / K},
         "residency": {"hit_rate": hits / max(1, hits + misses), "hits_per_step": hits / K,
                       "misses_per_step": misses / K, "waves_per_step": (s1.waves - s0.waves) / K,
-                      "d2h_expert_bytes": int(st.d2h_expert_bytes)},
+                      "d2h_expert_bytes": int(st.d2h_expert_bytes),
+                      "generations_per_step": (s1.generations - s0.generations) / K,
+                      "evictions_per_step": (s1.evictions - s0.evictions) / K},
         "layer_roofline": {"flops_per_step": flops, "achieved_tflops": flops / (ms_per_step / 1e3) / 1e12},
         "cpu_baseline": cpu_base,
         "e2e": {"value": replica_throughput(T, world, e2e_ms / K), "unit": "tokens/s",
@@ -972,6 +981,11 @@ def main():
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the 8192-token prefill block of the default decode run")
     ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--partial-spares", type=int, default=0,
+                    help="partial residency: rows of the 32-row pool kept unpublished (copies of the next "
+                         "group land there while the current one computes)")
+    ap.add_argument("--partial-policy", type=int, default=0, choices=[0, 1, 2],
+                    help="partial residency eviction policy: 0 LRU, 1 LFU, 2 LRU-FREQ")
     ap.add_argument("--gemm-min-tokens", type=int, default=48,
                     help="batch size from which the library takes the tensor-core path (its default)")
     args = ap.parse_args()

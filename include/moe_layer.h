@@ -95,7 +95,25 @@ typedef struct {
   int32_t num_slots;         /* FULL: records in slot_pool; PARTIAL: slots of the library's pool */
   int32_t residency;         /* moe_residency_t */
   int32_t add_residual;      /* 1: out = fp16(x + fp16(layer(x))) (residual stream of stacked layers) */
+  /* PARTIAL residency only (ignored in FULL):
+   * spare_slots      unpublished rows beyond the num_slots published ones:
+   *                  misses are copied into them while earlier kernels still
+   *                  read the published rows (0: misses reuse evicted rows
+   *                  once their readers have retired);
+   * staging_records  pinned staging buffers (one record each) a pageable
+   *                  host_backing is copied through (0: 4); a page-locked
+   *                  host_backing is copied from directly;
+   * cache_policy     moe_cache_policy_t: which published expert is evicted. */
+  int32_t spare_slots;
+  int32_t staging_records;
+  int32_t cache_policy;
 } moe_layer_config_t;
+
+typedef enum {
+  MOE_POLICY_LRU = 0,     /* least recently used */
+  MOE_POLICY_LFU = 1,     /* least frequently used (every access counted) */
+  MOE_POLICY_LRU_FREQ = 2 /* lowest freq * 1000 - age; frequencies x0.75 every 2 x num_slots misses */
+} moe_cache_policy_t;
 
 typedef struct {
   const float* router_w;         /* device, FP32 [E][H] row-major */
@@ -118,7 +136,12 @@ typedef struct {
   uint64_t expert_misses;    /* PARTIAL: demanded experts copied host -> device */
   uint64_t h2d_bytes;        /* PARTIAL: expert bytes copied host -> device */
   uint64_t d2h_expert_bytes; /* expert bytes copied device -> host: 0 by construction */
-  uint64_t waves;            /* PARTIAL: expert-compute waves (one per pool refill) */
+  uint64_t waves;            /* PARTIAL: expert-compute waves (transactions: one routed group each) */
+  uint64_t generations;      /* PARTIAL: cache generations published (a group with misses publishes one) */
+  uint64_t evictions;        /* PARTIAL: experts dropped from the published set */
+  uint64_t staged_copies;    /* PARTIAL: records copied through the pinned staging buffers */
+  int32_t faulted;           /* PARTIAL: 1 once a failure after publication has faulted the cache */
+  int32_t reserved;
 } moe_layer_stats_t;
 
 typedef struct {

@@ -55,6 +55,49 @@ void moe_slot_planner_invalidate(moe_slot_planner_t* planner, int32_t slot);
 /* NULL is accepted. */
 void moe_slot_planner_destroy(moe_slot_planner_t* planner);
 
+/* ------------------------------------------------------------------------
+ * Expert cache model (the partially resident pool's bookkeeping, pure host
+ * code). Horizon RunMap report, "Partial-residency contract", steps 1-7: a
+ * forward works on a complete published generation; misses are loaded into
+ * unpublished rows (spare rows, or the rows of victims once their consumers
+ * have retired) and become visible only when the whole routed group is
+ * published as a new generation; a transaction that fails before
+ * publication leaves the old generation authoritative; eviction discards
+ * GPU copies. Policies (F51 Nitro-MoE, "Layer 1 - expert persistence
+ * cache"; moe-stream, "Findings"): least recently used, least frequently
+ * used (every access counted), and LRU-FREQ, scoring freq * 1000 - age with
+ * all frequencies multiplied by 0.75 after every 2 x capacity misses; the
+ * lowest score is evicted first, ties to the lower row. */
+typedef struct moe_expert_cache moe_expert_cache_t;
+
+enum { MOE_CACHE_LRU = 0, MOE_CACHE_LFU = 1, MOE_CACHE_LRU_FREQ = 2 };
+
+/* A cache of `capacity` published rows plus `spare_rows` unpublished rows,
+ * all empty; NULL on an invalid argument. */
+moe_expert_cache_t* moe_expert_cache_create(int32_t n_records, int32_t capacity, int32_t spare_rows, int32_t policy);
+
+/* One forward over n distinct demanded experts (any order): every access is
+ * counted (in ascending id), then transactions of at most `capacity`
+ * experts (the resident ones first, then misses in ascending id) are
+ * planned and published one after another. For demanded[i] it writes
+ * txn_of[i], row_of[i] (the row it is read from) and hit[i] (resident
+ * before the call); *n_txn receives the number of transactions. If
+ * abort_txn >= 0, that transaction fails before publication instead: the
+ * state keeps the previous generation, *n_txn is set to abort_txn and the
+ * call returns 1. Returns 0, or -1 on an invalid argument. */
+int32_t moe_expert_cache_access(moe_expert_cache_t* cache, const int32_t* demanded, int32_t n, int32_t abort_txn,
+                                int32_t* txn_of, int32_t* row_of, int32_t* hit, int32_t* n_txn);
+
+/* Published row of `expert`, or -1. */
+int32_t moe_expert_cache_row_of(const moe_expert_cache_t* cache, int32_t expert);
+
+/* out5[0..4] = hits, misses, evictions, generations published, frequency
+ * decays. Returns 0, or -1 on NULL. */
+int32_t moe_expert_cache_stats(const moe_expert_cache_t* cache, uint64_t* out5);
+
+/* NULL is accepted. */
+void moe_expert_cache_destroy(moe_expert_cache_t* cache);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,161 @@
+"""Host-side expert cache of the partially resident pool (CPU only): the
+eviction policies against closed forms and against Belady's optimum written
+out here by brute force, and the publication rules (transactions within
+capacity, misses loaded into unpublished rows, an aborted transaction leaves
+the previous generation in place)."""
+import numpy as np
+import pytest
+
+from w4a16_routed_expert_gb300 import build as B
+from w4a16_routed_expert_gb300 import capi
+
+POLICIES = [capi.MOE_CACHE_LRU, capi.MOE_CACHE_LFU, capi.MOE_CACHE_LRU_FREQ]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    capi.lib()
+
+
+def _run_single(seq, n, C, policy, spares=0):
+    """One expert demanded per forward: the cache acts as a plain cache of C."""
+    c = capi.ExpertCache(n, C, spares, policy)
+    hits = 0
+    for e in seq:
+        r = c.access([e])
+        hits += r["hit"][0]
+    st = c.stats()
+    assert st["hits"] == hits and st["misses"] == len(seq) - hits
+    return hits, st
+
+
+def _belady_hits(seq, C):
+    """Optimal offline replacement: on a miss with a full cache, drop the
+    resident expert whose next use is farthest away (or never)."""
+    cache = set()
+    hits = 0
+    for i, e in enumerate(seq):
+        if e in cache:
+            hits += 1
+            continue
+        if len(cache) == C:
+            def next_use(x):
+                for j in range(i + 1, len(seq)):
+                    if seq[j] == x:
+                        return j
+                return len(seq) + 1
+            cache.remove(max(cache, key=next_use))
+        cache.add(e)
+    return hits
+
+
+def test_cyclic_scan_gets_no_lru_hits():
+    # moe-stream, "Findings": a fixed walk over more experts than fit; LRU
+    # always drops the one needed next. Every access's reuse distance is N-1
+    # > C, so LRU has zero hits; Belady keeps C - 1 of them each round.
+    N, C, rounds = 128, 32, 4
+    seq = list(range(N)) * rounds
+    hits, _ = _run_single(seq, N, C, capi.MOE_CACHE_LRU)
+    assert hits == 0
+    opt = _belady_hits(seq, C)
+    assert opt > 0
+    for p in POLICIES:
+        assert _run_single(seq, N, C, p)[0] <= opt
+
+
+def test_lfu_keeps_a_hot_set_that_lru_loses():
+    # 12 hot experts alternate with a walk over 120 others, capacity 16. A
+    # hot expert comes back after 23 other accesses of 23 distinct experts
+    # (> 16): LRU misses every access. LFU counts the hot experts 10x more
+    # often than the walk and keeps them once ahead: from the third round of
+    # the walk on, every hot access hits.
+    P, S, C = 12, 120, 16
+    seq = []
+    for i in range(3 * 2 * S):
+        seq.append((i // 2) % P if i % 2 == 0 else P + (i // 2) % S)
+    hits_lru, _ = _run_single(seq, P + S, C, capi.MOE_CACHE_LRU)
+    assert hits_lru == 0
+    hot_late = sum(1 for i, e in enumerate(seq) if e < P and i >= 4 * S)
+    opt = _belady_hits(seq, C)
+    for p in (capi.MOE_CACHE_LFU, capi.MOE_CACHE_LRU_FREQ):
+        h, _ = _run_single(seq, P + S, C, p)
+        assert hot_late <= h <= opt, (p, h, hot_late, opt)
+
+
+def test_lru_freq_decays_every_two_capacities_of_misses():
+    # F51 Nitro-MoE, "Layer 1": frequencies decay by 0.75 every 2x capacity
+    # misses. A cyclic scan with N > C misses every access.
+    N, C = 100, 20
+    seq = list(range(N)) * 3
+    hits, st = _run_single(seq, N, C, capi.MOE_CACHE_LRU_FREQ)
+    assert hits == 0 and st["decays"] == len(seq) // (2 * C)
+    for p in (capi.MOE_CACHE_LRU, capi.MOE_CACHE_LFU):
+        assert _run_single(seq, N, C, p)[1]["decays"] == 0
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_every_policy_within_the_optimum_on_skewed_traces(seed):
+    rng = np.random.default_rng(seed)
+    N, C = 64, 12
+    w = 1.0 / np.arange(1, N + 1) ** 1.1
+    seq = rng.choice(N, size=600, p=w / w.sum()).tolist()
+    opt = _belady_hits(seq, C)
+    for p in POLICIES:
+        h, st = _run_single(seq, N, C, p)
+        assert 0 <= h <= opt
+        # every miss beyond the first C loads evicts one published expert
+        assert st["evictions"] == max(0, st["misses"] - C)
+
+
+@pytest.mark.parametrize("policy", POLICIES)
+@pytest.mark.parametrize("spares", [0, 5, 16])
+def test_batched_forwards_respect_capacity_and_publication(policy, spares):
+    rng = np.random.default_rng(7 + policy + spares)
+    N, C = 80, 16
+    c = capi.ExpertCache(N, C, spares, policy)
+    gen = 0
+    for call in range(40):
+        n = int(rng.integers(1, 3 * C))
+        demanded = rng.choice(N, size=n, replace=False).tolist()
+        before = {e: c.row_of(e) for e in range(N)}
+        published_rows = {r for r in before.values() if r >= 0}
+        res = c.access(demanded)
+        # every demanded expert computed once; transactions within capacity,
+        # distinct rows inside a transaction, hits only in the first one
+        for t in range(res["n_txn"]):
+            rows = [r for r, tt in zip(res["row"], res["txn"]) if tt == t]
+            assert 0 < len(rows) <= C and len(set(rows)) == len(rows)
+            assert all(0 <= r < C + spares for r in rows)
+        for e, h, t, r in zip(res["experts"], res["hit"], res["txn"], res["row"]):
+            assert h == (before[e] >= 0)
+            if h:
+                assert t == 0 and r == before[e]
+        # misses of the first transaction go to rows that were not published
+        # when it started, as long as enough unpublished rows exist
+        misses0 = [r for e, h, t, r in zip(res["experts"], res["hit"], res["txn"], res["row"]) if t == 0 and not h]
+        if len(misses0) <= C + spares - len(published_rows):
+            assert not (set(misses0) & published_rows)
+        # at most C experts published afterwards, each in its own row
+        after = [c.row_of(e) for e in range(N)]
+        pub = [r for r in after if r >= 0]
+        assert len(pub) <= C and len(set(pub)) == len(pub)
+        st = c.stats()
+        assert st["generations"] >= gen
+        gen = st["generations"]
+
+
+def test_aborted_transaction_keeps_the_previous_generation():
+    N, C = 40, 8
+    c = capi.ExpertCache(N, C, 4, capi.MOE_CACHE_LRU)
+    c.access(list(range(8)))
+    gen0 = c.stats()["generations"]
+    rows0 = [c.row_of(e) for e in range(N)]
+    res = c.access(list(range(20, 32)), abort_txn=0)
+    assert res["aborted"]
+    assert [c.row_of(e) for e in range(N)] == rows0
+    assert c.stats()["generations"] == gen0
+    # the cache keeps working: the same request now publishes
+    res = c.access(list(range(20, 32)))
+    assert not res["aborted"] and c.stats()["generations"] > gen0
+    assert all(c.row_of(e) >= 0 for e in range(24, 32))

@@ -21,15 +21,18 @@ def _cuda():
     capi.lib()
 
 
-def _partial(lay, slots, max_tokens):
+def _partial(lay, slots, max_tokens, spares=0, policy=0, pinned=False, staging=0):
     s = lay.shape
     host = torch.from_numpy(lay.records[lay.expert_to_slot]).contiguous()  # expert order
+    if pinned:
+        host = host.pin_memory()
     dev = torch.device("cuda")
     ml = MoELayer(hidden=s.hidden, intermediate=s.intermediate, num_experts=s.num_experts, top_k=s.top_k,
                   group_size=s.group_size, renormalize=s.renormalize, has_shared=s.has_shared,
                   max_tokens=max_tokens, router_w=torch.from_numpy(lay.router_w).to(dev),
                   router_bias=torch.from_numpy(lay.router_bias).to(dev) if lay.router_bias is not None else None,
-                  num_slots=slots, host_backing=host)
+                  num_slots=slots, host_backing=host, spare_slots=spares, cache_policy=policy,
+                  staging_records=staging)
     return ml, host
 
 
@@ -85,6 +88,57 @@ def test_capacity_shortfall_fails_at_create():
     with pytest.raises(capi.MoEError) as ei:
         _partial(lay, 3, 4)
     assert ei.value.status == capi.MOE_ERR_CAPACITY
+
+
+POLICIES = [capi.MOE_POLICY_LRU, capi.MOE_POLICY_LFU, capi.MOE_POLICY_LRU_FREQ]
+
+
+@pytest.mark.parametrize("policy", POLICIES)
+@pytest.mark.parametrize("spares", [0, 3, 5])
+@pytest.mark.parametrize("pinned", [False, True])
+def test_every_policy_matches_full_residency(policy, spares, pinned):
+    """Horizon RunMap report, "Partial-residency contract": whichever experts
+    the policy keeps, a forward reads complete published copies, so the
+    outputs are the full-residency outputs bit for bit; misses go through
+    the pinned staging buffers only when the host copy is pageable."""
+    shape = synth.LayerShape(512, 384, 24, 3, 128, True, has_shared=True)
+    lay = synth.make_layer(shape, seed=25, codes="uniform")
+    full = GH.upload(lay, max_tokens=12)
+    ml, host = _partial(lay, 5, 12, spares=spares, policy=policy, pinned=pinned, staging=2)
+    before = host.numpy().copy()
+    gens = 0
+    for call in range(3):
+        x = synth.make_tokens(shape.hidden, 12, seed=250 + call)
+        gf = GH.run(full, x)
+        g = GH.run(ml, x)
+        for key in ("out", "ids", "w", "perm", "counts"):
+            assert np.array_equal(g[key], gf[key]), (call, key)
+        st = ml.stats()
+        assert st.generations >= gens and st.faulted == 0
+        gens = st.generations
+    st = ml.stats()
+    assert st.h2d_bytes == st.expert_misses * lay.records.shape[1]
+    assert st.staged_copies == (0 if pinned else st.expert_misses)
+    assert st.d2h_expert_bytes == 0
+    assert np.array_equal(host.numpy(), before), "host backing was written"
+    full.close()
+    ml.close()
+
+
+def test_failure_after_publication_faults_the_cache(monkeypatch):
+    shape = synth.LayerShape(256, 256, 16, 2, 64, True)
+    lay = synth.make_layer(shape, seed=26, codes="uniform")
+    x = synth.make_tokens(shape.hidden, 8, seed=26)
+    monkeypatch.setenv("MOE_FAULT_INJECT", "after_publish")
+    ml, _ = _partial(lay, 4, 8)
+    with pytest.raises(capi.MoEError) as ei:
+        GH.run(ml, x)
+    assert ei.value.status == capi.MOE_ERR_CUDA and "faulted" in str(ei.value)
+    assert ml.stats().faulted == 1
+    with pytest.raises(capi.MoEError) as ei:  # every later forward fails
+        GH.run(ml, x)
+    assert "faulted" in str(ei.value)
+    ml.close()
 
 
 def test_partial_residency_full_size_every_row():

@@ -30,7 +30,8 @@ MOE_RESIDENCY_PARTIAL = 1
 class moe_layer_config_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "hidden", "intermediate", "num_experts", "top_k", "group_size", "renormalize",
-        "has_shared_expert", "max_tokens", "num_slots", "residency", "add_residual")]
+        "has_shared_expert", "max_tokens", "num_slots", "residency", "add_residual", "spare_slots",
+        "staging_records", "cache_policy")]
 
 
 class moe_layer_weights_t(ctypes.Structure):
@@ -42,7 +43,8 @@ class moe_layer_weights_t(ctypes.Structure):
 class moe_layer_stats_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "forward_calls", "tokens", "expert_hits", "expert_misses", "h2d_bytes",
-        "d2h_expert_bytes", "waves")]
+        "d2h_expert_bytes", "waves", "generations", "evictions", "staged_copies")] + [
+        ("faulted", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class moe_layer_profile_t(ctypes.Structure):
@@ -88,10 +90,64 @@ PROTOTYPES = {
     "moe_slot_planner_slot_of": (_I32, [_P, _I32]),
     "moe_slot_planner_invalidate": (None, [_P, _I32]),
     "moe_slot_planner_destroy": (None, [_P]),
+    "moe_expert_cache_create": (_P, [_I32, _I32, _I32, _I32]),
+    "moe_expert_cache_access": (_I32, [_P, ctypes.POINTER(_I32), _I32, _I32, ctypes.POINTER(_I32),
+                                       ctypes.POINTER(_I32), ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "moe_expert_cache_row_of": (_I32, [_P, _I32]),
+    "moe_expert_cache_stats": (_I32, [_P, ctypes.POINTER(ctypes.c_uint64)]),
+    "moe_expert_cache_destroy": (None, [_P]),
 }
 
 MOE_PLAN_HITS_FIRST = 0
 MOE_PLAN_FIXED_ORDER_LRU = 1
+MOE_CACHE_LRU = 0
+MOE_CACHE_LFU = 1
+MOE_CACHE_LRU_FREQ = 2
+# moe_cache_policy_t of moe_layer_config_t (same values)
+MOE_POLICY_LRU, MOE_POLICY_LFU, MOE_POLICY_LRU_FREQ = 0, 1, 2
+
+
+class ExpertCache:
+    """Host-side model of the partially resident expert cache (no GPU)."""
+
+    def __init__(self, n_records: int, capacity: int, spare_rows: int = 0, policy: int = MOE_CACHE_LRU):
+        self.n_records = n_records
+        self.h = lib().moe_expert_cache_create(n_records, capacity, spare_rows, policy)
+        if not self.h:
+            raise ValueError("invalid cache parameters")
+
+    def access(self, demanded, abort_txn: int = -1):
+        d = [int(e) for e in demanded]
+        n = len(d)
+        arr = (_I32 * max(n, 1))(*d)
+        txn = (_I32 * max(n, 1))()
+        row = (_I32 * max(n, 1))()
+        hit = (_I32 * max(n, 1))()
+        nt = _I32()
+        rc = lib().moe_expert_cache_access(self.h, arr, n, abort_txn, txn, row, hit, ctypes.byref(nt))
+        if rc < 0:
+            raise ValueError("invalid access")
+        return dict(experts=d, txn=list(txn)[:n], row=list(row)[:n], hit=list(hit)[:n], n_txn=nt.value,
+                    aborted=rc == 1)
+
+    def row_of(self, e: int) -> int:
+        return lib().moe_expert_cache_row_of(self.h, e)
+
+    def stats(self):
+        out = (ctypes.c_uint64 * 5)()
+        lib().moe_expert_cache_stats(self.h, out)
+        return dict(hits=out[0], misses=out[1], evictions=out[2], generations=out[3], decays=out[4])
+
+    def close(self):
+        if self.h:
+            lib().moe_expert_cache_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class SlotPlanner:

@@ -75,6 +75,12 @@ moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w)
     if (c->num_slots < c->top_k + c->has_shared_expert)
       return fail(MOE_ERR_CAPACITY, "num_slots=%d cannot hold one token's %d experts", c->num_slots,
                   c->top_k + c->has_shared_expert);
+    if (c->spare_slots < 0 || c->spare_slots > n_records)
+      return fail(MOE_ERR_INVALID_ARG, "spare_slots=%d out of 0..%d", c->spare_slots, n_records);
+    if (c->staging_records < 0 || c->staging_records > 64)
+      return fail(MOE_ERR_INVALID_ARG, "staging_records=%d out of 0..64", c->staging_records);
+    if (c->cache_policy < MOE_POLICY_LRU || c->cache_policy > MOE_POLICY_LRU_FREQ)
+      return fail(MOE_ERR_INVALID_ARG, "cache_policy=%d unknown", c->cache_policy);
   } else {
     return fail(MOE_ERR_INVALID_ARG, "residency=%d unknown", c->residency);
   }

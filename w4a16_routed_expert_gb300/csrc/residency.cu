@@ -1,23 +1,37 @@
-// Partial residency: a library-owned pool of num_slots expert records on the
-// device, filled from the caller's host copy of every record.
+// Partial residency: a library-owned pool of expert records on the device,
+// filled from the caller's host copy of every record.
 //
-// Horizon RunMap report, "Partial-residency contract": the host copy is the
-// authority and is never written; misses move compact records host -> device
-// through page-locked memory, a copy is used only after its transfer has
-// completed (an event), eviction simply discards device copies, a failure
-// before use leaves the previous mapping authoritative, and too little
-// capacity fails at create. F51 Nitro-MoE, "Layer 1 - expert persistence
-// cache": a fixed slot pool per layer addressed through expert_to_slot.
+// Horizon RunMap report, "Partial-residency contract", steps 1-7, as this
+// driver keeps them:
+//  1-2. a forward plans its routed experts in transactions (groups computed
+//       together, at most num_slots of them); a group whose experts are all
+//       resident reads the published rows as they are;
+//  3. a miss is copied into a row that is not published (a spare row, or
+//       the row of an evicted expert once every kernel reading it has
+//       retired), through a bounded ring of pinned staging buffers when the
+//       host copy is pageable (copied from directly when it is page-locked);
+//  4. a staging buffer is refilled only after the event of its previous
+//       transfer has completed;
+//  5. the group's mapping (expert -> row) is published, as a new generation,
+//       only after its copies have completed (the table upload waits on
+//       their event on the forward's stream), and atomically (each
+//       transaction reads its own table);
+//  6. a row that leaves the published set is overwritten only after the
+//       kernels of every transaction that read it (their event) are done;
+//  7. eviction only drops the mapping: nothing is ever copied back to the
+//       host and the host copy is never written.
+// A transaction that fails before publication leaves the previous generation
+// authoritative (its rows return to the spares, contents untrusted); a
+// failure after publication faults the cache: every later forward fails
+// until the handle is destroyed. Capacity is fixed at create (num_slots +
+// spare_slots rows, staging_records buffers); too little fails create.
+// The policies that pick victims live in expert_cache.cpp.
 //
 // One forward: routing runs on the caller's stream; the expert counts come
-// back to the host (the only device -> host copy, and the only
-// synchronisation); the slot planner splits the demanded experts into waves
-// of at most num_slots experts (hits first). For each wave the side stream
-// waits until the previous wave's kernels are done with the slots it
-// overwrites, copies the wave's misses, and records an event the caller's
-// stream waits on before running the wave's expert kernels. Every wave has
-// its own events and its own segment table, so nothing is reused before it
-// has retired; the next forward's synchronisation retires them all.
+// back to the host (the only device -> host copy and the only
+// synchronisation); then, transaction by transaction, the copies go to the
+// side stream and the expert kernels to the caller's stream. With spare rows
+// the next transaction's copies stream while the current one computes.
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
@@ -25,9 +39,9 @@
 #include <new>
 #include <vector>
 
+#include "expert_cache.h"
 #include "layer_internal.h"
 #include "residency.h"
-#include "slot_planner.h"
 
 namespace moe {
 
@@ -37,24 +51,33 @@ thread_local char g_res_msg[256];
 }
 
 struct Residency {
-  SlotPlanner planner;
-  int num_slots = 0, n_records = 0, E = 0;
+  ExpertCache cache;
+  int num_slots = 0, rows = 0, n_records = 0, E = 0;
   size_t rb = 0;
   const uint8_t* host = nullptr;
-  bool registered_here = false;
-  uint8_t* pool = nullptr;
+  bool host_pinned = false;           // page-locked host copy: copied from directly
+  uint8_t* pool = nullptr;            // rows x rb
   cudaStream_t side = nullptr;
-  int max_waves = 0;
+  int max_txn = 0;
   int tbl_ints = 0;
-  std::vector<cudaEvent_t> ev_free, ev_ready;
+  std::vector<cudaEvent_t> ev_done;   // per transaction index: its kernels done (caller's stream)
+  std::vector<cudaEvent_t> ev_ready;  // per transaction index: its copies done (side stream)
+  std::vector<int> row_reader;        // per row: transaction index whose kernels last read it, -1 none
+  // pinned staging ring (pageable host copy)
+  int n_staging = 0;
+  std::vector<uint8_t*> staging;
+  std::vector<cudaEvent_t> ev_staging;
+  std::vector<char> staging_used;
+  int staging_next = 0;
   int32_t* h_counts = nullptr;
   int32_t* h_tbl = nullptr;
   int32_t* d_tbl = nullptr;
-  int inject_h2d_fail = 0;  // one-shot host-side fault injection
-  CodeMaps maps = {};       // tensor maps of the pool (tensor-core path)
+  int inject = 0;  // host-side fault injection: 1 before publication, 2 after (one-shot)
+  bool faulted = false;
+  CodeMaps maps = {};  // tensor maps of the pool (tensor-core path)
   bool maps_tried = false;
-  uint64_t hits = 0, misses = 0, h2d_bytes = 0, waves = 0;
-  Residency(int n, int s) : planner(n, s) {}
+  uint64_t waves = 0, h2d_bytes = 0, staged = 0;
+  Residency(int n, int cap, int spares, CachePolicy p) : cache(n, cap, spares, p) {}
 };
 
 const char* residency_last_error() { return g_res_err; }
@@ -62,64 +85,68 @@ const char* residency_last_error() { return g_res_err; }
 void residency_destroy(Residency* r) {
   if (!r) return;
   if (r->side) cudaStreamSynchronize(r->side);
-  for (cudaEvent_t e : r->ev_free)
+  for (cudaEvent_t e : r->ev_done)
     if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : r->ev_ready)
     if (e) cudaEventDestroy(e);
+  for (cudaEvent_t e : r->ev_staging)
+    if (e) cudaEventDestroy(e);
+  for (uint8_t* p : r->staging)
+    if (p) cudaFreeHost(p);
   if (r->side) cudaStreamDestroy(r->side);
   if (r->pool) cudaFree(r->pool);
   if (r->d_tbl) cudaFree(r->d_tbl);
   if (r->h_tbl) cudaFreeHost(r->h_tbl);
   if (r->h_counts) cudaFreeHost(r->h_counts);
-  if (r->registered_here) cudaHostUnregister(const_cast<uint8_t*>(r->host));
   delete r;
 }
 
 moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes, int n_records,
                               const void* host_backing, Residency** out) {
   *out = nullptr;
-  Residency* r = new (std::nothrow) Residency(n_records, cfg.num_slots);
+  const int spares = cfg.spare_slots;
+  Residency* r = new (std::nothrow) Residency(n_records, cfg.num_slots, spares, (CachePolicy)cfg.cache_policy);
   if (!r) {
     g_res_err = "host allocation failed";
     return MOE_ERR_OOM;
   }
   r->num_slots = cfg.num_slots;
+  r->rows = cfg.num_slots + spares;
   r->n_records = n_records;
   r->E = cfg.num_experts;
   r->rb = record_bytes;
   r->host = static_cast<const uint8_t*>(host_backing);
-  r->max_waves = (n_records + cfg.num_slots - 1) / cfg.num_slots + 1;
+  r->max_txn = (n_records + cfg.num_slots - 1) / cfg.num_slots + 1;
   r->tbl_ints = (int)((4 * (size_t)n_records + 1 + 63) / 64 * 64);
+  r->row_reader.assign(r->rows, -1);
   const char* inj = getenv("MOE_FAULT_INJECT");
-  r->inject_h2d_fail = (inj && strcmp(inj, "h2d_fail") == 0) ? 1 : 0;
+  if (inj && strcmp(inj, "h2d_fail") == 0) r->inject = 1;
+  if (inj && strcmp(inj, "after_publish") == 0) r->inject = 2;
 
   moe_status_t st = MOE_OK;
-  cudaError_t e = cudaMalloc(&r->pool, (size_t)cfg.num_slots * record_bytes);
+  cudaError_t e = cudaMalloc(&r->pool, (size_t)r->rows * record_bytes);
   if (e != cudaSuccess) {
     g_res_err = "slot pool allocation failed";
     st = MOE_ERR_OOM;
   }
   if (st == MOE_OK) {
-    // already page-locked (cudaHostAlloc or registered by the caller): use as is
     cudaPointerAttributes pa = {};
-    const bool pinned = cudaPointerGetAttributes(&pa, host_backing) == cudaSuccess && pa.type == cudaMemoryTypeHost;
+    r->host_pinned = cudaPointerGetAttributes(&pa, host_backing) == cudaSuccess && pa.type == cudaMemoryTypeHost;
     cudaGetLastError();
-    if (!pinned) {
-      int ro = 0;
-      int dev = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&ro, cudaDevAttrHostRegisterReadOnlySupported, dev);
-      const unsigned flags = ro ? cudaHostRegisterReadOnly : cudaHostRegisterDefault;
-      e = cudaHostRegister(const_cast<void*>(host_backing), (size_t)n_records * record_bytes, flags);
-      if (e == cudaSuccess) {
-        r->registered_here = true;
-      } else if (e == cudaErrorHostMemoryAlreadyRegistered) {
-        cudaGetLastError();
-      } else {
-        cudaGetLastError();
-        snprintf(g_res_msg, sizeof(g_res_msg), "registering the host backing failed: %s", cudaGetErrorString(e));
-        g_res_err = g_res_msg;
-        st = MOE_ERR_CUDA;
+    if (!r->host_pinned) {
+      // pageable host copy: a bounded ring of pinned staging buffers
+      r->n_staging = cfg.staging_records > 0 ? cfg.staging_records : 4;
+      r->staging.assign(r->n_staging, nullptr);
+      r->ev_staging.assign(r->n_staging, nullptr);
+      r->staging_used.assign(r->n_staging, 0);
+      for (int i = 0; i < r->n_staging && st == MOE_OK; ++i) {
+        if (cudaHostAlloc(reinterpret_cast<void**>(&r->staging[i]), record_bytes, cudaHostAllocDefault) != cudaSuccess) {
+          g_res_err = "pinned staging allocation failed";
+          st = MOE_ERR_OOM;
+        } else if (cudaEventCreateWithFlags(&r->ev_staging[i], cudaEventDisableTiming) != cudaSuccess) {
+          g_res_err = "event creation failed";
+          st = MOE_ERR_CUDA;
+        }
       }
     }
   }
@@ -128,10 +155,10 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
     st = MOE_ERR_CUDA;
   }
   if (st == MOE_OK) {
-    r->ev_free.assign(r->max_waves, nullptr);
-    r->ev_ready.assign(r->max_waves, nullptr);
-    for (int i = 0; i < r->max_waves && st == MOE_OK; ++i) {
-      if (cudaEventCreateWithFlags(&r->ev_free[i], cudaEventDisableTiming) != cudaSuccess ||
+    r->ev_done.assign(r->max_txn, nullptr);
+    r->ev_ready.assign(r->max_txn, nullptr);
+    for (int i = 0; i < r->max_txn && st == MOE_OK; ++i) {
+      if (cudaEventCreateWithFlags(&r->ev_done[i], cudaEventDisableTiming) != cudaSuccess ||
           cudaEventCreateWithFlags(&r->ev_ready[i], cudaEventDisableTiming) != cudaSuccess) {
         g_res_err = "event creation failed";
         st = MOE_ERR_CUDA;
@@ -139,7 +166,7 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
     }
   }
   if (st == MOE_OK) {
-    const size_t tb = (size_t)r->max_waves * r->tbl_ints * sizeof(int32_t);
+    const size_t tb = (size_t)r->max_txn * r->tbl_ints * sizeof(int32_t);
     if (cudaHostAlloc(&r->h_counts, (size_t)cfg.num_experts * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess ||
         cudaHostAlloc(&r->h_tbl, tb, cudaHostAllocDefault) != cudaSuccess ||
         cudaMalloc(&r->d_tbl, tb) != cudaSuccess) {
@@ -156,12 +183,43 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
   return MOE_OK;
 }
 
+namespace {
+
+// Copies record `expert` into pool row `row` on the side stream, once the
+// kernels that last read that row (their transaction's event) are done:
+// directly from a page-locked host copy, else through the next staging
+// buffer (refilled on the host after its previous transfer completed).
+cudaError_t transport(Residency* r, int expert, int row) {
+  cudaError_t e = cudaSuccess;
+  if (r->row_reader[row] >= 0) e = cudaStreamWaitEvent(r->side, r->ev_done[r->row_reader[row]], 0);
+  if (e != cudaSuccess) return e;
+  uint8_t* dst = r->pool + (size_t)row * r->rb;
+  const uint8_t* src = r->host + (size_t)expert * r->rb;
+  if (r->host_pinned) return cudaMemcpyAsync(dst, src, r->rb, cudaMemcpyHostToDevice, r->side);
+  const int si = r->staging_next;
+  r->staging_next = (si + 1) % r->n_staging;
+  if (r->staging_used[si]) {
+    e = cudaEventSynchronize(r->ev_staging[si]);
+    if (e != cudaSuccess) return e;
+  }
+  memcpy(r->staging[si], src, r->rb);
+  e = cudaMemcpyAsync(dst, r->staging[si], r->rb, cudaMemcpyHostToDevice, r->side);
+  if (e == cudaSuccess) e = cudaEventRecord(r->ev_staging[si], r->side);
+  r->staging_used[si] = 1;
+  r->staged += 1;
+  return e;
+}
+
+}  // namespace
+
 moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s) {
   const moe_layer_config_t& c = L->cfg;
   const int E = c.num_experts, k = c.top_k;
+  if (r->faulted)
+    return set_error(MOE_ERR_CUDA, "the expert cache is faulted (a failure after publication); destroy the handle");
   if (!r->maps_tried) {
     r->maps_tried = true;
-    encode_pool_maps(L, r->pool, r->num_slots, &r->maps);
+    encode_pool_maps(L, r->pool, r->rows, &r->maps);
   }
   // demanded experts: the only device -> host copy of the forward
   cudaError_t e = cudaMemcpyAsync(r->h_counts, L->counts, (size_t)E * sizeof(int32_t), cudaMemcpyDeviceToHost, s);
@@ -178,69 +236,96 @@ moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int 
   if (run != T * k) return set_error(MOE_ERR_INTERNAL, "expert counts sum to %d, expected %d", run, T * k);
   if (c.has_shared_expert) demanded.push_back(E);
 
-  const std::vector<SlotPlanner::Wave> waves = r->planner.plan(demanded);
-  if ((int)waves.size() > r->max_waves) return set_error(MOE_ERR_INTERNAL, "planner produced too many waves");
+  // every access is counted (ascending id): a hit is an expert published
+  // when the forward starts
+  for (int ex : demanded) r->cache.touch(ex, r->cache.row_of(ex) >= 0);
   const int n = r->n_records;
-  for (size_t wi = 0; wi < waves.size(); ++wi) {
-    const SlotPlanner::Wave& w = waves[wi];
-    int32_t* tbl = r->h_tbl + wi * r->tbl_ints;
+  std::vector<int> remaining = demanded;
+  for (int ti = 0; !remaining.empty(); ++ti) {
+    if (ti >= r->max_txn) return set_error(MOE_ERR_INTERNAL, "too many transactions in one forward");
+    const ExpertCache::Txn t = r->cache.next(remaining, ti == 0);
+    if (t.experts.empty()) return set_error(MOE_ERR_INTERNAL, "empty transaction");
+    // the transaction's table: expert -> row, and its segment list
+    int32_t* tbl = r->h_tbl + (size_t)ti * r->tbl_ints;
     int32_t* e2s = tbl;
     int32_t* nseg = tbl + n;
     int32_t* sexp = nseg + 1;
     int32_t* sstart = sexp + n;
     int32_t* scount = sstart + n;
     std::fill(e2s, e2s + n, -1);
-    *nseg = (int32_t)w.experts.size();
-    for (size_t j = 0; j < w.experts.size(); ++j) {
-      const int ex = w.experts[j];
-      e2s[ex] = w.slots[j];
-      sexp[j] = ex;
-      sstart[j] = ex < E ? start[ex] : T * k;
-      scount[j] = ex < E ? r->h_counts[ex] : T;
+    *nseg = (int32_t)t.experts.size();
+    // segments in ascending expert id (the order the kernels expect)
+    std::vector<int> ord(t.experts.size());
+    for (size_t j = 0; j < ord.size(); ++j) ord[j] = (int)j;
+    std::sort(ord.begin(), ord.end(), [&](int a, int b) { return t.experts[a] < t.experts[b]; });
+    for (size_t q = 0; q < ord.size(); ++q) {
+      const int j = ord[q], ex = t.experts[j];
+      e2s[ex] = t.rows[j];
+      sexp[q] = ex;
+      sstart[q] = ex < E ? start[ex] : T * k;
+      scount[q] = ex < E ? r->h_counts[ex] : T;
     }
-    if (!w.loads.empty()) {
-      if (r->inject_h2d_fail && wi == 1) {
-        // injected failure before this wave's copies: nothing of this wave
-        // is published; earlier waves stay committed
-        r->inject_h2d_fail = 0;
-        return set_error(MOE_ERR_CUDA, "injected host->device copy failure (wave %zu)", wi);
+    if (!t.loads.empty()) {
+      if (r->inject == 1 && ti >= 1) {
+        // injected failure before publication: the previous generation
+        // stays authoritative
+        r->inject = 0;
+        r->cache.abort(t);
+        return set_error(MOE_ERR_CUDA, "injected host->device copy failure before publication (transaction %d)", ti);
       }
-      e = cudaEventRecord(r->ev_free[wi], s);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(r->side, r->ev_free[wi], 0);
-      for (size_t j = 0; j < w.loads.size() && e == cudaSuccess; ++j) {
-        const int ex = w.loads[j].first, slot = w.loads[j].second;
-        e = cudaMemcpyAsync(r->pool + (size_t)slot * r->rb, r->host + (size_t)ex * r->rb, r->rb,
-                            cudaMemcpyHostToDevice, r->side);
-      }
-      if (e == cudaSuccess) e = cudaEventRecord(r->ev_ready[wi], r->side);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, r->ev_ready[wi], 0);
+      for (size_t j = 0; j < t.loads.size() && e == cudaSuccess; ++j) e = transport(r, t.loads[j].first, t.loads[j].second);
+      if (e == cudaSuccess) e = cudaEventRecord(r->ev_ready[ti], r->side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, r->ev_ready[ti], 0);
       if (e != cudaSuccess) {
-        // the slots this wave was filling can no longer be trusted
-        for (const auto& ld : w.loads) r->planner.invalidate(ld.second);
+        r->cache.abort(t);
         return set_error(MOE_ERR_CUDA, "expert copy host->device: %s", cudaGetErrorString(e));
       }
     }
-    int32_t* dtbl = r->d_tbl + wi * r->tbl_ints;
+    // publication on the forward's stream, after the copies completed
+    int32_t* dtbl = r->d_tbl + (size_t)ti * r->tbl_ints;
     e = cudaMemcpyAsync(dtbl, tbl, (size_t)r->tbl_ints * sizeof(int32_t), cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "wave table host->device: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) {
+      r->cache.abort(t);
+      return set_error(MOE_ERR_CUDA, "transaction table host->device: %s", cudaGetErrorString(e));
+    }
+    r->cache.publish(t);
+    if (r->inject == 2 && !t.loads.empty()) {
+      r->inject = 0;
+      r->faulted = true;
+      return set_error(MOE_ERR_CUDA, "injected failure after publication: the expert cache is faulted");
+    }
     const SegPtrs seg = {dtbl + n, dtbl + n + 1, dtbl + 2 * n + 1, dtbl + 3 * n + 1};
-    moe_status_t st = enqueue_experts(L, x, T, s, r->pool, dtbl, r->num_slots, seg, (int)w.experts.size(), &r->maps);
-    if (st != MOE_OK) return st;
-    r->planner.commit(w);
-    r->hits += w.experts.size() - w.loads.size();
-    r->misses += w.loads.size();
-    r->h2d_bytes += (uint64_t)w.loads.size() * r->rb;
+    moe_status_t st = enqueue_experts(L, x, T, s, r->pool, dtbl, r->rows, seg, (int)t.experts.size(), &r->maps);
+    if (st != MOE_OK) {
+      r->faulted = true;  // published, kernels not enqueued: the state is ambiguous
+      return st;
+    }
+    e = cudaEventRecord(r->ev_done[ti], s);
+    if (e != cudaSuccess) {
+      r->faulted = true;
+      return set_error(MOE_ERR_CUDA, "transaction event: %s", cudaGetErrorString(e));
+    }
+    for (int row : t.rows) r->row_reader[row] = ti;
     r->waves += 1;
+    r->h2d_bytes += (uint64_t)t.loads.size() * r->rb;
+    std::vector<int> rest;
+    for (int ex : remaining)
+      if (std::find(t.experts.begin(), t.experts.end(), ex) == t.experts.end()) rest.push_back(ex);
+    remaining.swap(rest);
   }
   return enqueue_combine(L, x, T, out, s);
 }
 
 void residency_fill_stats(const Residency* r, moe_layer_stats_t* st) {
-  st->expert_hits = r->hits;
-  st->expert_misses = r->misses;
+  st->expert_hits = r->cache.hits;
+  st->expert_misses = r->cache.misses;
   st->h2d_bytes = r->h2d_bytes;
   st->waves = r->waves;
   st->d2h_expert_bytes = 0;
+  st->generations = r->cache.generation();
+  st->evictions = r->cache.evictions;
+  st->staged_copies = r->staged;
+  st->faulted = r->faulted ? 1 : 0;
 }
 
 }  // namespace moe

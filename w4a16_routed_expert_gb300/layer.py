@@ -27,12 +27,16 @@ class MoELayer:
     router_w: cuda fp32 [E][H]; router_bias: cuda fp32 [E] or None;
     pool: cuda uint8 [num_slots][record_bytes] (full residency) ;
     expert_to_slot: cuda int32 [E (+1)];
-    host_backing: pinned cpu uint8 [E (+1)][record_bytes] (partial residency).
+    host_backing: cpu uint8 [E (+1)][record_bytes] (partial residency; pageable
+    memory is copied through the library's pinned staging buffers);
+    spare_slots / staging_records / cache_policy: partial residency, see
+    moe_layer_config_t.
     """
 
     def __init__(self, *, hidden, intermediate, num_experts, top_k, group_size, renormalize,
                  has_shared=False, max_tokens, router_w, router_bias=None, pool=None,
-                 expert_to_slot=None, num_slots=None, host_backing=None, add_residual=False):
+                 expert_to_slot=None, num_slots=None, host_backing=None, add_residual=False, spare_slots=0,
+                 staging_records=0, cache_policy=0):
         partial = host_backing is not None
         self.cfg = capi.moe_layer_config_t(
             hidden=hidden, intermediate=intermediate, num_experts=num_experts, top_k=top_k,
@@ -40,7 +44,8 @@ class MoELayer:
             max_tokens=max_tokens,
             num_slots=int(num_slots if num_slots is not None else (pool.shape[0] if pool is not None else 0)),
             residency=capi.MOE_RESIDENCY_PARTIAL if partial else capi.MOE_RESIDENCY_FULL,
-            add_residual=int(bool(add_residual)))
+            add_residual=int(bool(add_residual)), spare_slots=int(spare_slots),
+            staging_records=int(staging_records), cache_policy=int(cache_policy))
         self.weights = capi.moe_layer_weights_t(
             router_w=_ptr(router_w), router_bias=_ptr(router_bias),
             slot_pool=None if partial else _ptr(pool), expert_to_slot=None if partial else _ptr(expert_to_slot),
