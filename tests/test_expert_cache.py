@@ -159,3 +159,43 @@ def test_aborted_transaction_keeps_the_previous_generation():
     res = c.access(list(range(20, 32)))
     assert not res["aborted"] and c.stats()["generations"] > gen0
     assert all(c.row_of(e) >= 0 for e in range(24, 32))
+
+
+def _zipf_trace(n_experts, k, tokens, s, seed):
+    """Top-k routing of each token over n_experts with a Zipf(s) popularity
+    (the experts of one token are distinct)."""
+    rng = np.random.default_rng(seed)
+    w = 1.0 / np.arange(1, n_experts + 1) ** s
+    w = w / w.sum()
+    return [rng.choice(n_experts, size=k, replace=False, p=w).tolist() for _ in range(tokens)]
+
+
+def test_hit_rate_sweep_over_capacities(capsys):
+    """Hit rate of each policy at capacities 16 / 32 / 48 / 64 / 128 on a
+    synthetic top-4-of-128 trace with Zipf(1.1) popularity, one token per
+    forward. LRU is a stack algorithm: its hit rate never falls when the
+    capacity grows; the full capacity holds every expert after its first
+    use; no policy beats the offline optimum of the flattened trace."""
+    trace = _zipf_trace(128, 4, 1500, 1.1, seed=11)
+    flat = [e for tok in trace for e in tok]
+    rows = {}
+    for p, name in zip(POLICIES, ("lru", "lfu", "lru-freq")):
+        rates = []
+        for C in (16, 32, 48, 64, 128):
+            c = capi.ExpertCache(128, C, 0, p)
+            for tok in trace:
+                c.access(tok)
+            st = c.stats()
+            rates.append(st["hits"] / (st["hits"] + st["misses"]))
+            if C == 128:
+                assert st["misses"] == len(set(flat))  # only first uses miss
+        rows[name] = rates
+    assert all(a <= b + 1e-12 for a, b in zip(rows["lru"], rows["lru"][1:]))
+    for C, i in ((16, 0), (32, 1)):
+        opt = _belady_hits(flat, C) / len(flat)
+        for name in rows:
+            assert rows[name][i] <= opt + 1e-12, (name, C)
+    with capsys.disabled():
+        print("\nhit rate (top-4 of 128, Zipf 1.1, 1500 tokens) at capacity 16/32/48/64/128:")
+        for name, r in rows.items():
+            print(f"  {name:9s}" + " ".join(f"{v:6.3f}" for v in r))
