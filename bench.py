@@ -52,12 +52,16 @@ WORKLOADS = {
     "olmoe-prefill-t8192": (synth.OLMOE, 8192, 1, "OLMoE-shaped layer, 8192-token prefill"),
     "olmoe-stack16-t1": (synth.OLMOE, 1, 2, "16 stacked OLMoE-shaped layers with a residual stream, decode batch 1"),
     "olmoe-stack16-t64": (synth.OLMOE, 64, 2, "16 stacked OLMoE-shaped layers with a residual stream, batch 64"),
+    "olmoe-stack16-partial-t1": (synth.OLMOE, 1, 2,
+                                 "16 stacked OLMoE-shaped layers, decode batch 1, each layer 16 of its 64 "
+                                 "experts resident, filled from pinned host backing; with next-layer prefetch"),
     "gptoss-partial-t2048": (synth.GPTOSS_LIKE, 2048, 4,
                              "2880-wide layer, 128 experts top-4, 32 resident slots filled from pinned host "
                              "backing, 2048 tokens"),
 }
 STACK_LAYERS = 16
 PARTIAL_SLOTS = 32
+STACK_PARTIAL_SLOTS = 16
 DEFAULT_WORKLOAD = "olmoe-decode-t1"
 PREFILL_WORKLOAD = "olmoe-prefill-t8192"
 
@@ -805,6 +809,165 @@ def run_stack(args):
     return res
 
 
+def _h2d_peak(torch, dev):
+    """Live peak of pinned host -> device copies (1 GiB, after 2 warm-ups)."""
+    hb = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
+    db = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        db.copy_(hb, non_blocking=True)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for _ in range(5):
+        db.copy_(hb, non_blocking=True)
+    c1.record()
+    torch.cuda.synchronize()
+    peak = 5 * (1 << 30) / (c0.elapsed_time(c1) / 1e3) / 1e9
+    del hb, db
+    return peak
+
+
+def run_stack_partial(args):
+    """16 stacked layers as in run_stack, each partially resident (16 of 64
+    experts per layer in its device pool, the rest streamed from pinned host
+    memory), decode batch 1, timed eagerly twice: plain, then with
+    moe-stream's next-layer prefetch (layer l+1's router run on layer l's
+    input right after layer l is enqueued; its guessed experts copied while
+    layer l computes). Each arm starts from cold pools and runs the same
+    inputs; `value` is the prefetch arm."""
+    import torch
+
+    from w4a16_routed_expert_gb300 import build as B
+    from w4a16_routed_expert_gb300 import capi
+    from w4a16_routed_expert_gb300.layer import MoELayer
+
+    world, rank, local = _dist()
+    shape, T, seed, desc = WORKLOADS[args.workload]
+    lays = [synth.make_layer(shape, seed=synth.stack_layer_seed(seed, l)) for l in range(STACK_LAYERS)]
+    cpu_base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sdesc, _ = oracle_sample(lays[0], shape, T, seed, args.cpu_seconds)
+        cpu_base = {"value": v / STACK_LAYERS, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                    "sample": sdesc + f" of one layer, scaled to the {STACK_LAYERS}-layer stack"}
+    if not os.path.exists(capi.LIB_PATH):
+        B.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    h2d_peak = _h2d_peak(torch, dev)
+    K, W = min(args.steps, 200), args.warmup
+    noise = [torch.from_numpy(synth.make_noise(shape.hidden, T, seed, st)).to(dev) for st in range(32)]
+    x0 = torch.from_numpy(synth.make_tokens(shape.hidden, T, seed=1000 * (rank + 1))).to(dev)
+    hosts = [torch.from_numpy(lay.records[lay.expert_to_slot]).pin_memory() for lay in lays]
+
+    def arm(prefetch, e2e=False):
+        kw = lambda lay: dict(hidden=shape.hidden, intermediate=shape.intermediate, num_experts=shape.num_experts,
+                              top_k=shape.top_k, group_size=shape.group_size, renormalize=shape.renormalize,
+                              has_shared=shape.has_shared, max_tokens=T, add_residual=True,
+                              router_w=torch.from_numpy(lay.router_w).to(dev), router_bias=None)
+        layers = [MoELayer(num_slots=STACK_PARTIAL_SLOTS, host_backing=h, **kw(lay)) for lay, h in zip(lays, hosts)]
+        xbuf = [x0.clone()] + [torch.empty_like(x0) for _ in range(STACK_LAYERS)]
+        xh = x0.cpu().pin_memory()
+        oh = torch.empty_like(xh).pin_memory()
+        noise_h = [n.cpu().numpy() for n in noise]
+
+        def step(i):
+            if e2e:
+                xbuf[0].copy_(xh, non_blocking=True)
+            for l in range(STACK_LAYERS):
+                layers[l].forward(xbuf[l], out=xbuf[l + 1])
+                if prefetch and l + 1 < STACK_LAYERS:
+                    layers[l + 1].prefetch(xbuf[l])
+            if e2e:
+                # the same recurrence through host memory: the output comes
+                # back, the next input is formed on the host and sent
+                oh.copy_(xbuf[STACK_LAYERS], non_blocking=True)
+                torch.cuda.current_stream().synchronize()
+                y = oh.numpy().astype(np.float32)
+                y = y / np.sqrt(np.maximum((y * y).mean(axis=1, keepdims=True), 1e-12))
+                xh.numpy()[:] = (y + noise_h[i % len(noise_h)]).astype(np.float16)
+            else:
+                y = xbuf[STACK_LAYERS].float()
+                y = y * torch.rsqrt(y.square().mean(dim=1, keepdim=True).clamp_min(1e-12))
+                xbuf[0].copy_((y + noise[i % len(noise)]).half())
+
+        for i in range(W):
+            step(i)
+        torch.cuda.synchronize()
+        s0 = [l.stats() for l in layers]
+        sampler = ClockSampler(local) if not e2e else None
+        if sampler:
+            sampler.start()
+            time.sleep(0.3)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        start.record()
+        for i in range(K):
+            step(W + i)
+        end.record()
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        if world > 1:
+            dist.barrier()
+        clocks = None
+        if sampler:
+            sampler.stop()
+            clocks = sampler.summary(t0, t1)
+        s1 = [l.stats() for l in layers]
+        for l in layers:
+            l.sync()
+            l.close()
+        el = _max_over_ranks(torch, dev, world, start.elapsed_time(end))
+        d = lambda f: sum(getattr(b, f) - getattr(a, f) for a, b in zip(s0, s1))
+        return {"ms_per_step": el / K, "hits": d("expert_hits"), "misses": d("expert_misses"),
+                "h2d_bytes": d("h2d_bytes"), "prefetched": d("prefetched"), "used": d("prefetch_used"),
+                "waves": d("waves"), "prefetch_calls": d("prefetch_calls"), "clocks": clocks}
+
+    plain = arm(False)
+    pref = arm(True)
+    e2e = arm(True, e2e=True)
+    if rank != 0:
+        return None
+    rb = lays[0].records.shape[1]
+    h2d_gbs = pref["h2d_bytes"] / K / (pref["ms_per_step"] / 1e3) / 1e9
+    res = _common(args, world, desc, shape, T, {
+        "layers": STACK_LAYERS, "slots_per_layer": STACK_PARTIAL_SLOTS, "cache_policy": "lru",
+        "l2": "expert copies stream from host memory every step (16 of 64 experts resident per layer)"})
+    res.update({
+        "value": replica_throughput(T, world, pref["ms_per_step"]), "ms_per_step": pref["ms_per_step"],
+        "roofline": {"bound": "h2d", "kernel": "expert record copies (host -> device)", "achieved": h2d_gbs,
+                     "peak": h2d_peak, "unit": "GB/s", "frac": h2d_gbs / h2d_peak,
+                     "peak_source": "measured in this run: pinned 1 GiB host -> device copies",
+                     "traffic": None, "h2d_bytes_per_step": pref["h2d_bytes"] / K},
+        "prefetch": {
+            "ms_per_step_without": plain["ms_per_step"], "ms_per_step_with": pref["ms_per_step"],
+            "speedup": plain["ms_per_step"] / pref["ms_per_step"],
+            "used_guess_rate": pref["used"] / max(1, pref["prefetched"]),
+            "guesses_copied_per_step": pref["prefetched"] / K, "guesses_used_per_step": pref["used"] / K,
+            "misses_per_step_without": plain["misses"] / K, "misses_per_step_with": pref["misses"] / K,
+            "hit_rate_without": plain["hits"] / max(1, plain["hits"] + plain["misses"]),
+            "hit_rate_with": pref["hits"] / max(1, pref["hits"] + pref["misses"]),
+            "h2d_mb_per_step_without": plain["h2d_bytes"] / K / 1e6,
+            "h2d_mb_per_step_with": pref["h2d_bytes"] / K / 1e6,
+            "record_mb": rb / 1e6},
+        "cpu_baseline": cpu_base,
+        "e2e": {"value": replica_throughput(T, world, e2e["ms_per_step"]), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * shape.hidden * 2, "d2h_bytes_per_step": T * shape.hidden * 2,
+                "path": "host x -> device, 16 x (moe_layer_forward + next layer's moe_layer_prefetch), "
+                        "last output -> host, next input formed on the host"},
+        "clocks": pref["clocks"],
+        # per forward: routing, per wave gate/up + down, combine; per prefetch: routing
+        "gpu_launches": int(STACK_LAYERS * K * 2 + 2 * pref["waves"] + pref["prefetch_calls"]),
+    })
+    return res
+
+
 def run_partial(args):
     """One layer whose experts live in a 32-slot device pool filled from
     pinned host memory: every forward routes, reads back the demanded set,
@@ -836,19 +999,7 @@ def run_partial(args):
     xs = [torch.from_numpy(synth.make_tokens(shape.hidden, T, seed=1000 * (rank + 1) + r)).to(dev) for r in range(4)]
     out = torch.empty_like(xs[0])
     # live peak of pinned host -> device copies (the bound of this workload)
-    hb = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
-    db = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
-    for _ in range(2):
-        db.copy_(hb, non_blocking=True)
-    torch.cuda.synchronize()
-    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    c0.record()
-    for _ in range(5):
-        db.copy_(hb, non_blocking=True)
-    c1.record()
-    torch.cuda.synchronize()
-    h2d_peak = 5 * (1 << 30) / (c0.elapsed_time(c1) / 1e3) / 1e9
-    del hb, db
+    h2d_peak = _h2d_peak(torch, dev)
     K, W = args.steps, args.warmup
     for i in range(W):
         ml.forward(xs[i % 4], out=out)
@@ -996,6 +1147,8 @@ def main():
         return
     if args.impl == "reference":
         res = run_reference(args)
+    elif args.workload == "olmoe-stack16-partial-t1":
+        res = run_stack_partial(args)
     elif args.workload.startswith("olmoe-stack"):
         res = run_stack(args)
     elif args.workload.startswith("gptoss-partial"):

@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 typedef enum {
   MOE_OK = 0,
@@ -133,8 +133,8 @@ typedef struct {
   uint64_t forward_calls;    /* forwards run (T > 0) */
   uint64_t tokens;           /* tokens processed */
   uint64_t expert_hits;      /* PARTIAL: demanded experts found resident */
-  uint64_t expert_misses;    /* PARTIAL: demanded experts copied host -> device */
-  uint64_t h2d_bytes;        /* PARTIAL: expert bytes copied host -> device */
+  uint64_t expert_misses;    /* PARTIAL: demanded experts not resident when their forward started */
+  uint64_t h2d_bytes;        /* PARTIAL: expert bytes copied host -> device (forwards and prefetches) */
   uint64_t d2h_expert_bytes; /* expert bytes copied device -> host: 0 by construction */
   uint64_t waves;            /* PARTIAL: expert-compute waves (transactions: one routed group each) */
   uint64_t generations;      /* PARTIAL: cache generations published (a group with misses publishes one) */
@@ -142,6 +142,9 @@ typedef struct {
   uint64_t staged_copies;    /* PARTIAL: records copied through the pinned staging buffers */
   int32_t faulted;           /* PARTIAL: 1 once a failure after publication has faulted the cache */
   int32_t reserved;
+  uint64_t prefetch_calls;   /* PARTIAL: moe_layer_prefetch calls that planned a guess */
+  uint64_t prefetched;       /* PARTIAL: experts a prefetch copied in */
+  uint64_t prefetch_used;    /* PARTIAL: of those, demanded by a later forward while resident (once each) */
 } moe_layer_stats_t;
 
 typedef struct {
@@ -201,7 +204,7 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
 moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* x_host, int32_t T, void* out_host,
                                     int32_t* topk_ids_host, float* topk_w_host, void* stream);
 
-/* Copies the routing of the last forward on this handle into device buffers
+/* Copies the routing of the last forward (or prefetch guess) on this handle into device buffers
  * (any may be NULL): counts int32 [E], offsets int32 [E+1] (exclusive prefix
  * sum of counts), perm int32 [T*k] (flat index t*k+j at each sorted position,
  * ascending flat index inside an expert), inv_perm int32 [T*k]. Asynchronous
@@ -260,6 +263,25 @@ moe_status_t moe_layer_get_stats(const moe_layer_t* layer, moe_layer_stats_t* st
  * registration). NULL is accepted and returns MOE_OK. Call after the last
  * forward has completed. */
 moe_status_t moe_layer_destroy(moe_layer_t* layer);
+
+/* moe-stream, "Findings" (prefetching: the next layer's router, run early on
+ * the current state, guesses that layer's experts; most guesses are used).
+ * Routes the guess input x (device FP16 [T][H], e.g. the previous layer's
+ * input while that layer runs) with this handle's router, on the handle's
+ * side stream once x is ready on `stream`, reads the guessed expert set back
+ * (waits for the guess's routing only, not for `stream`), and copies the
+ * guessed experts that are not resident into the pool on the side stream:
+ * the shared expert, then routed experts by guessed count (ties to the lower
+ * id), at most num_slots in all; resident ones stay; victims follow the
+ * cache policy and are overwritten only after their readers retire. The
+ * guess is published in the cache at once; a later forward that reads a
+ * row it filled waits for its copies on the forward's stream before the
+ * rows are used. Results of later forwards are identical with or without
+ * prefetches. Call it after the forward that precedes the guessed one has
+ * been enqueued on `stream` (its routing writes the handle's routing
+ * buffers). FULL residency: returns MOE_OK and does nothing. T = 0:
+ * MOE_OK. T > max_tokens -> INVALID_ARG; a faulted cache -> MOE_ERR_CUDA. */
+moe_status_t moe_layer_prefetch(moe_layer_t* layer, const void* x, int32_t T, void* stream);
 
 /* Routing without any device allocation, for callers that must not allocate
  * device memory (a host runtime that owns every device byte and forbids

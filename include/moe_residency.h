@@ -95,6 +95,17 @@ int32_t moe_expert_cache_row_of(const moe_expert_cache_t* cache, int32_t expert)
  * decays. Returns 0, or -1 on NULL. */
 int32_t moe_expert_cache_stats(const moe_expert_cache_t* cache, uint64_t* out5);
 
+/* A prefetch (moe-stream, "Findings": the next layer's router run early on
+ * the current state guesses its experts): the n distinct guessed experts
+ * (at most `capacity` are made resident; resident ones are kept) are planned
+ * as one transaction without counting accesses, and published. Returns the
+ * number of experts it loaded, or -1 on an invalid argument. */
+int32_t moe_expert_cache_prefetch(moe_expert_cache_t* cache, const int32_t* guessed, int32_t n);
+
+/* out2[0] = experts loaded by prefetches, out2[1] = those demanded by a
+ * later access while still resident (each counted once). */
+int32_t moe_expert_cache_prefetch_stats(const moe_expert_cache_t* cache, uint64_t* out2);
+
 /* NULL is accepted. */
 void moe_expert_cache_destroy(moe_expert_cache_t* cache);
 

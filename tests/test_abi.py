@@ -45,7 +45,7 @@ def test_every_declared_entry_point_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert lib.moe_abi_version() == 2
+    assert lib.moe_abi_version() == 3
 
 
 @pytest.mark.parametrize("H,I,G", [(256, 128, 64), (2048, 1024, 128), (2048, 512, 128), (2880, 2880, 128)])

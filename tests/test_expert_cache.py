@@ -199,3 +199,22 @@ def test_hit_rate_sweep_over_capacities(capsys):
         print("\nhit rate (top-4 of 128, Zipf 1.1, 1500 tokens) at capacity 16/32/48/64/128:")
         for name, r in rows.items():
             print(f"  {name:9s}" + " ".join(f"{v:6.3f}" for v in r))
+
+
+def test_prefetched_guesses_become_hits_and_are_counted():
+    # moe-stream, "Findings": the guessed experts are loaded early; a later
+    # access that demands them finds them resident. Exactly the guesses that
+    # are demanded before eviction count as used.
+    N, C = 64, 16
+    c = capi.ExpertCache(N, C, 4, capi.MOE_CACHE_LRU)
+    c.access(list(range(8)))
+    assert c.prefetch([20, 21, 22, 23, 3]) == 4  # 3 is resident already
+    assert c.stats()["misses"] == 8  # a prefetch is not an access
+    res = c.access([20, 21, 30, 3])
+    hit = dict(zip(res["experts"], res["hit"]))
+    assert hit == {20: 1, 21: 1, 30: 0, 3: 1}
+    assert c.prefetch_stats() == dict(prefetched=4, used=2)
+    c.access([20, 22])  # 20 counted once; 22 is a later use of a guess
+    assert c.prefetch_stats() == dict(prefetched=4, used=3)
+    with pytest.raises(ValueError):
+        c.prefetch([1, 1])

@@ -44,7 +44,8 @@ class moe_layer_stats_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "forward_calls", "tokens", "expert_hits", "expert_misses", "h2d_bytes",
         "d2h_expert_bytes", "waves", "generations", "evictions", "staged_copies")] + [
-        ("faulted", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+        ("faulted", ctypes.c_int32), ("reserved", ctypes.c_int32)] + [
+        (n, ctypes.c_uint64) for n in ("prefetch_calls", "prefetched", "prefetch_used")]
 
 
 class moe_layer_profile_t(ctypes.Structure):
@@ -73,6 +74,7 @@ PROTOTYPES = {
                                 ctypes.POINTER(_P)]),
     "moe_layer_forward": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
     "moe_layer_forward_host": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
+    "moe_layer_prefetch": (_I32, [_P, _P, _I32, _P]),
     "moe_layer_routing": (_I32, [_P, _P, _P, _P, _P, _P]),
     "moe_layer_sync": (_I32, [_P, _P]),
     "moe_layer_get_stats": (_I32, [_P, ctypes.POINTER(moe_layer_stats_t)]),
@@ -95,6 +97,8 @@ PROTOTYPES = {
                                        ctypes.POINTER(_I32), ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "moe_expert_cache_row_of": (_I32, [_P, _I32]),
     "moe_expert_cache_stats": (_I32, [_P, ctypes.POINTER(ctypes.c_uint64)]),
+    "moe_expert_cache_prefetch": (_I32, [_P, ctypes.POINTER(_I32), _I32]),
+    "moe_expert_cache_prefetch_stats": (_I32, [_P, ctypes.POINTER(ctypes.c_uint64)]),
     "moe_expert_cache_destroy": (None, [_P]),
 }
 
@@ -132,6 +136,19 @@ class ExpertCache:
 
     def row_of(self, e: int) -> int:
         return lib().moe_expert_cache_row_of(self.h, e)
+
+    def prefetch(self, guessed) -> int:
+        g = [int(e) for e in guessed]
+        arr = (_I32 * max(len(g), 1))(*g)
+        rc = lib().moe_expert_cache_prefetch(self.h, arr, len(g))
+        if rc < 0:
+            raise ValueError("invalid prefetch")
+        return rc
+
+    def prefetch_stats(self):
+        out = (ctypes.c_uint64 * 2)()
+        lib().moe_expert_cache_prefetch_stats(self.h, out)
+        return dict(prefetched=out[0], used=out[1])
 
     def stats(self):
         out = (ctypes.c_uint64 * 5)()
@@ -237,6 +254,10 @@ def moe_layer_forward(h, x, T, out, ids, w, stream) -> int:
 
 def moe_layer_forward_host(h, x, T, out, ids, w, stream) -> int:
     return lib().moe_layer_forward_host(h, x, T, out, ids, w, stream)
+
+
+def moe_layer_prefetch(h, x, T, stream) -> int:
+    return lib().moe_layer_prefetch(h, x, T, stream)
 
 
 def moe_layer_routing(h, counts, offsets, perm, inv_perm, stream) -> int:

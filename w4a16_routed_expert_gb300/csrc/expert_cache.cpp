@@ -16,6 +16,7 @@ ExpertCache::ExpertCache(int n_records, int capacity, int spares, CachePolicy po
       expert_row_(n_records, -1),
       freq_(n_records, 0.0),
       last_use_(n_records, 0),
+      guessed_(n_records, 0),
       capacity_(capacity),
       policy_(policy) {}
 
@@ -37,6 +38,10 @@ void ExpertCache::touch(int e, bool hit) {
   freq_[e] += 1.0;
   if (hit) {
     ++hits;
+    if (guessed_[e]) {
+      ++prefetch_used;
+      guessed_[e] = 0;
+    }
   } else {
     ++misses;
     if (policy_ == kCacheLRUFreq && ++misses_since_decay_ >= 2u * (uint64_t)capacity_) {
@@ -91,8 +96,11 @@ ExpertCache::Txn ExpertCache::next(const std::vector<int>& remaining, bool first
   return t;
 }
 
-void ExpertCache::publish(const Txn& t) {
+void ExpertCache::publish(const Txn& t) { publish(t, false); }
+
+void ExpertCache::publish(const Txn& t, bool prefetch) {
   for (const auto& v : t.evict) {
+    guessed_[v.first] = 0;
     expert_row_[v.first] = -1;
     row_pub_[v.second] = 0;
     row_expert_[v.second] = -1;
@@ -101,7 +109,9 @@ void ExpertCache::publish(const Txn& t) {
     row_expert_[l.second] = l.first;
     row_pub_[l.second] = 1;
     expert_row_[l.first] = l.second;
+    if (prefetch) guessed_[l.first] = 1;
   }
+  if (prefetch) prefetched += t.loads.size();
   evictions += t.evict.size();
   if (!t.loads.empty() || !t.evict.empty()) ++generation_;
 }
@@ -190,6 +200,24 @@ int32_t moe_expert_cache_stats(const moe_expert_cache_t* cache, uint64_t* out5) 
   out5[2] = cache->c.evictions;
   out5[3] = cache->c.generation();
   out5[4] = cache->c.decays;
+  return 0;
+}
+
+int32_t moe_expert_cache_prefetch(moe_expert_cache_t* cache, const int32_t* guessed, int32_t n) {
+  if (!cache || n < 0 || (n > 0 && !guessed)) return -1;
+  std::vector<int> g(guessed, guessed + n);
+  std::sort(g.begin(), g.end());
+  for (int i = 0; i < n; ++i)
+    if (g[i] < 0 || g[i] >= cache->c.n_records() || (i && g[i] == g[i - 1])) return -1;
+  const moe::ExpertCache::Txn t = cache->c.plan_prefetch(g);
+  cache->c.publish(t, true);
+  return (int32_t)t.loads.size();
+}
+
+int32_t moe_expert_cache_prefetch_stats(const moe_expert_cache_t* cache, uint64_t* out2) {
+  if (!cache || !out2) return -1;
+  out2[0] = cache->c.prefetched;
+  out2[1] = cache->c.prefetch_used;
   return 0;
 }
 

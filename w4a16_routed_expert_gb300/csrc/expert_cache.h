@@ -50,8 +50,15 @@ class ExpertCache {
   // (their contents untrusted).
   void abort(const Txn& t);
 
-  // Accounting of one demanded access (hit or miss) for the policies.
+  // Accounting of one demanded access (hit or miss) for the policies; a hit
+  // on an expert a prefetch loaded counts that guess as used.
   void touch(int expert, bool hit);
+
+  // A prefetch (moe-stream, "Findings": the next layer's router run early on
+  // the current state): the guessed experts as one transaction, planned like
+  // next() but without counting accesses; publish it with publish(t, true).
+  Txn plan_prefetch(const std::vector<int>& guessed) { return next(guessed, false); }
+  void publish(const Txn& t, bool prefetch);
 
   int row_of(int expert) const { return expert_row_[expert]; }        // published row or -1
   int expert_in(int row) const { return row_expert_[row]; }           // -1: spare / empty
@@ -63,6 +70,7 @@ class ExpertCache {
   CachePolicy policy() const { return policy_; }
 
   uint64_t hits = 0, misses = 0, evictions = 0, decays = 0;
+  uint64_t prefetched = 0, prefetch_used = 0;  // experts loaded by prefetches; of them, demanded while resident
 
  private:
   double score(int expert) const;  // lower = evicted first
@@ -71,6 +79,7 @@ class ExpertCache {
   std::vector<int> expert_row_;    // published row of an expert, -1 none
   std::vector<double> freq_;       // per expert: accesses (LFU) or decayed frequency (LRU-FREQ)
   std::vector<uint64_t> last_use_; // per expert: clock of the last access
+  std::vector<char> guessed_;      // per expert: loaded by a prefetch, not demanded since
   uint64_t clock_ = 0;
   uint64_t generation_ = 0;
   uint64_t misses_since_decay_ = 0;

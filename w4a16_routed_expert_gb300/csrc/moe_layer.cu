@@ -745,6 +745,30 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
   return MOE_OK;
 }
 
+moe_status_t moe_layer_prefetch(moe_layer_t* layer, const void* x, int32_t T, void* stream) {
+  if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");
+  if (T < 0 || T > layer->cfg.max_tokens)
+    return fail(MOE_ERR_INVALID_ARG, "T=%d out of 0..max_tokens=%d", T, layer->cfg.max_tokens);
+  if (layer->cfg.residency == MOE_RESIDENCY_FULL || T == 0) return MOE_OK;
+  if (!x) return fail(MOE_ERR_INVALID_ARG, "x must not be NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t side = moe::residency_side(layer->res);
+  cudaEvent_t ready = moe::residency_input_event(layer->res);
+  cudaError_t e = cudaEventRecord(ready, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, ready, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "prefetch input dependency");
+  // the guess is routed like a forward's tokens, without profiling events
+  // and without a programmatic dependency on the side stream's last copy
+  const bool pdl_saved = layer->pdl, prof_saved = layer->profiling;
+  layer->pdl = false;
+  layer->profiling = false;
+  moe_status_t st = enqueue_route(layer, static_cast<const __half*>(x), T, nullptr, nullptr, side);
+  layer->pdl = pdl_saved;
+  layer->profiling = prof_saved;
+  if (st != MOE_OK) return st;
+  return moe::residency_prefetch(layer->res, layer, T);
+}
+
 moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* x_host, int32_t T, void* out_host,
                                     int32_t* topk_ids_host, float* topk_w_host, void* stream) {
   if (!layer) return fail(MOE_ERR_INVALID_ARG, "layer must not be NULL");

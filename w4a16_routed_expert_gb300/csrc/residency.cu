@@ -76,6 +76,13 @@ struct Residency {
   bool faulted = false;
   CodeMaps maps = {};  // tensor maps of the pool (tensor-core path)
   bool maps_tried = false;
+  // prefetch (moe-stream, "Findings"): the guess is routed on the side
+  // stream once its input is ready (ev_x); its copies complete at ev_pref;
+  // a forward that reads a row the prefetch filled waits on ev_pref first
+  cudaEvent_t ev_x = nullptr, ev_pref = nullptr;
+  std::vector<char> row_prefetched;
+  int32_t* h_guess = nullptr;
+  uint64_t prefetch_calls = 0;
   uint64_t waves = 0, h2d_bytes = 0, staged = 0;
   Residency(int n, int cap, int spares, CachePolicy p) : cache(n, cap, spares, p) {}
 };
@@ -91,6 +98,9 @@ void residency_destroy(Residency* r) {
     if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : r->ev_staging)
     if (e) cudaEventDestroy(e);
+  if (r->ev_x) cudaEventDestroy(r->ev_x);
+  if (r->ev_pref) cudaEventDestroy(r->ev_pref);
+  if (r->h_guess) cudaFreeHost(r->h_guess);
   for (uint8_t* p : r->staging)
     if (p) cudaFreeHost(p);
   if (r->side) cudaStreamDestroy(r->side);
@@ -119,6 +129,7 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
   r->max_txn = (n_records + cfg.num_slots - 1) / cfg.num_slots + 1;
   r->tbl_ints = (int)((4 * (size_t)n_records + 1 + 63) / 64 * 64);
   r->row_reader.assign(r->rows, -1);
+  r->row_prefetched.assign(r->rows, 0);
   const char* inj = getenv("MOE_FAULT_INJECT");
   if (inj && strcmp(inj, "h2d_fail") == 0) r->inject = 1;
   if (inj && strcmp(inj, "after_publish") == 0) r->inject = 2;
@@ -154,6 +165,11 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
     g_res_err = "side stream creation failed";
     st = MOE_ERR_CUDA;
   }
+  if (st == MOE_OK && (cudaEventCreateWithFlags(&r->ev_x, cudaEventDisableTiming) != cudaSuccess ||
+                       cudaEventCreateWithFlags(&r->ev_pref, cudaEventDisableTiming) != cudaSuccess)) {
+    g_res_err = "event creation failed";
+    st = MOE_ERR_CUDA;
+  }
   if (st == MOE_OK) {
     r->ev_done.assign(r->max_txn, nullptr);
     r->ev_ready.assign(r->max_txn, nullptr);
@@ -168,6 +184,7 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
   if (st == MOE_OK) {
     const size_t tb = (size_t)r->max_txn * r->tbl_ints * sizeof(int32_t);
     if (cudaHostAlloc(&r->h_counts, (size_t)cfg.num_experts * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc(&r->h_guess, (size_t)cfg.num_experts * sizeof(int32_t), cudaHostAllocDefault) != cudaSuccess ||
         cudaHostAlloc(&r->h_tbl, tb, cudaHostAllocDefault) != cudaSuccess ||
         cudaMalloc(&r->d_tbl, tb) != cudaSuccess) {
       g_res_err = "residency table allocation failed";
@@ -281,6 +298,17 @@ moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int 
         return set_error(MOE_ERR_CUDA, "expert copy host->device: %s", cudaGetErrorString(e));
       }
     }
+    // rows a prefetch filled are read only after its copies completed
+    bool reads_prefetched = false;
+    for (int row : t.rows) reads_prefetched = reads_prefetched || r->row_prefetched[row];
+    if (reads_prefetched) {
+      e = cudaStreamWaitEvent(s, r->ev_pref, 0);
+      if (e != cudaSuccess) {
+        r->cache.abort(t);
+        return set_error(MOE_ERR_CUDA, "prefetch dependency: %s", cudaGetErrorString(e));
+      }
+      std::fill(r->row_prefetched.begin(), r->row_prefetched.end(), 0);
+    }
     // publication on the forward's stream, after the copies completed
     int32_t* dtbl = r->d_tbl + (size_t)ti * r->tbl_ints;
     e = cudaMemcpyAsync(dtbl, tbl, (size_t)r->tbl_ints * sizeof(int32_t), cudaMemcpyHostToDevice, s);
@@ -316,6 +344,49 @@ moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int 
   return enqueue_combine(L, x, T, out, s);
 }
 
+cudaStream_t residency_side(Residency* r) { return r->side; }
+cudaEvent_t residency_input_event(Residency* r) { return r->ev_x; }
+
+moe_status_t residency_prefetch(Residency* r, moe_layer* L, int T) {
+  const moe_layer_config_t& c = L->cfg;
+  const int E = c.num_experts, k = c.top_k;
+  if (r->faulted)
+    return set_error(MOE_ERR_CUDA, "the expert cache is faulted (a failure after publication); destroy the handle");
+  // the guess's expert counts (routed on the side stream by the caller)
+  cudaError_t e = cudaMemcpyAsync(r->h_guess, L->counts, (size_t)E * sizeof(int32_t), cudaMemcpyDeviceToHost, r->side);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(r->side);
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "guess counts device->host: %s", cudaGetErrorString(e));
+  // the guessed experts: the shared one (demanded by every forward), then the
+  // routed ones by count (ties to the lower id), as many as fit
+  std::vector<int> order;
+  int run = 0;
+  for (int i = 0; i < E; ++i) {
+    run += r->h_guess[i];
+    if (r->h_guess[i] > 0) order.push_back(i);
+  }
+  if (run != T * k) return set_error(MOE_ERR_INTERNAL, "guess counts sum to %d, expected %d", run, T * k);
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return r->h_guess[a] > r->h_guess[b]; });
+  std::vector<int> guessed;
+  if (c.has_shared_expert) guessed.push_back(E);
+  for (int ex : order)
+    if ((int)guessed.size() < r->num_slots) guessed.push_back(ex);
+  const ExpertCache::Txn t = r->cache.plan_prefetch(guessed);
+  r->prefetch_calls += 1;
+  if (t.loads.empty()) return MOE_OK;
+  for (size_t j = 0; j < t.loads.size() && e == cudaSuccess; ++j) e = transport(r, t.loads[j].first, t.loads[j].second);
+  if (e == cudaSuccess) e = cudaEventRecord(r->ev_pref, r->side);
+  if (e != cudaSuccess) {
+    r->cache.abort(t);
+    return set_error(MOE_ERR_CUDA, "prefetch copy host->device: %s", cudaGetErrorString(e));
+  }
+  // published in the host model now; a forward reading these rows waits on
+  // ev_pref before its table (the device-side publication) is uploaded
+  r->cache.publish(t, true);
+  for (const auto& l : t.loads) r->row_prefetched[l.second] = 1;
+  r->h2d_bytes += (uint64_t)t.loads.size() * r->rb;
+  return MOE_OK;
+}
+
 void residency_fill_stats(const Residency* r, moe_layer_stats_t* st) {
   st->expert_hits = r->cache.hits;
   st->expert_misses = r->cache.misses;
@@ -326,6 +397,9 @@ void residency_fill_stats(const Residency* r, moe_layer_stats_t* st) {
   st->evictions = r->cache.evictions;
   st->staged_copies = r->staged;
   st->faulted = r->faulted ? 1 : 0;
+  st->prefetch_calls = r->prefetch_calls;
+  st->prefetched = r->cache.prefetched;
+  st->prefetch_used = r->cache.prefetch_used;
 }
 
 }  // namespace moe

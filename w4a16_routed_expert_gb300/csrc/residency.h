@@ -18,5 +18,11 @@ void residency_destroy(Residency* r);
 const char* residency_last_error();
 moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s);
 void residency_fill_stats(const Residency* r, moe_layer_stats_t* st);
+// Prefetch: the side stream the guess is routed on, the event the caller
+// records once the guess input is ready, and the planning + copies that
+// follow the guess's routing (already enqueued on the side stream).
+cudaStream_t residency_side(Residency* r);
+cudaEvent_t residency_input_event(Residency* r);
+moe_status_t residency_prefetch(Residency* r, moe_layer* L, int T);
 
 }  // namespace moe

@@ -70,6 +70,12 @@ class MoELayer:
                    "moe_layer_forward_host")
         return out_host
 
+    def prefetch(self, x: torch.Tensor, stream=None):
+        """Guess this layer's experts from x (e.g. the previous layer's input)
+        and start copying them into the pool (partial residency only)."""
+        capi.check(capi.moe_layer_prefetch(self.handle, _ptr(x), x.shape[0], _stream_handle(stream)),
+                   "moe_layer_prefetch")
+
     def routing(self, T: int, stream=None):
         dev = torch.device("cuda")
         E, k = self.num_experts, self.top_k
