@@ -267,19 +267,22 @@ moe_status_t moe_layer_destroy(moe_layer_t* layer);
 /* moe-stream, "Findings" (prefetching: the next layer's router, run early on
  * the current state, guesses that layer's experts; most guesses are used).
  * Routes the guess input x (device FP16 [T][H], e.g. the previous layer's
- * input while that layer runs) with this handle's router, on the handle's
- * side stream once x is ready on `stream`, reads the guessed expert set back
- * (waits for the guess's routing only, not for `stream`), and copies the
+ * input while that layer runs) with this handle's router on the handle's
+ * side stream once x is ready on `stream`, and returns without waiting. A
+ * thread the handle owns waits for the guess's expert counts and copies the
  * guessed experts that are not resident into the pool on the side stream:
  * the shared expert, then routed experts by guessed count (ties to the lower
  * id), at most num_slots in all; resident ones stay; victims follow the
  * cache policy and are overwritten only after their readers retire. The
- * guess is published in the cache at once; a later forward that reads a
- * row it filled waits for its copies on the forward's stream before the
- * rows are used. Results of later forwards are identical with or without
- * prefetches. Call it after the forward that precedes the guessed one has
- * been enqueued on `stream` (its routing writes the handle's routing
- * buffers). FULL residency: returns MOE_OK and does nothing. T = 0:
+ * guess is published in the cache; a later forward that reads a row it
+ * filled waits (on the forward's stream) for its copies before using it.
+ * Results of later forwards are identical with or without prefetches. The
+ * handle's next forward orders its routing after the guess's (they share
+ * the handle's routing buffers) and waits for the thread's planning before
+ * its own; a failure of that planning (its copies aborted, the previous
+ * generation kept) is returned once, by that forward, as MOE_ERR_CUDA.
+ * Call it after the forward that precedes the guessed one has been enqueued
+ * on `stream`. FULL residency: returns MOE_OK and does nothing. T = 0:
  * MOE_OK. T > max_tokens -> INVALID_ARG; a faulted cache -> MOE_ERR_CUDA. */
 moe_status_t moe_layer_prefetch(moe_layer_t* layer, const void* x, int32_t T, void* stream);
 

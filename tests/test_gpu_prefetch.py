@@ -146,3 +146,24 @@ def test_prefetch_edge_cases():
     capi.check(capi.moe_layer_prefetch(f.handle, x.data_ptr(), 8, None), "prefetch")
     assert f.stats().prefetch_calls == 0
     f.close()
+
+
+def test_a_failed_prefetch_is_reported_once_and_leaves_the_cache_consistent(monkeypatch):
+    # host-side injection: the planning thread aborts the guess's copies
+    # before publication; the next forward reports it, the one after is
+    # correct and nothing the guess would have loaded became resident
+    monkeypatch.setenv("MOE_FAULT_INJECT", "prefetch_fail")
+    shape = synth.LayerShape(256, 256, 16, 2, 64, True)
+    lay = synth.make_layer(shape, seed=34, codes="uniform")
+    m = _partial(lay, 6, 4)
+    x = synth.make_tokens(shape.hidden, 4, seed=34)
+    m.prefetch(torch.from_numpy(x).cuda())
+    with pytest.raises(capi.MoEError) as ei:
+        GH.run(m, x)
+    assert ei.value.status == capi.MOE_ERR_CUDA and "prefetch" in str(ei.value)
+    st = m.stats()
+    assert st.prefetch_calls == 1 and st.prefetched == 0 and st.h2d_bytes == 0
+    g = GH.run(m, x)
+    GH.compare(lay, x, g)
+    assert m.stats().faulted == 0
+    m.close()

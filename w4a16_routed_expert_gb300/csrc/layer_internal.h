@@ -16,6 +16,16 @@ struct Residency;
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// A stage-timing event: inside a stream capture it becomes an external
+// event node of the graph (so replays record it); outside, a plain record.
+inline void prof_record(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
+
 struct Layout {
   size_t off[6];
   size_t size[6];

@@ -342,7 +342,7 @@ moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, 
   ga.stats = L->gemm_stats;
   e = launch_gemm(true, maps->gate, maps->up, L->xs_map, ga, L->num_sms, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up GEMM launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[2], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[2], s);
   GemmArgs gb = ga;
   gb.s_off0 = L->lay.off[5];
   gb.s_off1 = L->lay.off[5];
@@ -354,7 +354,7 @@ moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, 
   gb.stats = L->gemm_stats ? L->gemm_stats + (size_t)L->num_sms * kGemmStats : nullptr;
   e = launch_gemm(false, maps->down, maps->down, L->h_map, gb, L->num_sms, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down GEMM launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[3], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[3], s);
   return MOE_OK;
 }
 
@@ -419,7 +419,7 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   const int grid_g = std::max(1, std::min(L->num_sms, max_seg * nrb_g));
   cudaError_t e = launch_tcgemv(p, true, grid_g, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "gate/up launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[2], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[2], s);
 
   TcGemvLaunch q = p;
   TcGemvArgs& b = q.a;
@@ -454,7 +454,7 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   const int grid_d = std::max(1, std::min(L->num_sms, max_seg * nrb_d));
   e = launch_tcgemv(q, false, grid_d, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "down launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[3], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[3], s);
   return MOE_OK;
 }
 
@@ -553,11 +553,11 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   const size_t fixed = decode_smem_bytes(a, 0);
   if (fixed + 2 * (size_t)a.slot_bytes > kSmemBudget) return MOE_ERR_UNSUPPORTED;
   a.stages = (int)std::min<size_t>(kDecodeMaxStages, (kSmemBudget - fixed) / a.slot_bytes);
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[0], s);
   if (L->trace) cudaMemsetAsync(L->trace, 0, (size_t)L->num_sms * moe::kTraceStamps * 8, s);
   cudaError_t e = launch_decode(a, L->num_sms, s, L->pdl && L->decode_pdl);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[4], s);
   L->last_single = true;
   return MOE_OK;
 }
@@ -614,11 +614,11 @@ moe_status_t enqueue_decode1(moe_layer* L, const __half* x, __half* out, int32_t
   a.max_units_d = (H / 16 + grid - 1) / grid;
   a.max_rows_rt = (E + grid - 1) / grid;
   if (decode1_smem_bytes(a) == 0) return MOE_ERR_UNSUPPORTED;
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[0], s);
   // (every CTA rewrites its stamps on every launch: no clearing launch)
   cudaError_t e = launch_decode1(a, grid, s, L->pdl && L->decode_pdl);
   if (e != cudaSuccess) return cuda_fail(e, "batch-1 decode launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[4], s);
   L->last_single = true;
   return MOE_OK;
 }
@@ -636,7 +636,7 @@ moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, 
   ca.has_shared = c.has_shared_expert;
   cudaError_t e = launch_combine(ca, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[4], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[4], s);
   return MOE_OK;
 }
 
@@ -676,11 +676,11 @@ moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_us
   ra.err = L->err;
   const bool small = T <= moe::kSmallRouteMaxT && (size_t)T * c.hidden * 2 <= 200 * 1024;
   if (!small) ra.nsplit = moe::router_split(T, c.num_experts, c.hidden, L->num_sms);
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[0], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[0], s);
   L->last_single = false;
   cudaError_t e = small ? moe::launch_route_small(ra, s, L->pdl) : moe::launch_route_large(ra, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "routing launch");
-  if (L->profiling) cudaEventRecordWithFlags(L->ev[1], s, cudaEventRecordExternal);
+  if (L->profiling) prof_record(L->ev[1], s);
   return MOE_OK;
 }
 
@@ -721,6 +721,13 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
       layer->stats.forward_calls += 1;
       layer->stats.tokens += (uint64_t)T;
       return MOE_OK;
+    }
+  }
+  if (layer->res) {
+    const cudaError_t e = moe::residency_before_route(layer->res, s);
+    if (e != cudaSuccess) {
+      layer->pdl = pdl_saved;
+      return cuda_fail(e, "ordering after a prefetch guess");
     }
   }
   moe_status_t st = enqueue_route(layer, xh, T, topk_ids, topk_w, s);

@@ -33,10 +33,14 @@
 // side stream and the expert kernels to the caller's stream. With spare rows
 // the next transaction's copies stream while the current one computes.
 #include <algorithm>
+#include <condition_variable>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <string>
+#include <thread>
 #include <vector>
 
 #include "expert_cache.h"
@@ -72,17 +76,28 @@ struct Residency {
   int32_t* h_counts = nullptr;
   int32_t* h_tbl = nullptr;
   int32_t* d_tbl = nullptr;
-  int inject = 0;  // host-side fault injection: 1 before publication, 2 after (one-shot)
+  int inject = 0;  // host-side fault injection (one-shot): 1 before publication, 2 after, 3 in a prefetch
   bool faulted = false;
   CodeMaps maps = {};  // tensor maps of the pool (tensor-core path)
   bool maps_tried = false;
   // prefetch (moe-stream, "Findings"): the guess is routed on the side
-  // stream once its input is ready (ev_x); its copies complete at ev_pref;
-  // a forward that reads a row the prefetch filled waits on ev_pref first
-  cudaEvent_t ev_x = nullptr, ev_pref = nullptr;
+  // stream once its input is ready (ev_x) and its counts read back (ev_guess);
+  // a worker thread plans it and issues its copies, complete at ev_pref; a
+  // forward that reads a row the prefetch filled waits on ev_pref first
+  cudaEvent_t ev_x = nullptr, ev_guess = nullptr, ev_pref = nullptr;
   std::vector<char> row_prefetched;
   int32_t* h_guess = nullptr;
   uint64_t prefetch_calls = 0;
+  bool guess_enqueued = false;  // a guess's routing is on the side stream (caller's thread only)
+  int device = 0;
+  std::thread worker;
+  std::mutex mu;
+  std::condition_variable cv;
+  bool stop = false, pending = false;  // under mu
+  int pending_T = 0;
+  moe_layer* pending_L = nullptr;
+  moe_status_t async_st = MOE_OK;  // failure of the last background planning, reported once
+  std::string async_msg;
   uint64_t waves = 0, h2d_bytes = 0, staged = 0;
   Residency(int n, int cap, int spares, CachePolicy p) : cache(n, cap, spares, p) {}
 };
@@ -91,6 +106,14 @@ const char* residency_last_error() { return g_res_err; }
 
 void residency_destroy(Residency* r) {
   if (!r) return;
+  if (r->worker.joinable()) {
+    {
+      std::lock_guard<std::mutex> lk(r->mu);
+      r->stop = true;
+    }
+    r->cv.notify_all();
+    r->worker.join();
+  }
   if (r->side) cudaStreamSynchronize(r->side);
   for (cudaEvent_t e : r->ev_done)
     if (e) cudaEventDestroy(e);
@@ -99,6 +122,7 @@ void residency_destroy(Residency* r) {
   for (cudaEvent_t e : r->ev_staging)
     if (e) cudaEventDestroy(e);
   if (r->ev_x) cudaEventDestroy(r->ev_x);
+  if (r->ev_guess) cudaEventDestroy(r->ev_guess);
   if (r->ev_pref) cudaEventDestroy(r->ev_pref);
   if (r->h_guess) cudaFreeHost(r->h_guess);
   for (uint8_t* p : r->staging)
@@ -133,6 +157,7 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
   const char* inj = getenv("MOE_FAULT_INJECT");
   if (inj && strcmp(inj, "h2d_fail") == 0) r->inject = 1;
   if (inj && strcmp(inj, "after_publish") == 0) r->inject = 2;
+  if (inj && strcmp(inj, "prefetch_fail") == 0) r->inject = 3;
 
   moe_status_t st = MOE_OK;
   cudaError_t e = cudaMalloc(&r->pool, (size_t)r->rows * record_bytes);
@@ -165,7 +190,12 @@ moe_status_t residency_create(const moe_layer_config_t& cfg, size_t record_bytes
     g_res_err = "side stream creation failed";
     st = MOE_ERR_CUDA;
   }
+  if (st == MOE_OK && cudaGetDevice(&r->device) != cudaSuccess) {
+    g_res_err = "no current device";
+    st = MOE_ERR_CUDA;
+  }
   if (st == MOE_OK && (cudaEventCreateWithFlags(&r->ev_x, cudaEventDisableTiming) != cudaSuccess ||
+                       cudaEventCreateWithFlags(&r->ev_guess, cudaEventDisableTiming) != cudaSuccess ||
                        cudaEventCreateWithFlags(&r->ev_pref, cudaEventDisableTiming) != cudaSuccess)) {
     g_res_err = "event creation failed";
     st = MOE_ERR_CUDA;
@@ -227,6 +257,12 @@ cudaError_t transport(Residency* r, int expert, int row) {
   return e;
 }
 
+// Waits until no prefetch is being planned on the worker thread.
+void join_prefetch(Residency* r) {
+  std::unique_lock<std::mutex> lk(r->mu);
+  r->cv.wait(lk, [&] { return !r->pending; });
+}
+
 }  // namespace
 
 moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s) {
@@ -252,6 +288,15 @@ moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int 
   }
   if (run != T * k) return set_error(MOE_ERR_INTERNAL, "expert counts sum to %d, expected %d", run, T * k);
   if (c.has_shared_expert) demanded.push_back(E);
+  // a prefetch planned on the worker thread finishes before this forward
+  // plans; its failure (its transaction aborted, the cache consistent) is
+  // reported here, once
+  join_prefetch(r);
+  if (r->async_st != MOE_OK) {
+    const moe_status_t ast = r->async_st;
+    r->async_st = MOE_OK;
+    return set_error(ast, "prefetch: %s", r->async_msg.c_str());
+  }
 
   // every access is counted (ascending id): a hit is an expert published
   // when the forward starts
@@ -347,15 +392,16 @@ moe_status_t residency_forward(Residency* r, moe_layer* L, const __half* x, int 
 cudaStream_t residency_side(Residency* r) { return r->side; }
 cudaEvent_t residency_input_event(Residency* r) { return r->ev_x; }
 
-moe_status_t residency_prefetch(Residency* r, moe_layer* L, int T) {
+namespace {
+
+// The guess's planning (worker thread): wait for its expert counts, pick
+// the guessed experts, copy the missing ones into the pool on the side
+// stream, publish them in the host model.
+moe_status_t plan_prefetch(Residency* r, moe_layer* L, int T) {
   const moe_layer_config_t& c = L->cfg;
   const int E = c.num_experts, k = c.top_k;
-  if (r->faulted)
-    return set_error(MOE_ERR_CUDA, "the expert cache is faulted (a failure after publication); destroy the handle");
-  // the guess's expert counts (routed on the side stream by the caller)
-  cudaError_t e = cudaMemcpyAsync(r->h_guess, L->counts, (size_t)E * sizeof(int32_t), cudaMemcpyDeviceToHost, r->side);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(r->side);
-  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "guess counts device->host: %s", cudaGetErrorString(e));
+  cudaError_t e = cudaEventSynchronize(r->ev_guess);
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "guess routing: %s", cudaGetErrorString(e));
   // the guessed experts: the shared one (demanded by every forward), then the
   // routed ones by count (ties to the lower id), as many as fit
   std::vector<int> order;
@@ -371,8 +417,13 @@ moe_status_t residency_prefetch(Residency* r, moe_layer* L, int T) {
   for (int ex : order)
     if ((int)guessed.size() < r->num_slots) guessed.push_back(ex);
   const ExpertCache::Txn t = r->cache.plan_prefetch(guessed);
-  r->prefetch_calls += 1;
   if (t.loads.empty()) return MOE_OK;
+  if (r->inject == 3) {
+    // injected failure before publication: the previous generation stays
+    r->inject = 0;
+    r->cache.abort(t);
+    return set_error(MOE_ERR_CUDA, "injected prefetch copy failure before publication");
+  }
   for (size_t j = 0; j < t.loads.size() && e == cudaSuccess; ++j) e = transport(r, t.loads[j].first, t.loads[j].second);
   if (e == cudaSuccess) e = cudaEventRecord(r->ev_pref, r->side);
   if (e != cudaSuccess) {
@@ -387,7 +438,60 @@ moe_status_t residency_prefetch(Residency* r, moe_layer* L, int T) {
   return MOE_OK;
 }
 
-void residency_fill_stats(const Residency* r, moe_layer_stats_t* st) {
+void worker_main(Residency* r) {
+  cudaSetDevice(r->device);
+  std::unique_lock<std::mutex> lk(r->mu);
+  for (;;) {
+    r->cv.wait(lk, [&] { return r->stop || r->pending; });
+    if (r->pending) {
+      lk.unlock();
+      const moe_status_t st = plan_prefetch(r, r->pending_L, r->pending_T);
+      lk.lock();
+      if (st != MOE_OK) {
+        r->async_st = st;
+        r->async_msg = moe_layer_last_error(nullptr);
+      }
+      r->pending = false;
+      r->cv.notify_all();
+      continue;
+    }
+    return;
+  }
+}
+
+}  // namespace
+
+cudaError_t residency_before_route(Residency* r, cudaStream_t s) {
+  if (!r->guess_enqueued) return cudaSuccess;
+  r->guess_enqueued = false;
+  return cudaStreamWaitEvent(s, r->ev_guess, 0);
+}
+
+moe_status_t residency_prefetch(Residency* r, moe_layer* L, int T) {
+  const int E = L->cfg.num_experts;
+  join_prefetch(r);
+  if (r->faulted)
+    return set_error(MOE_ERR_CUDA, "the expert cache is faulted (a failure after publication); destroy the handle");
+  // the guess's expert counts come back on the side stream; the worker
+  // thread plans the copies once they are there
+  cudaError_t e = cudaMemcpyAsync(r->h_guess, L->counts, (size_t)E * sizeof(int32_t), cudaMemcpyDeviceToHost, r->side);
+  if (e == cudaSuccess) e = cudaEventRecord(r->ev_guess, r->side);
+  if (e != cudaSuccess) return set_error(MOE_ERR_CUDA, "guess counts device->host: %s", cudaGetErrorString(e));
+  r->guess_enqueued = true;
+  r->prefetch_calls += 1;
+  {
+    std::lock_guard<std::mutex> lk(r->mu);
+    r->pending = true;
+    r->pending_T = T;
+    r->pending_L = L;
+    if (!r->worker.joinable()) r->worker = std::thread(worker_main, r);
+  }
+  r->cv.notify_all();
+  return MOE_OK;
+}
+
+void residency_fill_stats(Residency* r, moe_layer_stats_t* st) {
+  join_prefetch(r);
   st->expert_hits = r->cache.hits;
   st->expert_misses = r->cache.misses;
   st->h2d_bytes = r->h2d_bytes;
