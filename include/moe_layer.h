@@ -233,7 +233,11 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* prof
  * computed (consumer warp 0), 17 the CTA's h written, 18 every CTA's h
  * seen, 19 / 21 down inputs staged by consumer warp 0 / the last consumer
  * warp, 20 / 22 their down work done, 23 all down partials done, 24 output
- * rows written, 25 exit. Small-batch kernel (2..16 tokens): 0 entry, 1 own
+ * rows written, 25 exit. Stack kernel (moe_stack_forward at one token):
+ * the same stamps for one layer (the second of the stack, the first if it
+ * is alone), in the first layer's buffer; 0 is that layer's entry (the
+ * end of the layer before), 2 the partial logits and the input loaded.
+ * Small-batch kernel (2..16 tokens): 0 entry, 1 own
  * logit partials written, 2 all partials seen, 3 top-k done, 4 routing
  * done, 5 first gate/up item started, 6 last gate/up item done, 7 first down
  * item started, 8 consumers done, 9 finisher done, 10 all warps done, 11
@@ -263,6 +267,39 @@ moe_status_t moe_layer_get_stats(const moe_layer_t* layer, moe_layer_stats_t* st
  * registration). NULL is accepted and returns MOE_OK. Call after the last
  * forward has completed. */
 moe_status_t moe_layer_destroy(moe_layer_t* layer);
+
+/* Stacked layers: the residual stream of a decoder's MoE layers, the layer
+ * of Horizon RunMap report, "The complete execution path", steps 2-3, run
+ * once per layer. A stack borrows n_layers (>= 1) layer handles that map
+ * H -> H (they must outlive it) and runs x_{l+1} = layer_l(x_l) for
+ * l = 0..n_layers-1 on one stream, each layer with its own configuration
+ * (add_residual included); out = x_{n_layers}.
+ *   x       device FP16 [T][H], read only
+ *   out     device FP16 [T][H]; must overlap neither x nor states
+ *   states  device FP16 [n_layers - 1][T][H] receiving x_1 .. x_{n_layers-1}
+ *           (the inputs of layers 1.., e.g. for checking each layer), or NULL
+ * T <= the smallest max_tokens of the layers. One token over fully
+ * resident layers of one shape (H, I, E <= 128, k, G, shared expert) runs as
+ * a single cooperative launch (moe_stack_single_launch reports it; set
+ * MOE_STACK1=0 before create to turn it off): one grid-wide step per layer
+ * boundary instead of a launch. There each layer's router logits are summed
+ * from per-CTA partials over the rows of its input in a fixed order (not
+ * the order of a layer's own forward), so its FP32 logits may differ from
+ * that forward's in the last bits; results are repeatable bit for bit.
+ * Otherwise the layers' own forwards run one after another. Routing of the
+ * last stack forward is read per layer with moe_layer_routing; every layer's
+ * forward counters advance. Asynchronous; no allocation after create;
+ * graph-capturable when every layer's forward is. moe_stack_sync reports
+ * device-side failures (MOE_ERR_TIMEOUT) of the stack kernel and of every
+ * layer. */
+typedef struct moe_stack moe_stack_t;
+moe_status_t moe_stack_create(moe_layer_t* const* layers, int32_t n_layers, moe_stack_t** out);
+moe_status_t moe_stack_forward(moe_stack_t* stack, const void* x, int32_t T, void* out, void* states,
+                               void* stream);
+moe_status_t moe_stack_sync(moe_stack_t* stack, void* stream);
+int32_t moe_stack_single_launch(const moe_stack_t* stack);
+/* NULL is accepted. Call after the last forward has completed. */
+moe_status_t moe_stack_destroy(moe_stack_t* stack);
 
 /* moe-stream, "Findings" (prefetching: the next layer's router, run early on
  * the current state, guesses that layer's experts; most guesses are used).

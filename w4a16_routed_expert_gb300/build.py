@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w4a16.so")
-SOURCES = ["route.cu", "route_static.cu", "gemv.cu", "decode.cu", "decode1.cu", "gemm.cu", "moe_layer.cu", "residency.cu", "slot_planner.cpp", "expert_cache.cpp"]
+SOURCES = ["route.cu", "route_static.cu", "gemv.cu", "decode.cu", "decode1.cu", "gemm.cu", "moe_layer.cu", "stack.cu", "residency.cu", "slot_planner.cpp", "expert_cache.cpp"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + [

@@ -75,6 +75,11 @@ PROTOTYPES = {
     "moe_layer_forward": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
     "moe_layer_forward_host": (_I32, [_P, _P, _I32, _P, _P, _P, _P]),
     "moe_layer_prefetch": (_I32, [_P, _P, _I32, _P]),
+    "moe_stack_create": (_I32, [ctypes.POINTER(_P), _I32, ctypes.POINTER(_P)]),
+    "moe_stack_forward": (_I32, [_P, _P, _I32, _P, _P, _P]),
+    "moe_stack_sync": (_I32, [_P, _P]),
+    "moe_stack_single_launch": (_I32, [_P]),
+    "moe_stack_destroy": (_I32, [_P]),
     "moe_layer_routing": (_I32, [_P, _P, _P, _P, _P, _P]),
     "moe_layer_sync": (_I32, [_P, _P]),
     "moe_layer_get_stats": (_I32, [_P, ctypes.POINTER(moe_layer_stats_t)]),

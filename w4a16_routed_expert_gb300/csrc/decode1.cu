@@ -59,6 +59,7 @@ __host__ __device__ constexpr uint32_t r16(uint32_t v) { return (v + 15u) & ~15u
 
 struct D1Layout {
   uint32_t gcode, dcode, gsc, dsc, xb, xc, hb, hc, redg, redd, y, rpart, e2s, keys, cand, route, bars, ctl, total;
+  uint32_t lgs, xo, wsl, sub, wstride;  // stack kernel: logits, output rows, next router slice, partial sums
   uint32_t ug, ud;  // bytes of one 16-row unit of one matrix (+ slack for the ragged last group)
   uint32_t scg, scd, ngh, ngi, nwg, nwd, ngrp, kk, ncand;
 };
@@ -108,6 +109,13 @@ __host__ __device__ inline D1Layout d1_layout(const Decode1Args& a) {
   L.hc = L.hb;
   L.redg = o;
   o += mug * L.ngh * 2u * kUnit * 4u;
+  // stack kernel: the 8 partial-logit subtotals of every expert live in the
+  // gate/up reduction area (free at the start of a layer) when they fit
+  L.sub = L.redg;
+  if (a.stack && 8u * E * 4u > mug * L.ngh * 2u * kUnit * 4u) {
+    L.sub = o;
+    o += 8u * E * 4u;
+  }
   L.redd = o;  // down partials
   o += mud * ns * L.ngi * kUnit * 4u;
   L.y = o;
@@ -126,6 +134,17 @@ __host__ __device__ inline D1Layout d1_layout(const Decode1Args& a) {
   o += (mug + ns) * 8u;
   L.ctl = o;
   o += 64u;
+  L.wstride = mud * (uint32_t)kUnit;  // floats per expert in the router slice
+  o = r16(o);  // the router slice takes 16-byte asynchronous copies
+  L.lgs = L.xo = L.wsl = o;
+  if (a.stack) {
+    L.lgs = o;
+    o += r16(E * 4u);
+    L.xo = o;
+    o += L.wstride * 4u;
+    L.wsl = o;
+    o += E * L.wstride * 4u;
+  }
   L.total = o + 1024u;  // alignment slack of the base
   return L;
 }
@@ -295,11 +314,31 @@ __host__ __device__ inline int walk_tiles(int g0, int g1, int gpe, int t, int* s
   return i;
 }
 
-template <int NV, int CPG>
-__global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant__ Decode1Args a) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  const D1Layout L = d1_layout(a);
-  unsigned char* smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
+// part[e] = sum over the CTA's output rows r of xo[r] * w[e * ws + r], one
+// expert per thread, the rows taken from (e / 2) on (so that, at 16 rows a
+// slice, the 32 lanes of a warp read 32 different banks); zero without rows.
+__device__ __forceinline__ void d1_row_partials(const float* xo, const float* w, int ws, int E, int ndr,
+                                                float* part) {
+  for (int e = threadIdx.x; e < E; e += kD1Threads) {
+    float acc = 0.f;
+    int r = ndr > 0 ? (e >> 1) % ndr : 0;
+    for (int i = 0; i < ndr; ++i) {
+      acc = fmaf(xo[r], w[e * ws + r], acc);
+      r = r + 1 == ndr ? 0 : r + 1;
+    }
+    part[e] = acc;
+  }
+}
+
+constexpr int kD1Runs = 8;       // stack kernel: runs of CTAs the partial logits are summed in
+constexpr int kD1RunMax = 32;    // most CTAs in a run (grid <= 256)
+
+// One layer of the batch-1 decode. STACK: the layer runs inside the stack
+// kernel (its logits come from the partials the CTAs published at the end of
+// the layer before; at its end it publishes the next layer's).
+template <int NV, int CPG, bool STACK>
+__device__ __forceinline__ void d1_layer(const Decode1Args& a, unsigned char* smem, const D1Layout& L, int layer,
+                                         bool traced) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.r.H, I = a.I, E = a.r.E, k = a.r.k;
   const int grid = gridDim.x, bid = blockIdx.x;
@@ -335,21 +374,29 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
   uint32_t* logits_ready = a.ctr;
   uint32_t* gu_done = a.ctr + 1;
   const uint32_t mod = a.ctr_mod;
-  unsigned long long* tr = (tid == 0) ? a.trace : nullptr;
-  unsigned long long* trp = (tid == kD1Producer * 32) ? a.trace : nullptr;
-  unsigned long long* trw = (tid == (kD1Warps - 1) * 32) ? a.trace : nullptr;  // last consumer warp
+  unsigned long long* const tb = traced ? a.trace : nullptr;
+  unsigned long long* tr = (tid == 0) ? tb : nullptr;
+  unsigned long long* trp = (tid == kD1Producer * 32) ? tb : nullptr;
+  unsigned long long* trw = (tid == (kD1Warps - 1) * 32) ? tb : nullptr;  // last consumer warp
 
+  // Every barrier in use completes one phase per layer (the layers of a stack
+  // have one shape, so a CTA has the same tiles in each): layer l waits for
+  // the phase of parity l & 1; they are initialised once.
+  const uint32_t par = (uint32_t)layer & 1u;
   trace_mark(tr, 0);
-  if (tid == 0) {
-    for (int i = 0; i < mug + ns_max; ++i) mbar_init(&bars[i], 1);
-    *abort_flag = 0;
-    *issued = 0;
-    fence_mbar_init();
+  if (layer == 0) {
+    if (tid == 0) {
+      for (int i = 0; i < mug + ns_max; ++i) mbar_init(&bars[i], 1);
+      *issued = 0;
+      fence_mbar_init();
+    }
+    // programmatic dependent launch: nothing above touched global memory
+    pdl_trigger();
+    pdl_wait();
+    __syncthreads();
+  } else if (tid == 0) {
+    *issued = 0;  // read by tid 0 alone (teardown), after the block syncs below
   }
-  // programmatic dependent launch: nothing above touched global memory
-  pdl_trigger();
-  pdl_wait();
-  __syncthreads();
   trace_mark(tr, 1);
 
   // ------------------------------------------------ 1. router logits (FP32)
@@ -358,6 +405,93 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
   uint4* xb = reinterpret_cast<uint4*>(smem + L.xb);
   float* xc = reinterpret_cast<float*>(smem + L.xc);
   const int nwg = (int)L.nwg, wpg = a.G / 8;  // staged words, words per group
+  float* lgs = reinterpret_cast<float*>(smem + L.lgs);  // stack kernel: this layer's logits
+  float* xo = reinterpret_cast<float*>(smem + L.xo);    // stack kernel: the CTA's output rows
+  float* wsl = reinterpret_cast<float*>(smem + L.wsl);  // stack kernel: router slice of those rows
+  const int wst = (int)L.wstride;
+  if constexpr (STACK) {
+    const int d0r = d0 * kUnit;
+    if (layer == 0) {
+      if (tid == 0) {
+        // epoch bases of the launch, read before this CTA's first arrival
+        s_base[0] = ld_relaxed(logits_ready);
+        s_base[1] = ld_relaxed(gu_done);
+      }
+      // the first layer's partial logits over the CTA's rows of its input
+      // (those of later layers are formed at the end of the layer before)
+      for (int q = tid; q < E * ndr; q += kD1Threads) {
+        const int e = q / ndr, r = q - e * ndr;
+        wsl[e * wst + r] = __ldg(a.r.wr + (size_t)e * H + d0r + r);
+      }
+      for (int r = tid; r < ndr; r += kD1Threads) xo[r] = __half2float(a.r.x[d0r + r]);
+      __syncthreads();
+      d1_row_partials(xo, wsl, wst, E, ndr, a.part_in + (size_t)bid * E);
+      __syncthreads();
+      if (tid == 0) epoch_arrive(logits_ready, mod);
+    }
+    if (warp == kD1Producer) {
+      if (lane == 0) {
+        for (int cur = g0, t = 0; cur < g1 && t < mug; ++t) {
+          const int sq = cur / gpe;
+          const int pend = min(g1, (sq + 1) * gpe);
+          const int n8 = min(2, pend - cur);
+          tile_s[t] = sq;
+          tile_r0[t] = (cur - sq * gpe) * 8;
+          tile_n[t] = n8 * 8;
+          cur += n8;
+        }
+        if (nu > mug) {
+          record_error(a.r.err, MOE_DEV_ERR_BOUNDS);
+          *abort_flag = 1;
+        }
+      }
+      for (int e = lane; e < E + a.r.has_shared; e += 32) e2s[e] = __ldg(a.expert_to_slot + e);
+    } else if (tid == 0) {
+      // every CTA has published this layer's partials (and so its rows of
+      // this layer's input)
+      const uint32_t base = (s_base[0] - s_base[0] % (uint32_t)grid + (uint32_t)layer * (uint32_t)grid) % mod;
+      epoch_wait(logits_ready, base, mod, (uint32_t)grid, abort_flag, a.r.err);
+      trace_mark(tr, 3);
+    }
+    __syncthreads();
+    float* sub = reinterpret_cast<float*>(smem + L.sub);
+    // The input (written by every CTA during this launch: L2 loads) and the
+    // partial logits, summed in a fixed order: kD1Runs runs of consecutive
+    // CTAs, each run in CTA order, then the runs in order, then the bias. A
+    // thread issues its partials' loads and its input word's load before it
+    // uses either, so all of them are in flight at once.
+    const uint4* xg = reinterpret_cast<const uint4*>(a.r.x);
+    for (int q0 = 0; q0 < max(nwg, kD1Runs * E); q0 += kD1Threads) {
+      const int q = q0 + tid;
+      const bool has_p = q < kD1Runs * E, has_x = q < nwg;
+      const int c = has_p ? q / E : 0, e = has_p ? q - c * E : 0;
+      const int b0 = c * grid / kD1Runs, n = has_p ? (c + 1) * grid / kD1Runs - b0 : 0;
+      float t[kD1RunMax];
+#pragma unroll
+      for (int i = 0; i < kD1RunMax; ++i) t[i] = i < n ? __ldcg(a.part_in + (size_t)(b0 + i) * E + e) : 0.f;
+      const uint4 xv = (has_x && 8 * q < H) ? __ldcg(xg + q) : make_uint4(0u, 0u, 0u, 0u);
+      if (has_p) {
+        float v = 0.f;
+#pragma unroll
+        for (int i = 0; i < kD1RunMax; ++i)
+          if (i < n) v += t[i];
+        sub[c * E + e] = v;
+      }
+      if (has_x) xb[q] = b_frag(xv);
+    }
+    __syncthreads();
+    trace_mark(tr, 2);
+    for (int q = tid; q < E + (int)L.ngh; q += kD1Threads) {
+      if (q < E) {
+        float v = sub[q];
+        for (int c = 1; c < kD1Runs; ++c) v += sub[c * E + q];
+        lgs[q] = v + (a.r.bias ? __ldg(a.r.bias + q) : 0.f);
+      } else {
+        xc[q - E] = words_const(xb, (q - E) * wpg, wpg);
+      }
+    }
+    __syncthreads();
+  } else {
   if (warp < kD1Warps) {
     for (int i = 0; i < my_rows; ++i) {
       const float v = logit_part_t1(a.r, bid + i * grid, warp);
@@ -406,6 +540,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
     for (int gi = tid - 32; gi < (int)L.ngh; gi += kD1Threads - 32) xc[gi] = words_const(xb, gi * wpg, wpg);
   }
   __syncthreads();
+  }  // !STACK
 
   // ------------------------------------------------------------ 2. routing
   const int ngrp = (int)L.ngrp, kk = (int)L.kk, ncand = (int)L.ncand, ncand4 = (ncand + 3) & ~3;
@@ -425,7 +560,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
     // sentinels that lose every tie)
     for (int gq = warp; gq < ngrp; gq += kD1Warps) {
       const int e = gq * 32 + lane;
-      const float v = e < E ? route_key(__ldcg(a.r.logits + e)) : -INFINITY;
+      const float v = e < E ? route_key(STACK ? lgs[e] : __ldcg(a.r.logits + e)) : -INFINITY;
       keys[e] = v;
       __syncwarp();
       const float4* k4 = reinterpret_cast<const float4*>(keys + gq * 32);
@@ -448,7 +583,10 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
     // softmax maximum and denominator, the summation of warp_softmax_topk
     float v[NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) v[i] = (lane + 32 * i < E) ? route_key(__ldcg(a.r.logits + lane + 32 * i)) : -INFINITY;
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = e < E ? route_key(STACK ? lgs[e] : __ldcg(a.r.logits + e)) : -INFINITY;
+    }
     float m = -INFINITY;
 #pragma unroll
     for (int i = 0; i < NV; ++i) m = fmaxf(m, v[i]);
@@ -561,7 +699,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
       // (after a failed wait every down barrier is still armed, with no
       // bytes, so that the teardown's waits end)
       bool landed = true;
-      for (int u = 0; u < nu && landed; ++u) landed = mbar_wait_sleep(&bars[u], 0u, abort_flag, a.r.err);
+      for (int u = 0; u < nu && landed; ++u) landed = mbar_wait_sleep(&bars[u], par, abort_flag, a.r.err);
       for (int sq = 0; sq < ns_max; ++sq) {
         uint64_t* bar = &bars[mug + sq];
         const bool any = landed && sq < nseg && ndr > 0;
@@ -622,10 +760,17 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
       // for (cp.async.wait_all + a consumer barrier) before the first use
       const int ngs = (int)(L.scg / 16u), nds = ndu * (int)(L.scd / 16u);
       const int n_g = nu * 2 * ngs, n_all = n_g + nseg * nds;
-      for (int q = tid; q < n_all; q += kD1Warps * 32) {
+      // stack kernel: the next layer's router slice of this CTA's output
+      // rows, for the partial logits it forms at the end of this layer
+      const int cpe = ndr / 4, n_w = (STACK && a.wr_next) ? E * cpe : 0;
+      for (int q = tid; q < n_all + n_w; q += kD1Warps * 32) {
         const uint8_t* src;
         unsigned char* dst;
-        if (q < n_g) {
+        if (q >= n_all) {
+          const int e = (q - n_all) / cpe, i = q - n_all - e * cpe;
+          src = reinterpret_cast<const uint8_t*>(a.wr_next + (size_t)e * H + d0 * kUnit + 4 * i);
+          dst = reinterpret_cast<unsigned char*>(wsl + e * wst + 4 * i);
+        } else if (q < n_g) {
           const int u = q / (2 * ngs), rem = q - u * 2 * ngs, m = rem / ngs, i = rem - m * ngs;
           if (16 * i >= tile_n[u] * (int)L.ngh * 2) continue;  // the tile's scale rows only
           const int sq = tile_s[u], r0 = tile_r0[u];
@@ -653,7 +798,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
     asm volatile("cp.async.wait_all;" ::: "memory");
     asm volatile("bar.sync 1, %0;" ::"n"(kD1Warps * 32) : "memory");
     for (int u = 0; u < nu && gw0 < gw1; ++u) {
-      if (!mbar_wait_sleep(&bars[u], 0u, abort_flag, a.r.err)) break;
+      if (!mbar_wait_sleep(&bars[u], par, abort_flag, a.r.err)) break;
       if (u < 4 && warp == 0) trace_mark(tr, 9 + u);
       const unsigned char* unit = gcode + (size_t)u * 2u * L.ug;
       const __half* gs = reinterpret_cast<const __half*>(smem + L.gsc + (size_t)u * 2u * L.scg);
@@ -694,7 +839,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
   trace_mark(tr, 17);
   if (tid == 0) {
     // every CTA counts itself, also after a failure, so no CTA waits in vain
-    const uint32_t base = s_base[1] - s_base[1] % (uint32_t)grid;
+    const uint32_t base = (s_base[1] - s_base[1] % (uint32_t)grid + (uint32_t)layer * (uint32_t)grid) % mod;
     epoch_arrive(gu_done, mod);
     epoch_wait(gu_done, base, mod, (uint32_t)grid, abort_flag, a.r.err);
     trace_mark(tr, 18);
@@ -756,7 +901,7 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
       }
       __syncwarp();
       if (sq != waited) {
-        if (!mbar_wait_sleep(&bars[mug + sq], 0u, abort_flag, a.r.err)) break;
+        if (!mbar_wait_sleep(&bars[mug + sq], par, abort_flag, a.r.err)) break;
         if (waited < 0 && warp == 0) trace_mark(tr, 19);
         if (waited < 0) trace_mark(trw, 21);
         waited = sq;
@@ -813,19 +958,54 @@ __global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant
       if (a.r.has_shared) acc += y[k * ydim + lr];
       __half o = __float2half_rn(acc);
       const int orow = d0 * kUnit + lr;
-      if (a.x_res) o = __float2half_rn(__half2float(a.x_res[orow]) + __half2float(o));
+      if (a.x_res) o = __float2half_rn(__half2float(__ldcg(a.x_res + orow)) + __half2float(o));
       a.out[orow] = o;
+      if (STACK) xo[lr] = __half2float(o);
     }
   }
   trace_mark(tr, 24);
+  if constexpr (STACK) {
+    if (a.wr_next) {
+      // the next layer's partial logits over these rows; the count releases
+      // them and the rows of the output (the next layer's input)
+      __syncthreads();
+      if (!*abort_flag) d1_row_partials(xo, wsl, wst, E, ndr, a.part_out + (size_t)bid * E);
+      __syncthreads();
+      if (tid == 0) epoch_arrive(logits_ready, mod);
+    }
+  }
 
   // ---------------------------------------------------------- teardown
   if (tid == 0 && *abort_flag && *issued) {
     // let every issued copy land before the CTA's shared memory is released
-    for (int u = 0; u < nu; ++u) mbar_wait(&bars[u], 0u, nullptr, nullptr);
-    for (int sq = 0; sq < ns_max; ++sq) mbar_wait(&bars[mug + sq], 0u, nullptr, nullptr);
+    for (int u = 0; u < nu; ++u) mbar_wait(&bars[u], par, nullptr, nullptr);
+    for (int sq = 0; sq < ns_max; ++sq) mbar_wait(&bars[mug + sq], par, nullptr, nullptr);
   }
   trace_mark(tr, 25);
+  if (STACK) __syncthreads();  // the next layer reuses the shared memory
+}
+
+template <int NV, int CPG>
+__global__ void __launch_bounds__(kD1Threads, 1) k_decode1(const __grid_constant__ Decode1Args a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const D1Layout L = d1_layout(a);
+  unsigned char* smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
+  if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(smem + L.ctl) = 0;  // abort flag
+  d1_layer<NV, CPG, false>(a, smem, L, 0, true);
+}
+
+// The layers of a stack in one launch: layer l + 1 starts when every CTA has
+// written its rows of layer l's output and its partial logits of layer l + 1
+// (one grid-wide count per layer boundary instead of a launch). A CTA that
+// gave up in one layer skips the work of the later ones but still counts
+// itself at every step.
+template <int NV, int CPG>
+__global__ void __launch_bounds__(kD1Threads, 1) k_decode1_stack(const __grid_constant__ Decode1Stack S) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const D1Layout L = d1_layout(S.layer[0]);
+  unsigned char* smem = smem_raw + (((smem_u32(smem_raw) + 1023u) & ~1023u) - smem_u32(smem_raw));
+  if (threadIdx.x == 0) *reinterpret_cast<volatile int*>(smem + L.ctl) = 0;  // abort flag
+  for (int l = 0; l < S.n_layers; ++l) d1_layer<NV, CPG, true>(S.layer[l], smem, L, l, l == S.trace_layer);
 }
 
 template <int NV, int CPG>
@@ -854,6 +1034,33 @@ cudaError_t launch_decode1_nv(const Decode1Args& a, int grid, cudaStream_t s, bo
   return a.G == 64 ? launch_decode1_t<NV, 2>(a, grid, s, pdl) : launch_decode1_t<NV, 4>(a, grid, s, pdl);
 }
 
+template <int NV, int CPG>
+cudaError_t launch_decode1_stack_t(const Decode1Stack& st, int grid, cudaStream_t s, bool pdl) {
+  const size_t smem = decode1_smem_bytes(st.layer[0]);
+  if (smem == 0) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_smem(k_decode1_stack<NV, CPG>, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kD1Threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, k_decode1_stack<NV, CPG>, st);
+}
+
+template <int NV>
+cudaError_t launch_decode1_stack_nv(const Decode1Stack& st, int grid, cudaStream_t s, bool pdl) {
+  return st.layer[0].G == 64 ? launch_decode1_stack_t<NV, 2>(st, grid, s, pdl)
+                             : launch_decode1_stack_t<NV, 4>(st, grid, s, pdl);
+}
+
 }  // namespace
 
 int decode1_max_tiles(int nseg, int I, int grid) {
@@ -874,7 +1081,25 @@ size_t decode1_smem_bytes(const Decode1Args& a) {
   return L.total <= kSmemBudget ? L.total : 0;
 }
 
+cudaError_t launch_decode1_stack(const Decode1Stack& st, int grid, cudaStream_t s, bool pdl) {
+  if (st.n_layers < 1 || st.n_layers > kD1MaxLayers || grid > kD1Runs * kD1RunMax) return cudaErrorInvalidValue;
+  const Decode1Args& a = st.layer[0];
+  for (int l = 0; l < st.n_layers; ++l) {
+    const Decode1Args& b = st.layer[l];
+    // one shape for every layer (one layout, one template), one counter pair
+    if (!b.stack || b.r.T != 1 || b.r.H != a.r.H || b.I != a.I || b.r.E != a.r.E || b.r.k != a.r.k || b.G != a.G ||
+        b.r.has_shared != a.r.has_shared || b.ctr != a.ctr || b.ctr_mod != a.ctr_mod || !b.part_in || !b.part_out ||
+        (l + 1 < st.n_layers) != (b.wr_next != nullptr))
+      return cudaErrorInvalidValue;
+  }
+  if (a.ctr_mod == 0 || a.ctr_mod % (uint32_t)grid) return cudaErrorInvalidValue;
+  if (a.r.E <= 64) return launch_decode1_stack_nv<2>(st, grid, s, pdl);
+  if (a.r.E <= 128) return launch_decode1_stack_nv<4>(st, grid, s, pdl);
+  return cudaErrorInvalidValue;  // the partial logits of larger E: per-layer launches
+}
+
 cudaError_t launch_decode1(const Decode1Args& a, int grid, cudaStream_t s, bool pdl) {
+  if (a.stack) return cudaErrorInvalidValue;
   if (a.r.T != 1 || a.ctr_mod == 0 || a.ctr_mod % (uint32_t)grid) return cudaErrorInvalidValue;
   if (a.r.E <= 64) return launch_decode1_nv<2>(a, grid, s, pdl);
   if (a.r.E <= 128) return launch_decode1_nv<4>(a, grid, s, pdl);

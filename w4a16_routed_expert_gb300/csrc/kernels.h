@@ -244,6 +244,19 @@ struct Decode1Args {
   int max_units_g;              // most gate/up tiles of a CTA (decode1_max_tiles)
   int max_units_d;              // ceil(H / 16 / grid)
   int max_rows_rt;              // router rows per CTA: ceil(E / grid)
+  // stacked layers in one launch (k_decode1_stack), 0 / nullptr otherwise:
+  int stack;                    // 1: this layer runs inside the stack kernel
+  const float* wr_next;         // next layer's router [E][H], nullptr at the last layer
+  float* part_in;               // [grid][E] partial logits of this layer, one row per CTA
+  float* part_out;              // [grid][E] partial logits of the next layer
+};
+// Layers of one stack launch: x of layer l + 1 is the out of layer l; every
+// layer has the same shape.
+constexpr int kD1MaxLayers = 48;
+struct Decode1Stack {
+  Decode1Args layer[kD1MaxLayers];
+  int n_layers;
+  int trace_layer;  // the layer whose phases are stamped (when trace is set)
 };
 // Most gate/up tiles (16 rows, 8 at an expert's end) any CTA of the grid
 // gets when nseg experts' I rows are split in 8-row granules.
@@ -251,6 +264,7 @@ int decode1_max_tiles(int nseg, int I, int grid);
 // Dynamic shared memory of k_decode1 for these arguments (0: does not fit).
 size_t decode1_smem_bytes(const Decode1Args& a);
 cudaError_t launch_decode1(const Decode1Args& a, int grid, cudaStream_t s, bool pdl);
+cudaError_t launch_decode1_stack(const Decode1Stack& st, int grid, cudaStream_t s, bool pdl);
 cudaError_t launch_gemm(bool dual, const CUtensorMap& codes0, const CUtensorMap& codes1, const CUtensorMap& act,
                         const GemmArgs& a, int grid, cudaStream_t s, bool pdl);
 size_t gemm_smem_bytes(bool dual);

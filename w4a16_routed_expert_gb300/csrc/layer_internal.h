@@ -133,6 +133,10 @@ moe_status_t enqueue_decode1(moe_layer* L, const __half* x, __half* out, int32_t
                              cudaStream_t s);
 // Enqueue the weighted combine of the expert outputs into out.
 moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, cudaStream_t s);
+// Arguments of the batch-1 kernel for one layer (the single-layer launch and
+// the stack kernel).
+void fill_decode1_args(moe_layer* L, const __half* x, __half* out, int32_t* ids_user, float* w_user,
+                       Decode1Args* a);
 // Record the calling thread's error message; returns st.
 moe_status_t set_error(moe_status_t st, const char* fmt, ...);
 

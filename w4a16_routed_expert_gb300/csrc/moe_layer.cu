@@ -562,13 +562,13 @@ moe_status_t enqueue_decode(moe_layer* L, const __half* x, int T, __half* out, i
   return MOE_OK;
 }
 
-moe_status_t enqueue_decode1(moe_layer* L, const __half* x, __half* out, int32_t* ids_user, float* w_user,
-                             cudaStream_t s) {
+void fill_decode1_args(moe_layer* L, const __half* x, __half* out, int32_t* ids_user, float* w_user,
+                       Decode1Args* ap) {
   const moe_layer_config_t& c = L->cfg;
   const int H = c.hidden, I = c.intermediate, E = c.num_experts, k = c.top_k;
   const int grid = L->num_sms;
-  if (grid < 1) return MOE_ERR_UNSUPPORTED;
-  Decode1Args a = {};
+  Decode1Args& a = *ap;
+  a = Decode1Args{};
   RouteArgs& r = a.r;
   r.x = x;
   r.wr = L->w.router_w;
@@ -613,6 +613,14 @@ moe_status_t enqueue_decode1(moe_layer* L, const __half* x, __half* out, int32_t
   a.max_units_g = decode1_max_tiles(a.nseg_max, I, grid);
   a.max_units_d = (H / 16 + grid - 1) / grid;
   a.max_rows_rt = (E + grid - 1) / grid;
+}
+
+moe_status_t enqueue_decode1(moe_layer* L, const __half* x, __half* out, int32_t* ids_user, float* w_user,
+                             cudaStream_t s) {
+  const int grid = L->num_sms;
+  if (grid < 1) return MOE_ERR_UNSUPPORTED;
+  Decode1Args a;
+  fill_decode1_args(L, x, out, ids_user, w_user, &a);
   if (decode1_smem_bytes(a) == 0) return MOE_ERR_UNSUPPORTED;
   if (L->profiling) prof_record(L->ev[0], s);
   // (every CTA rewrites its stamps on every launch: no clearing launch)

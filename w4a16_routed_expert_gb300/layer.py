@@ -5,6 +5,7 @@ layer runs in the library's CUDA kernels.
 """
 from __future__ import annotations
 
+import ctypes
 from typing import Optional
 
 import torch
@@ -102,6 +103,48 @@ class MoELayer:
     def close(self):
         if getattr(self, "handle", None):
             capi.moe_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MoEStack:
+    """Layers run one after another on one stream: x_{l+1} = layer_l(x_l).
+
+    Borrows the MoELayer objects (keep them alive while the stack lives).
+    A one-token forward over fully resident layers of one shape runs as a
+    single kernel launch (``single_launch``)."""
+
+    def __init__(self, layers):
+        self._layers = list(layers)
+        arr = (capi._P * len(self._layers))(*[l.handle for l in self._layers])
+        h = capi._P()
+        capi.check(capi.lib().moe_stack_create(arr, len(self._layers), ctypes.byref(h)), "moe_stack_create")
+        self.handle = h.value
+        self.hidden = self._layers[0].hidden
+
+    @property
+    def single_launch(self) -> bool:
+        return bool(capi.lib().moe_stack_single_launch(self.handle))
+
+    def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, states: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(x)
+        capi.check(capi.lib().moe_stack_forward(self.handle, _ptr(x), x.shape[0], _ptr(out), _ptr(states),
+                                                _stream_handle(stream)), "moe_stack_forward")
+        return out
+
+    def sync(self, stream=None):
+        capi.check(capi.lib().moe_stack_sync(self.handle, _stream_handle(stream)), "moe_stack_sync")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            capi.lib().moe_stack_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
