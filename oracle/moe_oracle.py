@@ -16,7 +16,13 @@ layer, each step written in the order the layer defines it:
 5. counting-sort permutation by expert                        -> counting_sort
 6. expert FFN ``y = W_d (silu(W_g x) * (W_u x))`` on dequantised INT4 weights
                                                               -> expert_ffn
-7. weighted combine ``out = sum_j w_j y_j (+ y_shared)``     -> moe_forward
+7. weighted combine ``out = sum_j w_j y_j (+ g y_shared)``   -> moe_forward
+
+Variants (readings of this library; the pages print none of them): an
+asymmetric zero point per group, ``w = (q - z) * s`` with z a code 0..15
+stored one per byte in three more record sections (gate_z, up_z, down_z);
+any group size G (32, 64, 128); a shared expert gated per token by
+``g = sigmoid(x . w_gate)`` (weight 1 without a gate vector).
 
 Sources (page title, section):
 * Horizon RunMap report, "Architecture invariants" / "What is implemented" /
@@ -48,12 +54,15 @@ def _align256(v: int) -> int:
     return -(-v // 256) * 256
 
 
-def record_layout(H: int, I: int, G: int):
-    """Section offsets of one expert record and the padded record size."""
+def record_layout(H: int, I: int, G: int, zero_points: bool = False):
+    """Section offsets of one expert record and the padded record size; with
+    zero points, three byte-per-group sections follow the scales."""
     groups_h = -(-H // G)
     groups_i = -(-I // G)
     order = (("gate_q", I * (H // 2)), ("up_q", I * (H // 2)), ("down_q", H * (I // 2)),
              ("gate_s", 2 * I * groups_h), ("up_s", 2 * I * groups_h), ("down_s", 2 * H * groups_i))
+    if zero_points:
+        order = order + (("gate_z", I * groups_h), ("up_z", I * groups_h), ("down_z", H * groups_i))
     offs = {}
     cur = 0
     for name, nbytes in order:
@@ -75,29 +84,37 @@ def unpack_codes(raw: np.ndarray, N: int, K: int) -> np.ndarray:
     return q
 
 
-def dequantize(q: np.ndarray, scales: np.ndarray, G: int) -> np.ndarray:
-    """w[n, k] = (q[n, k] - 8) * s[n, k // G] in float64."""
+def dequantize(q: np.ndarray, scales: np.ndarray, G: int, zeros=None) -> np.ndarray:
+    """w[n, k] = (q[n, k] - z[n, k // G]) * s[n, k // G] in float64, z = 8
+    when no zero points are given."""
     N, K = q.shape
     s = np.asarray(scales, dtype=np.float16).astype(np.float64)
-    w = np.asarray(q).astype(np.float64) - 8.0
+    w = np.asarray(q).astype(np.float64)
     for gi in range(s.shape[1]):
-        w[:, gi * G:(gi + 1) * G] *= s[:, gi:gi + 1]
+        z = 8.0 if zeros is None else np.asarray(zeros)[:, gi:gi + 1].astype(np.float64)
+        w[:, gi * G:(gi + 1) * G] = (w[:, gi * G:(gi + 1) * G] - z) * s[:, gi:gi + 1]
     return w
 
 
-def expert_matrices(record: np.ndarray, H: int, I: int, G: int):
+def expert_matrices(record: np.ndarray, H: int, I: int, G: int, zero_points: bool = False):
     """Dequantised (W_gate [I][H], W_up [I][H], W_down [H][I]) of one record."""
-    offs, _ = record_layout(H, I, G)
+    offs, _ = record_layout(H, I, G, zero_points)
     rec = np.asarray(record, dtype=np.uint8).reshape(-1)
 
     def sect(name):
         o, n = offs[name]
         return rec[o:o + n]
 
+    def zeros(name, n, ng):
+        return sect(name).reshape(n, ng) if zero_points else None
+
     gh, gi = -(-H // G), -(-I // G)
-    wg = dequantize(unpack_codes(sect("gate_q"), I, H), sect("gate_s").view(np.float16).reshape(I, gh), G)
-    wu = dequantize(unpack_codes(sect("up_q"), I, H), sect("up_s").view(np.float16).reshape(I, gh), G)
-    wd = dequantize(unpack_codes(sect("down_q"), H, I), sect("down_s").view(np.float16).reshape(H, gi), G)
+    wg = dequantize(unpack_codes(sect("gate_q"), I, H), sect("gate_s").view(np.float16).reshape(I, gh), G,
+                    zeros("gate_z", I, gh))
+    wu = dequantize(unpack_codes(sect("up_q"), I, H), sect("up_s").view(np.float16).reshape(I, gh), G,
+                    zeros("up_z", I, gh))
+    wd = dequantize(unpack_codes(sect("down_q"), H, I), sect("down_s").view(np.float16).reshape(H, gi), G,
+                    zeros("down_z", H, gi))
     return wg, wu, wd
 
 
@@ -203,6 +220,16 @@ def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
 
 
+def shared_gate_weight(x: np.ndarray, gate_w) -> np.ndarray:
+    """Per-token weight of the shared expert: sigmoid(x . w_gate) in float64,
+    1 for every token without a gate vector."""
+    x64 = np.asarray(x, dtype=np.float64)
+    if gate_w is None:
+        return np.ones(x64.shape[0])
+    z = x64 @ np.asarray(gate_w, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
 def expert_ffn(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, xrows: np.ndarray) -> np.ndarray:
     """SwiGLU expert: y = W_d (silu(W_g x) * (W_u x)) for each row of xrows."""
     x64 = np.asarray(xrows, dtype=np.float64)
@@ -213,7 +240,7 @@ def expert_ffn(wg: np.ndarray, wu: np.ndarray, wd: np.ndarray, xrows: np.ndarray
 
 
 def moe_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k, G,
-                renormalize, has_shared=False, tokens=None):
+                renormalize, has_shared=False, tokens=None, zero_points=False, shared_gate=None):
     """Whole layer for the tokens in ``tokens`` (default: all).
 
     Routing (logits, softmax, selection, weights, permutation) is computed for
@@ -229,14 +256,17 @@ def moe_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k
     if tokens is None:
         tokens = np.arange(T)
     out = expert_combine(x, ids, w, records, expert_to_slot, H=H, I=I, E=E, k=k, G=G,
-                         has_shared=has_shared, tokens=tokens)
+                         has_shared=has_shared, tokens=tokens, zero_points=zero_points,
+                         shared_gate=shared_gate)
     return dict(out=out, logits=L, probs=p, ids=ids, weights=w, counts=counts,
                 offsets=offsets, perm=perm, inv_perm=inv_perm)
 
 
-def expert_combine(x, ids, w, records, expert_to_slot, *, H, I, E, k, G, has_shared=False, tokens=None):
-    """out[t] = sum_j w[t, j] * y_{ids[t, j]}(x[t]) (+ y_shared(x[t])) for the
-    requested tokens, given the routing (ids, w) of the whole batch."""
+def expert_combine(x, ids, w, records, expert_to_slot, *, H, I, E, k, G, has_shared=False, tokens=None,
+                   zero_points=False, shared_gate=None):
+    """out[t] = sum_j w[t, j] * y_{ids[t, j]}(x[t]) (+ g_t y_shared(x[t])) for
+    the requested tokens, given the routing (ids, w) of the whole batch; g_t
+    from shared_gate_weight."""
     x = np.asarray(x)
     ids = np.asarray(ids)
     w = np.asarray(w, dtype=np.float64)
@@ -246,7 +276,7 @@ def expert_combine(x, ids, w, records, expert_to_slot, *, H, I, E, k, G, has_sha
     out = np.zeros((tokens.size, H), dtype=np.float64)
     used = sorted(set(int(e) for e in ids[tokens].reshape(-1)))
     for e in used:
-        wg, wu, wd = expert_matrices(records[int(expert_to_slot[e])], H, I, G)
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[e])], H, I, G, zero_points)
         for j in range(k):
             rows = np.nonzero(ids[tokens, j] == e)[0]
             if rows.size == 0:
@@ -254,13 +284,13 @@ def expert_combine(x, ids, w, records, expert_to_slot, *, H, I, E, k, G, has_sha
             y = expert_ffn(wg, wu, wd, x[tokens[rows]])
             out[rows] += w[tokens[rows], j][:, None] * y
     if has_shared:
-        wg, wu, wd = expert_matrices(records[int(expert_to_slot[E])], H, I, G)
-        out += expert_ffn(wg, wu, wd, x[tokens])
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[E])], H, I, G, zero_points)
+        out += shared_gate_weight(x[tokens], shared_gate)[:, None] * expert_ffn(wg, wu, wd, x[tokens])
     return out
 
 
 def dense_masked_forward(x, router_w, router_bias, records, expert_to_slot, *, H, I, E, k, G,
-                         renormalize, has_shared=False):
+                         renormalize, has_shared=False, zero_points=False, shared_gate=None):
     """Brute force: every expert runs on every token; a [T][E] mask-weight
     matrix (zero for experts a token did not select) combines them."""
     x = np.asarray(x)
@@ -278,12 +308,18 @@ def dense_masked_forward(x, router_w, router_bias, records, expert_to_slot, *, H
         M[t, sel[t]] = ps
     Y = np.zeros((E, T, H), dtype=np.float64)
     for e in range(E):
-        wg, wu, wd = expert_matrices(records[int(expert_to_slot[e])], H, I, G)
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[e])], H, I, G, zero_points)
         Y[e] = expert_ffn(wg, wu, wd, x)
     out = np.einsum("te,eth->th", M, Y)
     if has_shared:
-        wg, wu, wd = expert_matrices(records[int(expert_to_slot[E])], H, I, G)
-        out = out + expert_ffn(wg, wu, wd, x)
+        wg, wu, wd = expert_matrices(records[int(expert_to_slot[E])], H, I, G, zero_points)
+        ys = expert_ffn(wg, wu, wd, x)
+        for t in range(T):
+            gate = 1.0
+            if shared_gate is not None:
+                gate = 1.0 / (1.0 + np.exp(-float(np.dot(x[t].astype(np.float64),
+                                                         np.asarray(shared_gate, dtype=np.float64)))))
+            out[t] = out[t] + gate * ys[t]
     return out, sel
 
 

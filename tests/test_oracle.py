@@ -338,7 +338,7 @@ def test_planted_mistakes_are_caught(golden_dir, mistake, monkeypatch):
     """A plausible mistake planted in the oracle must fail the hand-worked pin."""
     fx = _load(golden_dir, "two_expert_h4.json")
     if mistake == "no_zero_point":
-        monkeypatch.setattr(O, "dequantize", lambda q, s, G: q.astype(np.float64)
+        monkeypatch.setattr(O, "dequantize", lambda q, s, G, zeros=None: q.astype(np.float64)
                             * np.asarray(s, np.float16).astype(np.float64)[:, np.arange(q.shape[1]) // G])
     elif mistake == "swapped_nibbles":
         orig = O.unpack_codes
@@ -360,3 +360,139 @@ def test_planted_mistakes_are_caught(golden_dir, mistake, monkeypatch):
         if r["ids"].tolist() != c["ids"] or not np.allclose(r["out"], c["out"], rtol=1e-12, atol=1e-14):
             caught = True
     assert caught
+
+
+# ----------------------------------------------------------------------------
+# variants: asymmetric zero points, G = 32, sigmoid-gated shared expert
+# ----------------------------------------------------------------------------
+
+def test_zero_point_record_hand_built(golden_dir):
+    fx = _load(golden_dir, "zero_point_record.json")
+    H, I, G = fx["H"], fx["I"], fx["G"]
+    offs, size = O.record_layout(H, I, G, zero_points=True)
+    assert {k: v[0] for k, v in offs.items()} == fx["offsets"] and size == fx["record_bytes"]
+    rec = np.zeros(size, dtype=np.uint8)
+    o = fx["offsets"]
+
+    def put(name, arr, dtype):
+        b = np.asarray(arr, dtype=dtype).reshape(-1).view(np.uint8)
+        rec[o[name]:o[name] + b.size] = b
+
+    put("gate_q", fx["gate_q_bytes"], np.uint8)
+    put("up_q", fx["up_q_bytes"], np.uint8)
+    put("down_q", fx["down_q_bytes"], np.uint8)
+    put("gate_s", fx["gate_s"], np.float16)
+    put("up_s", fx["up_s"], np.float16)
+    put("down_s", fx["down_s"], np.float16)
+    put("gate_z", fx["gate_z"], np.uint8)
+    put("up_z", fx["up_z"], np.uint8)
+    put("down_z", fx["down_z"], np.uint8)
+    wg, wu, wd = O.expert_matrices(rec, H, I, G, zero_points=True)
+    assert wg.tolist() == fx["gate_w"]
+    assert wu.tolist() == fx["up_w"]
+    assert wd.tolist() == fx["down_w"]
+    # the same bytes read without zero points: zero point 8 everywhere
+    q = O.unpack_codes(np.array(fx["gate_q_bytes"], dtype=np.uint8), I, H)
+    assert q.tolist() == fx["gate_codes"]
+
+
+def test_zero_point_8_is_the_symmetric_format():
+    rng = np.random.default_rng(3)
+    q = rng.integers(0, 16, size=(5, 96))
+    s = rng.uniform(-1, 1, size=(5, 3)).astype(np.float16)
+    a = O.dequantize(q, s, 32)
+    b = O.dequantize(q, s, 32, zeros=np.full((5, 3), 8, dtype=np.uint8))
+    assert np.array_equal(a, b)
+    # and a zero point z shifts every weight of its group by (8 - z) * s
+    z = rng.integers(0, 16, size=(5, 3)).astype(np.uint8)
+    c = O.dequantize(q, s, 32, zeros=z)
+    shift = (8.0 - z.astype(np.float64)) * s.astype(np.float64)
+    assert np.allclose(c - a, np.repeat(shift, 32, axis=1), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("K", [128, 96])
+def test_g32_with_paired_scales_is_g64(K):
+    # groups of 32 whose scales (and zero points) agree in pairs are groups
+    # of 64: the G = 32 reading reduces to the pinned G = 64 one (K = 96:
+    # the last G = 64 group is the ragged 32 codes)
+    rng = np.random.default_rng(4)
+    q = rng.integers(0, 16, size=(4, K))
+    s64 = rng.uniform(-2, 2, size=(4, -(-K // 64))).astype(np.float16)
+    z64 = rng.integers(0, 16, size=s64.shape).astype(np.uint8)
+    s32 = np.repeat(s64, 2, axis=1)[:, :K // 32]
+    z32 = np.repeat(z64, 2, axis=1)[:, :K // 32]
+    assert np.array_equal(O.dequantize(q, s32, 32), O.dequantize(q, s64, 64))
+    assert np.array_equal(O.dequantize(q, s32, 32, z32), O.dequantize(q, s64, 64, z64))
+    # one different scale in the second half changes exactly those 32 codes
+    s32b = s32.copy()
+    s32b[0, 1] = np.float16(float(s32[0, 1]) + 1.0)
+    d = O.dequantize(q, s32b, 32) != O.dequantize(q, s32, 32)
+    assert not d[1:].any() and not d[0, :32].any() and not d[0, 64:].any()
+
+
+def test_shared_gate_weight_hand_worked():
+    # sigmoid(ln 3) = 3 / (3 + 1) = 0.75; sigmoid(0) = 0.5; no gate -> 1
+    x = np.array([[math.log(3.0), 5.0], [0.0, 0.0]])
+    g = np.array([1.0, 0.0])
+    assert np.allclose(O.shared_gate_weight(x, g), [0.75, 0.5], rtol=0, atol=1e-15)
+    assert O.shared_gate_weight(x, None).tolist() == [1.0, 1.0]
+
+
+def _gated_layer(zero_points):
+    shape = synth.LayerShape(64, 32, 6, 2, 32, True, has_shared=True, zero_points=zero_points, shared_gate=True)
+    return shape, synth.make_layer(shape, seed=12, codes="uniform")
+
+
+@pytest.mark.parametrize("zero_points", [False, True])
+def test_shared_gate_special_cases(zero_points):
+    shape, lay = _gated_layer(zero_points)
+    x = synth.make_tokens(shape.hidden, 5, seed=12)
+    kw = dict(H=shape.hidden, I=shape.intermediate, E=shape.num_experts, k=shape.top_k, G=shape.group_size,
+              renormalize=shape.renormalize, zero_points=zero_points)
+    args = (x, lay.router_w, None, lay.records, lay.expert_to_slot)
+    routed = O.moe_forward(*args, has_shared=False, **kw)["out"]
+    full = O.moe_forward(*args, has_shared=True, **kw)["out"]
+    # a zero gate vector: every token takes half the shared expert
+    half = O.moe_forward(*args, has_shared=True, shared_gate=np.zeros(shape.hidden), **kw)["out"]
+    assert np.allclose(half, routed + 0.5 * (full - routed), rtol=1e-12, atol=1e-15)
+    # a gate that saturates: weight 1 (to the last bits of float64)
+    big = np.full(shape.hidden, 1e3) * np.sign(x.astype(np.float64).sum(axis=0) + 1e-9)
+    sat = O.moe_forward(*args, has_shared=True, shared_gate=big, **kw)["out"]
+    gw = O.shared_gate_weight(x, big)
+    ok = gw > 1 - 1e-12
+    assert ok.any() and np.allclose(sat[ok], full[ok], rtol=1e-10, atol=1e-14)
+    # brute force (every expert on every token, a dense mask) agrees
+    dense, _ = O.dense_masked_forward(*args, has_shared=True, shared_gate=lay.shared_gate, **kw)
+    ref = O.moe_forward(*args, has_shared=True, shared_gate=lay.shared_gate, **kw)["out"]
+    assert np.allclose(dense, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_asymmetric_quantiser_round_trips_within_half_a_step():
+    # the generator's asymmetric quantiser: every weight within half a scale
+    # step of (q - z) * s (clipping aside), using the oracle's dequantisation
+    rng = np.random.default_rng(5)
+    w = rng.standard_normal((6, 96)).astype(np.float32) * np.float32(0.02)
+    q, s, z = synth.quantize_int4_asym(w, 32)
+    wd = O.dequantize(q, s, 32, zeros=z)
+    step = np.repeat(s.astype(np.float64), 32, axis=1)
+    assert (np.abs(wd - w) <= 0.5 * step + 1e-6).all()
+
+
+@pytest.mark.parametrize("mistake", ["zero_point_ignored", "zero_point_sign", "gate_ignored", "gate_sign"])
+def test_planted_variant_mistakes_are_caught(golden_dir, mistake, monkeypatch):
+    """A plausible mistake planted in the variants' oracle code fails a pin."""
+    orig_dq, orig_gate = O.dequantize, O.shared_gate_weight
+    if mistake == "zero_point_ignored":
+        monkeypatch.setattr(O, "dequantize", lambda q, s, G, zeros=None: orig_dq(q, s, G))
+    elif mistake == "zero_point_sign":
+        monkeypatch.setattr(O, "dequantize", lambda q, s, G, zeros=None: orig_dq(
+            q, s, G, None if zeros is None else (16 - np.asarray(zeros, dtype=np.int64)) % 16))
+    elif mistake == "gate_ignored":
+        monkeypatch.setattr(O, "shared_gate_weight", lambda x, g: orig_gate(x, None))
+    elif mistake == "gate_sign":
+        monkeypatch.setattr(O, "shared_gate_weight", lambda x, g: orig_gate(x, None if g is None else -np.asarray(g)))
+    with pytest.raises(AssertionError):
+        if mistake.startswith("zero_point"):
+            test_zero_point_record_hand_built(golden_dir)
+        else:
+            test_shared_gate_weight_hand_worked()

@@ -20,7 +20,10 @@ file layout of the moe-stream page, section "Method"):
   k, the high nibble the odd k. Row stride K/2 bytes.
 * ``*_s``: FP16 scales, [N][ceil(K/G)] row-major, one per G consecutive codes
   along K; the last group of a row covers the remaining K mod G codes.
-* The dequantised weight is ``(q - 8) * s`` (unsigned 4-bit, zero point 8).
+* The dequantised weight is ``(q - 8) * s`` (unsigned 4-bit, zero point 8),
+  or, for a layer with zero points, ``(q - z) * s`` with one code z per
+  group stored as one byte in three more sections after the scales:
+  ``gate_z | up_z | down_z``, each [N][ceil(K/G)].
 * Each section starts on a 256-byte boundary; the record size is rounded up to
   a multiple of 256 bytes.
 
@@ -56,6 +59,8 @@ class LayerShape:
     router_std: float = 0.02
     expert_std: float = 0.02
     zipf_s: float = 0.0  # >0: add -zipf_s*ln(e+1) to expert e's logit
+    zero_points: bool = False  # asymmetric quantisation, a zero code per group
+    shared_gate: bool = False  # the shared expert gated per token by sigmoid(x . w_gate)
 
     @property
     def n_records(self) -> int:
@@ -70,7 +75,7 @@ MANY_EXPERTS = LayerShape(2048, 512, 512, 10, 128, True, has_shared=True, zipf_s
 GPTOSS_LIKE = LayerShape(2880, 2880, 128, 4, 128, True)
 
 
-def section_layout(H: int, I: int, G: int) -> dict:
+def section_layout(H: int, I: int, G: int, zero_points: bool = False) -> dict:
     """Byte offset and size of each section of the canonical record."""
     ng_h = -(-H // G)
     ng_i = -(-I // G)
@@ -82,6 +87,8 @@ def section_layout(H: int, I: int, G: int) -> dict:
         ("up_s", I * ng_h * 2),
         ("down_s", H * ng_i * 2),
     ]
+    if zero_points:
+        sizes += [("gate_z", I * ng_h), ("up_z", I * ng_h), ("down_z", H * ng_i)]
     out = {}
     off = 0
     for name, size in sizes:
@@ -93,8 +100,8 @@ def section_layout(H: int, I: int, G: int) -> dict:
     return out
 
 
-def record_bytes(H: int, I: int, G: int) -> int:
-    return section_layout(H, I, G)["record_bytes"]
+def record_bytes(H: int, I: int, G: int, zero_points: bool = False) -> int:
+    return section_layout(H, I, G, zero_points)["record_bytes"]
 
 
 def quantize_int4(w: np.ndarray, G: int):
@@ -118,6 +125,26 @@ def quantize_int4(w: np.ndarray, G: int):
     return np.ascontiguousarray(q), s16
 
 
+def quantize_int4_asym(w: np.ndarray, G: int):
+    """Asymmetric INT4 quantisation (data preparation): per group of G along
+    K, scale = fp16((max - min) / 15) (1.0 for a constant group), zero code
+    z = clip(rint(-min / scale), 0, 15), code = clip(rint(w / scale) + z, 0, 15)."""
+    w = np.asarray(w, dtype=np.float32)
+    N, K = w.shape
+    ng = -(-K // G)
+    pad = ng * G - K
+    # padding repeats each row's last value, so it leaves min / max alone
+    wp = np.pad(w, ((0, 0), (0, pad)), mode="edge") if pad else w
+    wg = wp.reshape(N, ng, G)
+    lo, hi = wg.min(axis=2), wg.max(axis=2)
+    s16 = ((hi - lo) / np.float32(15.0)).astype(np.float16)
+    s16[s16 == 0] = np.float16(1.0)
+    s32 = s16.astype(np.float32)
+    z = np.clip(np.rint(-lo / s32), 0, 15).astype(np.uint8)
+    q = np.clip(np.rint(wg / s32[:, :, None]) + z[:, :, None], 0, 15).astype(np.uint8).reshape(N, ng * G)[:, :K]
+    return np.ascontiguousarray(q), s16, np.ascontiguousarray(z)
+
+
 def pack_nibbles(q: np.ndarray) -> np.ndarray:
     """[N][K] codes in 0..15 -> [N][K/2] bytes, low nibble = even k."""
     q = np.asarray(q, dtype=np.uint8)
@@ -125,8 +152,10 @@ def pack_nibbles(q: np.ndarray) -> np.ndarray:
     return np.ascontiguousarray((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
 
 
-def pack_record(H, I, G, gate_q, up_q, down_q, gate_s, up_s, down_s) -> np.ndarray:
-    lay = section_layout(H, I, G)
+def pack_record(H, I, G, gate_q, up_q, down_q, gate_s, up_s, down_s, gate_z=None, up_z=None,
+                down_z=None) -> np.ndarray:
+    zp = gate_z is not None
+    lay = section_layout(H, I, G, zp)
     rec = np.zeros(lay["record_bytes"], dtype=np.uint8)
     parts = {
         "gate_q": pack_nibbles(gate_q),
@@ -136,6 +165,10 @@ def pack_record(H, I, G, gate_q, up_q, down_q, gate_s, up_s, down_s) -> np.ndarr
         "up_s": np.ascontiguousarray(up_s, dtype=np.float16).view(np.uint8),
         "down_s": np.ascontiguousarray(down_s, dtype=np.float16).view(np.uint8),
     }
+    if zp:
+        parts.update(gate_z=np.ascontiguousarray(gate_z, dtype=np.uint8),
+                     up_z=np.ascontiguousarray(up_z, dtype=np.uint8),
+                     down_z=np.ascontiguousarray(down_z, dtype=np.uint8))
     for name, arr in parts.items():
         off, size = lay[name]
         flat = arr.reshape(-1)
@@ -150,16 +183,22 @@ def _expert_codes(shape: LayerShape, rng: np.random.Generator, codes: str):
     for (n, k) in ((I, H), (I, H), (H, I)):
         if codes == "quantized":
             w = rng.standard_normal((n, k), dtype=np.float32) * np.float32(shape.expert_std)
-            mats.append(quantize_int4(w, G))
+            mats.append(quantize_int4_asym(w, G) if shape.zero_points else quantize_int4(w, G))
         elif codes == "uniform":
             # every code 0..15 equally likely; scales spread over a range so
             # that no single scale dominates (exercises q = 0 and q = 15).
             q = rng.integers(0, 16, size=(n, k), dtype=np.uint8)
             ng = -(-k // G)
             s = (rng.uniform(0.5, 1.5, size=(n, ng)) * (shape.expert_std / 4.6)).astype(np.float16)
-            mats.append((q, s))
+            if shape.zero_points:
+                mats.append((q, s, rng.integers(0, 16, size=(n, ng), dtype=np.uint8)))
+            else:
+                mats.append((q, s))
         else:
             raise ValueError(codes)
+    if shape.zero_points:
+        (gq, gs, gz), (uq, us, uz), (dq, ds, dz) = mats
+        return gq, uq, dq, gs, us, ds, gz, uz, dz
     (gq, gs), (uq, us), (dq, ds) = mats
     return gq, uq, dq, gs, us, ds
 
@@ -171,6 +210,7 @@ class Layer:
     router_bias: Optional[np.ndarray]  # fp32 [E] or None
     records: np.ndarray             # uint8 [n_slots][record_bytes], in slot order
     expert_to_slot: np.ndarray      # int32 [n_records]
+    shared_gate: Optional[np.ndarray] = None  # fp32 [H] gate vector of the shared expert, or None
 
 
 def _expert_record(args):
@@ -200,7 +240,7 @@ def make_layer(shape: LayerShape, seed: int, codes: str = "quantized",
         slot_of = np.random.default_rng(children[2]).permutation(n_slots)[:nrec].astype(np.int32)
     else:
         slot_of = np.arange(nrec, dtype=np.int32)
-    rb = record_bytes(shape.hidden, shape.intermediate, shape.group_size)
+    rb = record_bytes(shape.hidden, shape.intermediate, shape.group_size, shape.zero_points)
     records = np.full((n_slots, rb), 0xFF, dtype=np.uint8)
     jobs = [(shape, children[3 + e], codes) for e in range(nrec)]
     weights_per_layer = nrec * 3 * shape.hidden * shape.intermediate
@@ -216,7 +256,11 @@ def make_layer(shape: LayerShape, seed: int, codes: str = "quantized",
     else:
         for e, job in enumerate(jobs):
             records[slot_of[e]] = _expert_record(job)
-    return Layer(shape, router_w, bias, records, slot_of)
+    gate = None
+    if shape.shared_gate and shape.has_shared:
+        gate = (np.random.default_rng(np.random.SeedSequence(seed).spawn(4 + nrec)[3 + nrec])
+                .standard_normal(shape.hidden, dtype=np.float32) * np.float32(shape.router_std))
+    return Layer(shape, router_w, bias, records, slot_of, gate)
 
 
 def make_tokens(H: int, T: int, seed: int, std: float = 1.0) -> np.ndarray:
