@@ -88,7 +88,7 @@ typedef struct {
   int32_t intermediate;      /* I, multiple of 32 */
   int32_t num_experts;       /* E routed experts, 1..1024 */
   int32_t top_k;             /* k, 1..min(E, 32) */
-  int32_t group_size;        /* G, 64 or 128 (codes per FP16 scale along K) */
+  int32_t group_size;        /* G, 32, 64 or 128 (codes per FP16 scale along K) */
   int32_t renormalize;       /* 0: w = softmax over all E; 1: w renormalised over the top k */
   int32_t has_shared_expert; /* 1: record index E is a shared expert run on every token, weight 1 */
   int32_t max_tokens;        /* upper bound of T; workspace is sized for it at create */
@@ -107,6 +107,10 @@ typedef struct {
   int32_t spare_slots;
   int32_t staging_records;
   int32_t cache_policy;
+  /* 1: asymmetric quantisation, w = (q - z) * s with one zero code z (0..15)
+   * per group, one byte each, in three record sections after the scales
+   * (moe_record_bytes_zp, moe_record_section 6..8); 0: z = 8. */
+  int32_t zero_points;
 } moe_layer_config_t;
 
 typedef enum {
@@ -125,6 +129,9 @@ typedef struct {
   const void* host_backing;      /* PARTIAL: host memory, [E (+1)] records back to back, registered
                                     (pinned) by the library for the handle's lifetime and never
                                     written. FULL: must be NULL. */
+  const float* shared_gate;      /* device FP32 [H]: the shared expert's output is weighted per token
+                                    by sigmoid(x . shared_gate); NULL: weight 1. Needs a shared
+                                    expert. */
 } moe_layer_weights_t;
 
 typedef struct moe_layer moe_layer_t;
@@ -164,8 +171,13 @@ int32_t moe_abi_version(void);
 /* Padded size in bytes of one canonical expert record; 0 for an invalid shape. */
 size_t moe_record_bytes(int32_t hidden, int32_t intermediate, int32_t group_size);
 
+/* Padded size of one record with (zero_points = 1) or without zero-point
+ * sections; 0 for an invalid shape. */
+size_t moe_record_bytes_zp(int32_t hidden, int32_t intermediate, int32_t group_size, int32_t zero_points);
+
 /* Byte offset and size of section `section` (0 gate_q, 1 up_q, 2 down_q,
- * 3 gate_s, 4 up_s, 5 down_s) inside one record. */
+ * 3 gate_s, 4 up_s, 5 down_s, and in a record with zero points 6 gate_z,
+ * 7 up_z, 8 down_z) inside one record. */
 moe_status_t moe_record_section(int32_t hidden, int32_t intermediate, int32_t group_size,
                                 int32_t section, size_t* offset, size_t* bytes);
 

@@ -37,7 +37,8 @@ def stream():
 
 def oracle_kw(shape):
     return dict(H=shape.hidden, I=shape.intermediate, E=shape.num_experts, k=shape.top_k,
-                G=shape.group_size, renormalize=shape.renormalize, has_shared=shape.has_shared)
+                G=shape.group_size, renormalize=shape.renormalize, has_shared=shape.has_shared,
+                zero_points=shape.zero_points)
 
 
 def upload(lay: synth.Layer, max_tokens: int, add_residual: bool = False) -> MoELayer:
@@ -47,10 +48,12 @@ def upload(lay: synth.Layer, max_tokens: int, add_residual: bool = False) -> MoE
     e2s = torch.from_numpy(lay.expert_to_slot.astype(np.int32)).to(dev)
     rw = torch.from_numpy(lay.router_w).to(dev)
     rb = torch.from_numpy(lay.router_bias).to(dev) if lay.router_bias is not None else None
+    gate = torch.from_numpy(lay.shared_gate).to(dev) if lay.shared_gate is not None else None
     return MoELayer(hidden=s.hidden, intermediate=s.intermediate, num_experts=s.num_experts, top_k=s.top_k,
                     group_size=s.group_size, renormalize=s.renormalize, has_shared=s.has_shared,
                     max_tokens=max_tokens, router_w=rw, router_bias=rb, pool=pool, expert_to_slot=e2s,
-                    num_slots=pool.shape[0], add_residual=add_residual)
+                    num_slots=pool.shape[0], add_residual=add_residual, zero_points=s.zero_points,
+                    shared_gate=gate)
 
 
 def run(ml: MoELayer, x_np: np.ndarray):
@@ -78,7 +81,7 @@ def compare(lay: synth.Layer, x_np: np.ndarray, g: dict, tokens=None, tol: float
     kw = oracle_kw(s)
     T = x_np.shape[0]
     ref = O.moe_forward(x_np, lay.router_w, lay.router_bias, lay.records, lay.expert_to_slot,
-                        tokens=tokens, **kw)
+                        tokens=tokens, shared_gate=lay.shared_gate, **kw)
     near = set(O.near_tie_tokens(ref["logits"], s.top_k, TIE_EPS).tolist())
     decided = np.array([t for t in range(T) if t not in near], dtype=np.int64)
     # routing: ids bit-exact where decided
@@ -101,7 +104,8 @@ def compare(lay: synth.Layer, x_np: np.ndarray, g: dict, tokens=None, tol: float
         sub = toks[nt_rows]
         out_ref[nt_rows] = O.expert_combine(x_np, g["ids"], w_ref, lay.records, lay.expert_to_slot,
                                             H=s.hidden, I=s.intermediate, E=s.num_experts, k=s.top_k,
-                                            G=s.group_size, has_shared=s.has_shared, tokens=sub)
+                                            G=s.group_size, has_shared=s.has_shared, tokens=sub,
+                                            zero_points=s.zero_points, shared_gate=lay.shared_gate)
     got = g["out"][toks]
     err = np.abs(got - out_ref)
     bound = tol * np.maximum(1.0, np.abs(out_ref))

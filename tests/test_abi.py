@@ -56,6 +56,16 @@ def test_record_layout_agrees_with_oracle_and_generator(lib, H, I, G):
         assert capi.record_section(H, I, G, i) == offs[name]
 
 
+@pytest.mark.parametrize("H,I,G", [(2048, 1024, 32), (2880, 2880, 128), (256, 512, 64)])
+def test_zero_point_record_layout_matches_generator(lib, H, I, G):
+    offs = synth.section_layout(H, I, G, zero_points=True)
+    assert lib.moe_record_bytes_zp(H, I, G, 1) == offs["record_bytes"]
+    assert lib.moe_record_bytes_zp(H, I, G, 0) == synth.record_bytes(H, I, G) == lib.moe_record_bytes(H, I, G)
+    names = ("gate_q", "up_q", "down_q", "gate_s", "up_s", "down_s", "gate_z", "up_z", "down_z")
+    for i, name in enumerate(names):
+        assert capi.record_section(H, I, G, i) == offs[name]
+
+
 def test_host_side_validation_and_errors(lib):
     assert lib.moe_layer_destroy(None) == capi.MOE_OK
     assert lib.moe_record_bytes(0, 128, 64) == 0
@@ -72,9 +82,12 @@ def test_host_side_validation_and_errors(lib):
     cfg.top_k = 9
     assert lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
     cfg.top_k = 2
-    cfg.group_size = 32
+    cfg.group_size = 48
     assert lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_UNSUPPORTED
     cfg.group_size = 64
+    cfg.zero_points = 2
+    assert lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
+    cfg.zero_points = 0
     w.slot_pool = 100  # not 256-byte aligned
     assert lib.moe_layer_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)) == capi.MOE_ERR_INVALID_ARG
     # partial residency with too few slots for one token's experts

@@ -31,13 +31,13 @@ class moe_layer_config_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "hidden", "intermediate", "num_experts", "top_k", "group_size", "renormalize",
         "has_shared_expert", "max_tokens", "num_slots", "residency", "add_residual", "spare_slots",
-        "staging_records", "cache_policy")]
+        "staging_records", "cache_policy", "zero_points")]
 
 
 class moe_layer_weights_t(ctypes.Structure):
     _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
                 ("slot_pool", ctypes.c_void_p), ("expert_to_slot", ctypes.c_void_p),
-                ("host_backing", ctypes.c_void_p)]
+                ("host_backing", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p)]
 
 
 class moe_layer_stats_t(ctypes.Structure):
@@ -68,6 +68,7 @@ _I32 = ctypes.c_int32
 PROTOTYPES = {
     "moe_abi_version": (_I32, []),
     "moe_record_bytes": (ctypes.c_size_t, [_I32, _I32, _I32]),
+    "moe_record_bytes_zp": (ctypes.c_size_t, [_I32, _I32, _I32, _I32]),
     "moe_record_section": (_I32, [_I32, _I32, _I32, _I32, ctypes.POINTER(ctypes.c_size_t),
                                   ctypes.POINTER(ctypes.c_size_t)]),
     "moe_layer_create": (_I32, [ctypes.POINTER(moe_layer_config_t), ctypes.POINTER(moe_layer_weights_t),

@@ -540,7 +540,7 @@ bool coop_pdl_probe_once() {
 
 size_t decode_smem_bytes(const DecodeArgs& a, int stages) { return decode_smem_layout(a, stages).total; }
 
-TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes) {
+TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes, bool zp) {
   TcGemvPlan p;
   const int mats = dual ? 2 : 1;
   p.rb = 16;
@@ -553,7 +553,8 @@ TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes) {
   p.code_mat_bytes = (uint32_t)p.nbox * 128u * (uint32_t)p.rb;
   const int ng = (K + G - 1) / G;
   p.sstride = ((uint32_t)p.rb * ng * 2u + 15u) & ~15u;
-  p.slot_bytes = ((uint32_t)mats * (p.code_mat_bytes + p.sstride) + 1023u) & ~1023u;
+  p.zstride = zp ? (((uint32_t)p.rb * ng + 15u) & ~15u) : 0u;
+  p.slot_bytes = ((uint32_t)mats * (p.code_mat_bytes + p.sstride + p.zstride) + 1023u) & ~1023u;
   return p;
 }
 

@@ -134,13 +134,13 @@ __device__ __forceinline__ int find_segment(const int* prefix, int nseg, int t) 
   return lo;
 }
 
-// (q - 8) * s for the 8 codes of one word (k = 8i .. 8i+7), as 8 FP16 in
+// (q - z) * s for the 8 codes of one word (k = 8i .. 8i+7), as 8 FP16 in
 // k order. Codes k=2b (low nibble) and 2b+1 (high nibble) of byte b become
 // the half pair {1024 + q_lo, 1024 + q_hi} via the exponent-bias trick, then
-// (h - 1032) is exact and one multiply by the FP16 scale rounds once.
-__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
+// (h - (1024 + z)) is exact and one multiply by the FP16 scale rounds once
+// (z = 8 without zero points: bias = 1032).
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2, __half2 bias) {
   const uint32_t hi = w >> 4;
-  const __half2 bias = __half2half2(__ushort_as_half(0x6408));  // 1032
   uint32_t out[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
@@ -374,13 +374,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int slot = a.expert_to_slot[e];
       if (slot < 0 || slot >= a.num_slots) slot = 0;
       const bool rvalid = m0 + unit < a.N;
-      const __half* sp = reinterpret_cast<const __half*>(a.pool + (size_t)slot * a.record_bytes +
-                                                         (upper ? a.s_off1 : a.s_off0)) +
+      const uint8_t* recp = a.pool + (size_t)slot * a.record_bytes;
+      const __half* sp = reinterpret_cast<const __half*>(recp + (upper ? a.s_off1 : a.s_off0)) +
                          (size_t)(m0 + unit) * a.ng;
+      const uint8_t* zrow = recp + (upper ? a.z_off1 : a.z_off0) + (size_t)(m0 + unit) * a.ng;
       const int ngroups = (nK + kCodeK - 1) / kCodeK;
-      // this row's scale for the group's next K step, loaded one step ahead
-      // so its latency overlaps the current step's conversion
-      __half sv_next = (rvalid && par < nK) ? __ldg(sp + (par * BK) / a.G) : __float2half(0.f);
+      // this row's scales (and zero points) for the group's next K step,
+      // loaded one step ahead so their latency overlaps the current step's
+      // conversion; a step of BK codes is one group, or two at G = 32 (its
+      // first 32 codes in the first, the rest in the second)
+      const bool two = a.G < BK;
+      auto step_params = [&](int kk, uint32_t& s_pair, uint32_t& z_pair) {
+        const int gi = (kk * BK) / a.G;
+        const __half s0 = __ldg(sp + gi), s1 = two ? __ldg(sp + gi + 1) : s0;
+        s_pair = (uint32_t)__half_as_ushort(s0) | ((uint32_t)__half_as_ushort(s1) << 16);
+        uint32_t z0 = 8u, z1 = 8u;
+        if (a.zp) {
+          z0 = __ldg(zrow + gi);
+          z1 = two ? (uint32_t)__ldg(zrow + gi + 1) : z0;
+        }
+        z_pair = z0 | (z1 << 16);
+      };
+      uint32_t sv_next = 0u, zv_next = 0x00080008u;
+      if (rvalid && par < nK) step_params(par, sv_next, zv_next);
       for (int grp = 0; grp < ngroups && ok; ++grp, ++gc) {
         const int sc = gc % kCodeStages;
         int good = 1;
@@ -396,8 +412,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int kk = grp * kCodeK + par; kk < k_end; kk += 2) {
           const uint32_t g = gbase + (uint32_t)kk;
           const int sa = g % kAStages;
-          const __half sv = sv_next;
-          if (rvalid && kk + 2 < nK) sv_next = __ldg(sp + ((kk + 2) * BK) / a.G);
+          const uint32_t sv = sv_next, zv = zv_next;
+          if (rvalid && kk + 2 < nK) step_params(kk + 2, sv_next, zv_next);
           if (lane == 0)
             good = timed_wait(&B.a_empty[sa], ((g / kAStages) & 1u) ^ 1u, abort_flag, a.err, rec ? &dw[1] : nullptr);
           good = __shfl_sync(0xffffffffu, good, 0);
@@ -411,11 +427,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint4 w0 = *reinterpret_cast<const uint4*>(crowp + ((cc ^ (crow & 7)) << 4));
           const uint4 w1 = *reinterpret_cast<const uint4*>(crowp + (((cc + 1) ^ (crow & 7)) << 4));
           unsigned char* rowp = smem + L::off_a + (uint32_t)sa * L::a_tile + r * (BK * 2);
-          const __half2 s2 = __half2half2(sv);
+          const __half2 s_lo = __half2half2(__ushort_as_half((unsigned short)(sv & 0xFFFFu)));
+          const __half2 s_hi = __half2half2(__ushort_as_half((unsigned short)(sv >> 16)));
+          // 1024 + z: exponent-bias form of the zero point (exact)
+          const __half2 b_lo = __half2half2(__ushort_as_half((unsigned short)(0x6400u + (zv & 0xFFFFu))));
+          const __half2 b_hi = __half2half2(__ushort_as_half((unsigned short)(0x6400u + (zv >> 16))));
           const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
           for (int c = 0; c < 8; ++c)  // 16-byte chunk c (8 halves) of the 128-byte A row
-            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = dequant8(words[c], s2);
+            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) =
+                dequant8(words[c], c < 4 ? s_lo : s_hi, c < 4 ? b_lo : b_hi);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&B.a_full[sa]);

@@ -33,15 +33,17 @@ struct GemvHdr {
 static_assert(sizeof(GemvHdr) <= kHdrBytes, "GEMV header exceeds its reserved bytes");
 
 struct GemvSmem {
-  uint32_t ring, bs, cs, red, total;
+  uint32_t ring, bs, cs, xs, red, total;
 };
 GemvSmem __host__ __device__ inline gemv_smem_layout(const TcGemvLaunch& p) {
   GemvSmem L;
   const uint32_t ns = (uint32_t)p.ns;
+  const uint32_t csb = ((uint32_t)p.cs_groups * ns * 4u + 15u) & ~15u;
   L.ring = kHdrBytes;  // rounded up to 1024 in the kernel (slack below)
   L.bs = L.ring + 1024u + (uint32_t)p.stages * p.slot_bytes;
   L.cs = L.bs + (uint32_t)p.bs_chunks * ns * 64u;
-  L.red = L.cs + (((uint32_t)p.cs_groups * ns * 4u + 15u) & ~15u);
+  L.xs = L.cs + csb;  // group activation sums (zero points)
+  L.red = L.xs + (p.a.zp ? csb : 0u);
   L.total = L.red + ((2u * (uint32_t)tc_red_words((int)ns) * 4u + 15u) & ~15u);
   return L;
 }
@@ -57,6 +59,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) k_tcgemv(const __grid_cons
   unsigned char* ring = smem + (((sbase + lay.ring + 1023u) & ~1023u) - sbase);
   uint4* Bs = reinterpret_cast<uint4*>(smem + lay.bs);
   float* Cs = reinterpret_cast<float*>(smem + lay.cs);
+  float* Xs = p.a.zp ? reinterpret_cast<float*>(smem + lay.xs) : nullptr;
   float* red = reinterpret_cast<float*>(smem + lay.red);
 
   if (tid == 0) {
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) k_tcgemv(const __grid_cons
         const int ntok = min(kTcMaxTok, cnt - tb);
         if (sgi != b_seg || tb != b_tb) {
           tc_bar();  // every consumer warp is done with the previous B fragments
-          tc_build_b<false>(a, sgi, tb, ntok, NS, Bs, Cs, tid);
+          tc_build_b<false>(a, sgi, tb, ntok, NS, Bs, Cs, tid, Xs);
           b_seg = sgi;
           b_tb = tb;
           tc_bar();
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 1) k_tcgemv(const __grid_cons
         // the finisher has read this buffer (token tile ti - 2)
         if (lane == 0) mbar_wait(&hdr->red.free_[b], ((uint32_t)(ti >> 1) & 1u) ^ 1u, &hdr->abort_flag, a.err);
         __syncwarp();
-        tc_compute<DUAL>(a, slot, Bs, Cs, ntok, NS, red + b * tc_red_words(NS), warp, lane);
+        tc_compute<DUAL>(a, slot, Bs, Cs, ntok, NS, red + b * tc_red_words(NS), warp, lane, Xs);
         __syncwarp();
         if (lane == 0) mbar_arrive(&hdr->red.full[b]);
         ++ti;
@@ -172,6 +175,23 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
   pdl_wait();
   const int t = blockIdx.y;
   const int h4 = blockIdx.x * 256 + threadIdx.x;
+  // gated shared expert: weight sigmoid(x_t . gate), the dot product summed
+  // by every block of the token in the same fixed order (threads strided
+  // over H, then the block's tree)
+  float gw = 1.f;
+  if (a.has_shared && a.gate) {
+    __shared__ float part[256];
+    float d = 0.f;
+    for (int h = threadIdx.x; h < a.H; h += 256)
+      d = fmaf(__half2float(a.xin[(size_t)t * a.H + h]), __ldg(a.gate + h), d);
+    part[threadIdx.x] = d;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+      if (threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
+      __syncthreads();
+    }
+    gw = 1.f / (1.f + expf(-part[0]));
+  }
   if (4 * h4 >= a.H) return;
   const int Tk = a.T * a.k;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -185,10 +205,17 @@ __global__ void __launch_bounds__(256) k_combine(CombineArgs a) {
   }
   if (a.has_shared) {
     const float4 y = __ldcg(reinterpret_cast<const float4*>(a.ypart + ((size_t)Tk + t) * a.H) + h4);
-    acc.x += y.x;
-    acc.y += y.y;
-    acc.z += y.z;
-    acc.w += y.w;
+    if (a.gate) {
+      acc.x = fmaf(gw, y.x, acc.x);
+      acc.y = fmaf(gw, y.y, acc.y);
+      acc.z = fmaf(gw, y.z, acc.z);
+      acc.w = fmaf(gw, y.w, acc.w);
+    } else {
+      acc.x += y.x;
+      acc.y += y.y;
+      acc.z += y.z;
+      acc.w += y.w;
+    }
   }
   __half2 o01 = __floats2half2_rn(acc.x, acc.y);
   __half2 o23 = __floats2half2_rn(acc.z, acc.w);

@@ -63,6 +63,8 @@ struct GemmArgs {
   int num_slots;
   long long s_off0, s_off1;     // scale sections (gate, up) or (down, -)
   int N, K, G, ng;
+  int zp;                       // 1: zero-point sections (one byte per group)
+  long long z_off0, z_off1;     // zero-point sections (gate, up) or (down, -)
   const int32_t* num_seg;
   const int32_t* seg_expert;
   const int32_t* seg_start;
@@ -102,6 +104,9 @@ struct TcGemvArgs {
   int nbox;                     // ceil(K / 256) code boxes per matrix row
   uint32_t code_mat_bytes;      // nbox * 128 * rb
   uint32_t sstride;             // scale bytes per matrix in a slot (16-byte multiple)
+  int zp;                       // 1: zero-point sections (one code per group, one byte each)
+  long long z_off0, z_off1;     // zero-point sections (gate, up) or (down, -)
+  uint32_t zstride;             // zero-point bytes per matrix in a slot (16-byte multiple)
   const int32_t* seg_expert;
   const int32_t* seg_start;
   const int32_t* seg_count;
@@ -117,11 +122,12 @@ struct TcGemvArgs {
 
 struct TcGemvPlan {
   int rb, rt, kparts, lkparts, nbox;
-  uint32_t code_mat_bytes, sstride, slot_bytes;  // slot_bytes: multiple of 1024
+  uint32_t code_mat_bytes, sstride, zstride, slot_bytes;  // slot_bytes: multiple of 1024
 };
 // Items of about item_bytes code bytes with rb a power-of-two multiple of 16
-// and rb / 16 <= 8. Requires K % 32 == 0, G % 32 == 0, N % 16 == 0.
-TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes);
+// and rb / 16 <= 8. Requires K % 32 == 0, G % 32 == 0, N % 16 == 0. A slot
+// holds the codes, the scale rows and (zp) the zero-point rows.
+TcGemvPlan plan_tcgemv(int N, int K, int G, bool dual, int item_bytes, bool zp);
 // 3-D map {K / 2 bytes, N rows, slots} of one code section, 128-byte boxes of
 // box_rows rows, 128-byte swizzle.
 bool encode_tcgemv_map(CUtensorMap* tm, const void* pool_section, int K, int N, int num_slots, size_t record_bytes,
@@ -171,6 +177,8 @@ struct CombineArgs {
   const __half* x;      // residual input or nullptr
   __half* out;          // [T][H]
   int T, H, k, has_shared;
+  const float* gate;    // shared expert gate vector [H] (weight sigmoid(x . gate)) or nullptr (weight 1)
+  const __half* xin;    // the layer input [T][H] (for the gate)
 };
 
 // Launch shape of one grouped-GEMV launch, chosen on the host.

@@ -27,19 +27,29 @@ inline void prof_record(cudaEvent_t ev, cudaStream_t s) {
 }
 
 struct Layout {
-  size_t off[6];
-  size_t size[6];
+  size_t off[9];   // gate_q, up_q, down_q, gate_s, up_s, down_s (, gate_z, up_z, down_z)
+  size_t size[9];
   size_t record;
   size_t payload;
+  bool zp = false;
 };
 
-inline bool record_layout(int H, int I, int G, Layout* L) {
+// The canonical record: each section on a 256-byte boundary; with zero
+// points, one byte per group of each matrix in three sections after the
+// scales.
+inline bool record_layout(int H, int I, int G, bool zp, Layout* L) {
   if (H <= 0 || I <= 0 || G <= 0 || (H % 2) || (I % 2)) return false;
   const size_t gh = (size_t)(H + G - 1) / G, gi = (size_t)(I + G - 1) / G;
-  const size_t sizes[6] = {(size_t)I * H / 2, (size_t)I * H / 2, (size_t)H * I / 2,
-                           2 * (size_t)I * gh,  2 * (size_t)I * gh,  2 * (size_t)H * gi};
+  const size_t sizes[9] = {(size_t)I * H / 2, (size_t)I * H / 2, (size_t)H * I / 2,
+                           2 * (size_t)I * gh,  2 * (size_t)I * gh,  2 * (size_t)H * gi,
+                           (size_t)I * gh,      (size_t)I * gh,      (size_t)H * gi};
+  const int n = zp ? 9 : 6;
   size_t cur = 0, payload = 0;
-  for (int i = 0; i < 6; ++i) {
+  for (int i = 0; i < 9; ++i) {
+    L->off[i] = 0;
+    L->size[i] = 0;
+  }
+  for (int i = 0; i < n; ++i) {
     cur = align256(cur);
     L->off[i] = cur;
     L->size[i] = sizes[i];
@@ -48,6 +58,7 @@ inline bool record_layout(int H, int I, int G, Layout* L) {
   }
   L->record = align256(cur);
   L->payload = payload;
+  L->zp = zp;
   return true;
 }
 
@@ -86,6 +97,7 @@ struct moe_layer {
   int32_t* ids_stage = nullptr;
   float* w_stage = nullptr;
   int last_T = 0;
+  bool variant = false;          // zero points, G = 32 or a gated shared expert: the multi-kernel path only
   bool decode1 = true;           // batch-1 decode kernel (full residency, T == 1)
   bool megakernel = true;        // single-launch decode (full residency)
   int megakernel_max_tokens = 4;  // largest T it takes (<= 16); measured faster than the multi-kernel path up to 4

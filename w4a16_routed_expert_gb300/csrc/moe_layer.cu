@@ -43,8 +43,11 @@ moe_status_t validate(const moe_layer_config_t* c, const moe_layer_weights_t* w)
     return fail(MOE_ERR_UNSUPPORTED, "hidden=%d: supported 128..4096, multiple of 32", c->hidden);
   if (c->intermediate < 128 || c->intermediate > 4096 || c->intermediate % 32)
     return fail(MOE_ERR_UNSUPPORTED, "intermediate=%d: supported 128..4096, multiple of 32", c->intermediate);
-  if (c->group_size != 64 && c->group_size != 128)
-    return fail(MOE_ERR_UNSUPPORTED, "group_size=%d: supported 64 or 128", c->group_size);
+  if (c->group_size != 32 && c->group_size != 64 && c->group_size != 128)
+    return fail(MOE_ERR_UNSUPPORTED, "group_size=%d: supported 32, 64 or 128", c->group_size);
+  if (c->zero_points != 0 && c->zero_points != 1) return fail(MOE_ERR_INVALID_ARG, "zero_points must be 0 or 1");
+  if (w && w->shared_gate && !c->has_shared_expert)
+    return fail(MOE_ERR_INVALID_ARG, "shared_gate needs has_shared_expert = 1");
   if (c->num_experts < 1 || c->num_experts > 1024)
     return fail(MOE_ERR_INVALID_ARG, "num_experts=%d out of 1..1024", c->num_experts);
   if (c->top_k < 1 || c->top_k > 32 || c->top_k > c->num_experts)
@@ -127,16 +130,21 @@ extern "C" {
 int32_t moe_abi_version(void) { return MOE_ABI_VERSION; }
 
 size_t moe_record_bytes(int32_t hidden, int32_t intermediate, int32_t group_size) {
+  return moe_record_bytes_zp(hidden, intermediate, group_size, 0);
+}
+
+size_t moe_record_bytes_zp(int32_t hidden, int32_t intermediate, int32_t group_size, int32_t zero_points) {
   Layout L;
-  if (!record_layout(hidden, intermediate, group_size, &L)) return 0;
+  if ((zero_points != 0 && zero_points != 1) || !record_layout(hidden, intermediate, group_size, zero_points != 0, &L))
+    return 0;
   return L.record;
 }
 
 moe_status_t moe_record_section(int32_t hidden, int32_t intermediate, int32_t group_size, int32_t section,
                                 size_t* offset, size_t* bytes) {
   Layout L;
-  if (!record_layout(hidden, intermediate, group_size, &L)) return fail(MOE_ERR_INVALID_ARG, "invalid shape");
-  if (section < 0 || section > 5) return fail(MOE_ERR_INVALID_ARG, "section %d out of 0..5", section);
+  if (!record_layout(hidden, intermediate, group_size, true, &L)) return fail(MOE_ERR_INVALID_ARG, "invalid shape");
+  if (section < 0 || section > 8) return fail(MOE_ERR_INVALID_ARG, "section %d out of 0..8", section);
   if (offset) *offset = L.off[section];
   if (bytes) *bytes = L.size[section];
   return MOE_OK;
@@ -157,7 +165,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
   if (!L) return fail(MOE_ERR_OOM, "host allocation failed");
   L->cfg = *config;
   L->w = *weights;
-  record_layout(config->hidden, config->intermediate, config->group_size, &L->lay);
+  record_layout(config->hidden, config->intermediate, config->group_size, config->zero_points != 0, &L->lay);
+  L->variant = config->zero_points != 0 || config->group_size == 32 || weights->shared_gate != nullptr;
   L->n_records = config->num_experts + config->has_shared_expert;
   const char* pdl_env = getenv("MOE_PDL");
   L->pdl = !(pdl_env && pdl_env[0] == '0');
@@ -244,8 +253,8 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
     // (MOE_GEMV_ITEM_BYTES overrides, for tuning)
     int item_bytes = 65536;
     if (const char* ib = getenv("MOE_GEMV_ITEM_BYTES")) item_bytes = std::max(4096, std::min(131072, atoi(ib)));
-    L->dec_pg = moe::plan_tcgemv(I, H, config->group_size, true, item_bytes);
-    L->dec_pd = moe::plan_tcgemv(H, I, config->group_size, false, item_bytes);
+    L->dec_pg = moe::plan_tcgemv(I, H, config->group_size, true, item_bytes, config->zero_points != 0);
+    L->dec_pd = moe::plan_tcgemv(H, I, config->group_size, false, item_bytes, config->zero_points != 0);
     if (config->residency == MOE_RESIDENCY_FULL) {
       const uint8_t* pool = static_cast<const uint8_t*>(weights->slot_pool);
       moe::encode_pool_maps(L, pool, config->num_slots, &L->pool_maps);
@@ -329,6 +338,9 @@ moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, 
   ga.K = H;
   ga.G = G;
   ga.ng = (H + G - 1) / G;
+  ga.zp = L->lay.zp ? 1 : 0;
+  ga.z_off0 = L->lay.off[6];
+  ga.z_off1 = L->lay.off[7];
   ga.num_seg = seg.num_seg;
   ga.seg_expert = seg.seg_expert;
   ga.seg_start = seg.seg_start;
@@ -346,6 +358,8 @@ moe_status_t enqueue_gemm(moe_layer* L, const __half* x, int T, cudaStream_t s, 
   GemmArgs gb = ga;
   gb.s_off0 = L->lay.off[5];
   gb.s_off1 = L->lay.off[5];
+  gb.z_off0 = L->lay.off[8];
+  gb.z_off1 = L->lay.off[8];
   gb.N = H;
   gb.K = I;
   gb.ng = (I + G - 1) / G;
@@ -390,6 +404,10 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   a.nbox = pg.nbox;
   a.code_mat_bytes = pg.code_mat_bytes;
   a.sstride = pg.sstride;
+  a.zp = L->lay.zp ? 1 : 0;
+  a.z_off0 = L->lay.off[6];
+  a.z_off1 = L->lay.off[7];
+  a.zstride = pg.zstride;
   a.seg_expert = seg.seg_expert;
   a.seg_start = seg.seg_start;
   a.seg_count = seg.seg_count;
@@ -435,6 +453,9 @@ moe_status_t enqueue_experts(moe_layer* L, const __half* x, int T, cudaStream_t 
   b.nbox = pd.nbox;
   b.code_mat_bytes = pd.code_mat_bytes;
   b.sstride = pd.sstride;
+  b.z_off0 = L->lay.off[8];
+  b.z_off1 = 0;
+  b.zstride = pd.zstride;
   b.act = L->hbuf;
   b.act_gather = 0;
   b.h_out = nullptr;
@@ -642,6 +663,8 @@ moe_status_t enqueue_combine(moe_layer* L, const __half* x, int T, __half* out, 
   ca.H = c.hidden;
   ca.k = c.top_k;
   ca.has_shared = c.has_shared_expert;
+  ca.gate = L->w.shared_gate;
+  ca.xin = x;
   cudaError_t e = launch_combine(ca, s, L->pdl);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   if (L->profiling) prof_record(L->ev[4], s);
@@ -709,7 +732,10 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
   // programmatic dependent launch only on explicitly created streams
   const bool pdl_saved = layer->pdl;
   if (s == nullptr) layer->pdl = false;
-  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->decode1 && T == 1) {
+  // the single-launch decode kernels take the base format only (zero point
+  // 8, G of 64 or 128, an ungated shared expert); variants use the
+  // multi-kernel path
+  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->decode1 && !layer->variant && T == 1) {
     moe_status_t sd = moe::enqueue_decode1(layer, xh, oh, topk_ids, topk_w, s);
     if (sd != MOE_ERR_UNSUPPORTED) {
       layer->pdl = pdl_saved;
@@ -720,7 +746,8 @@ moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, voi
       return MOE_OK;
     }
   }
-  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->megakernel && T <= layer->megakernel_max_tokens) {
+  if (layer->cfg.residency == MOE_RESIDENCY_FULL && layer->megakernel && !layer->variant &&
+      T <= layer->megakernel_max_tokens) {
     moe_status_t sd = moe::enqueue_decode(layer, xh, T, oh, topk_ids, topk_w, s);
     if (sd != MOE_ERR_UNSUPPORTED) {
       layer->pdl = pdl_saved;

@@ -39,8 +39,8 @@ void free_stack(moe_stack* st) {
   delete st;
 }
 
-// Batch-1 single-launch eligibility: every layer fully resident, with the
-// batch-1 kernel enabled, and of the first layer's shape; the stack layout
+// Batch-1 single-launch eligibility: every layer fully resident in the base
+// format, with the batch-1 kernel enabled, and of the first layer's shape; the stack layout
 // fits in shared memory; the partial logits of E experts are summed by the
 // stack kernel (E <= 128).
 bool stack_kernel_fits(const moe_stack* st) {
@@ -53,7 +53,8 @@ bool stack_kernel_fits(const moe_stack* st) {
   if (c0.num_experts > 128 || L0->num_sms < 1) return false;
   for (const moe_layer* L : st->layers) {
     const moe_layer_config_t& c = L->cfg;
-    if (c.residency != MOE_RESIDENCY_FULL || !L->decode1 || L->num_sms != L0->num_sms || L->device != L0->device ||
+    if (c.residency != MOE_RESIDENCY_FULL || !L->decode1 || L->variant || L->num_sms != L0->num_sms ||
+        L->device != L0->device ||
         c.hidden != c0.hidden || c.intermediate != c0.intermediate || c.num_experts != c0.num_experts ||
         c.top_k != c0.top_k || c.group_size != c0.group_size || c.has_shared_expert != c0.has_shared_expert)
       return false;

@@ -118,7 +118,8 @@ __device__ __forceinline__ void tc_issue_item(const TcGemvArgs& a, const CUtenso
   const int r0 = rbi * a.rb;
   const int nrows = min(a.rb, a.N - r0);
   const uint32_t sbytes = (uint32_t)nrows * a.ng * 2u;
-  mbar_arrive_expect_tx(full, M * (a.code_mat_bytes + sbytes));
+  const uint32_t zbytes = a.zp ? (uint32_t)nrows * a.ng : 0u;  // a multiple of 16 (nrows is)
+  mbar_arrive_expect_tx(full, M * (a.code_mat_bytes + sbytes + zbytes));
   for (int b = 0; b < a.nbox; ++b) {
     tma_load_3d_hint(sb + b * 128u * a.rb, m0, b * 128, r0, slot, full, pol);
     if (DUAL) tma_load_3d_hint(sb + a.code_mat_bytes + b * 128u * a.rb, m1, b * 128, r0, slot, full, pol);
@@ -127,6 +128,12 @@ __device__ __forceinline__ void tc_issue_item(const TcGemvArgs& a, const CUtenso
   unsigned char* ss = sb + M * a.code_mat_bytes;
   bulk_g2s(ss, rec + a.s_off0 + (size_t)r0 * a.ng * 2, sbytes, full, pol);
   if (DUAL) bulk_g2s(ss + a.sstride, rec + a.s_off1 + (size_t)r0 * a.ng * 2, sbytes, full, pol);
+  if (a.zp) {
+    // zero-point rows after the scale blocks
+    unsigned char* zs = ss + M * a.sstride;
+    bulk_g2s(zs, rec + a.z_off0 + (size_t)r0 * a.ng, zbytes, full, pol);
+    if (DUAL) bulk_g2s(zs + a.zstride, rec + a.z_off1 + (size_t)r0 * a.ng, zbytes, full, pol);
+  }
 }
 
 // K-part partial sums in shared memory: per (consumer warp, matrix) a block
@@ -148,7 +155,7 @@ __device__ __forceinline__ void tc_bar() { asm volatile("bar.sync 1, %0;" ::"r"(
 // caller synchronises afterwards.
 template <bool COHERENT>
 __device__ __forceinline__ void tc_build_b(const TcGemvArgs& a, int sgi, int tb, int ntok, int NS, uint4* Bs,
-                                           float* Cs, int tc) {
+                                           float* Cs, int tc, float* Xs = nullptr) {
   const int K = a.K;
   const int nchunk = K >> 5, nch_pad = (nchunk + 1) & ~1;
   const int pos0 = a.seg_start[sgi] + tb;
@@ -193,21 +200,25 @@ __device__ __forceinline__ void tc_build_b(const TcGemvArgs& a, int sgi, int tb,
         }
     }
     Cs[q] = 1032.f * se + 72.f * so;
+    if (Xs) Xs[q] = se + so;  // the group's sum of activations (zero points)
   }
 }
 
 // One consumer warp's part of an item (row tile w / kparts, K part
 // w % kparts) for the current token tile; partial sums to red
 // ([warp][m][16 rows][NS tokens]). CPG = chunks per quantisation group
-// (G / 32, 2 or 4), so the group walk has a fixed trip count.
-template <bool DUAL, int CPG>
+// (G / 32: 1, 2 or 4), so the group walk has a fixed trip count. A step
+// loads one chunk pair (ldmatrix x4): half a group at G = 64 / 128, two
+// groups at G = 32. ZP: the group's zero point z enters as
+// sum_k (q - z) x_k = (D - C) + (8 - z) X, X the group's activation sum.
+template <bool DUAL, int CPG, bool ZP>
 __device__ __forceinline__ void tc_compute_g(const TcGemvArgs& a, const unsigned char* sb, const uint4* Bs,
-                                             const float* Cs, int ntok, int NS, float* red, int warp, int lane) {
+                                             const float* Cs, const float* Xs, int ntok, int NS, float* red,
+                                             int warp, int lane) {
   constexpr int M = DUAL ? 2 : 1;
   const int u = warp >> a.lkparts, kp = warp & (a.kparts - 1);
   const int g = lane >> 2, c = lane & 3;
   const int nchunk = a.K >> 5;
-  const int g0 = (kp * a.ng) >> a.lkparts, g1 = ((kp + 1) * a.ng) >> a.lkparts;
   // ldmatrix source of this lane: matrix lane / 8 = rows (mi & 1) * 8 + lane % 8 of chunk j + (mi >> 1).
   // Chunk pairs start at even j, so the pair's box is j / 8 and the
   // swizzled 16-byte column is ((j % 8) + (mi >> 1)) ^ (lane % 8).
@@ -216,6 +227,7 @@ __device__ __forceinline__ void tc_compute_g(const TcGemvArgs& a, const unsigned
   const uint32_t lbase = smem_u32(sb) + (uint32_t)(u * 16 + (mi & 1) * 8 + x7) * 128u;
   const uint32_t hx4 = (uint32_t)((hi ^ x7) << 4);  // (j % 8 + hi) ^ x7 = (j & 6) ^ (hi ^ x7) for even j
   const unsigned char* sc = sb + M * a.code_mat_bytes;
+  const unsigned char* zc = sc + M * a.sstride;  // zero-point rows (ZP)
   const bool has_tok = g < ntok;
   const uint4* bsl = Bs + g * 4 + c;  // token g, column group c; chunk j at + j * NS * 4
   const int bstep = NS * 4;
@@ -226,50 +238,102 @@ __device__ __forceinline__ void tc_compute_g(const TcGemvArgs& a, const unsigned
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[m][i] = 0.f;
 
-  // group by group: each chunk pair is loaded (ldmatrix + B fragments),
-  // dequantised and multiplied; one accumulator chain per matrix and group
-  for (int gi = g0; gi < g1; ++gi) {
-    float d[M][4];
+  // group epilogue: remove the offsets (and the zero points), apply the scales
+  auto epilogue = [&](int gi, const float (&d)[M][4]) {
+    const float cc0 = (2 * c < NS) ? Cs[gi * NS + 2 * c] : 0.f;
+    const float cc1 = (2 * c + 1 < NS) ? Cs[gi * NS + 2 * c + 1] : 0.f;
+    float x0 = 0.f, x1 = 0.f;
+    if (ZP) {
+      x0 = (2 * c < NS) ? Xs[gi * NS + 2 * c] : 0.f;
+      x1 = (2 * c + 1 < NS) ? Xs[gi * NS + 2 * c + 1] : 0.f;
+    }
 #pragma unroll
-    for (int m = 0; m < M; ++m)
+    for (int m = 0; m < M; ++m) {
+      const __half* scm = reinterpret_cast<const __half*>(sc + m * a.sstride);
+      const float s0 = __half2float(scm[rg * a.ng + gi]);
+      const float s8 = __half2float(scm[(rg + 8) * a.ng + gi]);
+      if (ZP) {
+        const unsigned char* zm = zc + m * a.zstride;
+        const float o0 = 8.f - (float)zm[rg * a.ng + gi], o8 = 8.f - (float)zm[(rg + 8) * a.ng + gi];
+        acc[m][0] = fmaf(s0, fmaf(o0, x0, d[m][0] - cc0), acc[m][0]);
+        acc[m][1] = fmaf(s0, fmaf(o0, x1, d[m][1] - cc1), acc[m][1]);
+        acc[m][2] = fmaf(s8, fmaf(o8, x0, d[m][2] - cc0), acc[m][2]);
+        acc[m][3] = fmaf(s8, fmaf(o8, x1, d[m][3] - cc1), acc[m][3]);
+      } else {
+        acc[m][0] = fmaf(s0, d[m][0] - cc0, acc[m][0]);
+        acc[m][1] = fmaf(s0, d[m][1] - cc1, acc[m][1]);
+        acc[m][2] = fmaf(s8, d[m][2] - cc0, acc[m][2]);
+        acc[m][3] = fmaf(s8, d[m][3] - cc1, acc[m][3]);
+      }
+    }
+  };
+
+  if constexpr (CPG == 1) {
+    // G = 32: a chunk pair is two groups; the K parts take pairs of groups
+    const int npair = (a.ng + 1) >> 1;
+    const int p0 = (kp * npair) >> a.lkparts, p1 = ((kp + 1) * npair) >> a.lkparts;
+    for (int pp = p0; pp < p1; ++pp) {
+      const int j = 2 * pp;  // chunk of group j; group j + 1 (if any) is chunk j + 1
+      float d0[M][4], d1[M][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) d[m][i] = 0.f;
-    const int jg = gi * CPG;
+      for (int m = 0; m < M; ++m)
 #pragma unroll
-    for (int pp = 0; pp < CPG / 2; ++pp) {
-      const int j = jg + 2 * pp;
-      if (j >= nchunk) break;  // short last group
+        for (int i = 0; i < 4; ++i) d0[m][i] = d1[m][i] = 0.f;
       uint4 b0 = make_uint4(0u, 0u, 0u, 0u), b1 = b0;
       if (has_tok) {
         b0 = bsl[j * bstep];
-        b1 = bsl[(j + 1) * bstep];
+        b1 = bsl[(j + 1) * bstep];  // zero past the last chunk (the fragments are padded to a pair)
       }
       const uint32_t off = lbase + (uint32_t)(j >> 3) * boxb + ((((uint32_t)j << 4) & 0x60u) ^ hx4);
 #pragma unroll
       for (int m = 0; m < M; ++m) {
         uint32_t r[4];
         ldmatrix_x4(r, off + (uint32_t)m * a.code_mat_bytes);
-        // r[0]: row g chunk j, r[1]: row g+8 chunk j, r[2]: row g chunk j+1, r[3]: row g+8 chunk j+1
         const DeqWord w0 = dequant_word(r[0]), w1 = dequant_word(r[1]);
-        mma_16816(d[m], w0.h04, w1.h04, w0.h15, w1.h15, b0.x, b0.y);
-        mma_16816(d[m], w0.h26, w1.h26, w0.h37, w1.h37, b0.z, b0.w);
+        mma_16816(d0[m], w0.h04, w1.h04, w0.h15, w1.h15, b0.x, b0.y);
+        mma_16816(d0[m], w0.h26, w1.h26, w0.h37, w1.h37, b0.z, b0.w);
         const DeqWord w2 = dequant_word(r[2]), w3 = dequant_word(r[3]);
-        mma_16816(d[m], w2.h04, w3.h04, w2.h15, w3.h15, b1.x, b1.y);
-        mma_16816(d[m], w2.h26, w3.h26, w2.h37, w3.h37, b1.z, b1.w);
+        mma_16816(d1[m], w2.h04, w3.h04, w2.h15, w3.h15, b1.x, b1.y);
+        mma_16816(d1[m], w2.h26, w3.h26, w2.h37, w3.h37, b1.z, b1.w);
       }
+      epilogue(j, d0);
+      if (j + 1 < a.ng) epilogue(j + 1, d1);
     }
-    // group epilogue: remove the offsets, apply the scales
-    const float cc0 = (2 * c < NS) ? Cs[gi * NS + 2 * c] : 0.f;
-    const float cc1 = (2 * c + 1 < NS) ? Cs[gi * NS + 2 * c + 1] : 0.f;
+  } else {
+    const int g0 = (kp * a.ng) >> a.lkparts, g1 = ((kp + 1) * a.ng) >> a.lkparts;
+    // group by group: each chunk pair is loaded (ldmatrix + B fragments),
+    // dequantised and multiplied; one accumulator chain per matrix and group
+    for (int gi = g0; gi < g1; ++gi) {
+      float d[M][4];
 #pragma unroll
-    for (int m = 0; m < M; ++m) {
-      const __half* scm = reinterpret_cast<const __half*>(sc + m * a.sstride);
-      const float s0 = __half2float(scm[rg * a.ng + gi]);
-      const float s8 = __half2float(scm[(rg + 8) * a.ng + gi]);
-      acc[m][0] = fmaf(s0, d[m][0] - cc0, acc[m][0]);
-      acc[m][1] = fmaf(s0, d[m][1] - cc1, acc[m][1]);
-      acc[m][2] = fmaf(s8, d[m][2] - cc0, acc[m][2]);
-      acc[m][3] = fmaf(s8, d[m][3] - cc1, acc[m][3]);
+      for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d[m][i] = 0.f;
+      const int jg = gi * CPG;
+#pragma unroll
+      for (int pp = 0; pp < CPG / 2; ++pp) {
+        const int j = jg + 2 * pp;
+        if (j >= nchunk) break;  // short last group
+        uint4 b0 = make_uint4(0u, 0u, 0u, 0u), b1 = b0;
+        if (has_tok) {
+          b0 = bsl[j * bstep];
+          b1 = bsl[(j + 1) * bstep];
+        }
+        const uint32_t off = lbase + (uint32_t)(j >> 3) * boxb + ((((uint32_t)j << 4) & 0x60u) ^ hx4);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          uint32_t r[4];
+          ldmatrix_x4(r, off + (uint32_t)m * a.code_mat_bytes);
+          // r[0]: row g chunk j, r[1]: row g+8 chunk j, r[2]: row g chunk j+1, r[3]: row g+8 chunk j+1
+          const DeqWord w0 = dequant_word(r[0]), w1 = dequant_word(r[1]);
+          mma_16816(d[m], w0.h04, w1.h04, w0.h15, w1.h15, b0.x, b0.y);
+          mma_16816(d[m], w0.h26, w1.h26, w0.h37, w1.h37, b0.z, b0.w);
+          const DeqWord w2 = dequant_word(r[2]), w3 = dequant_word(r[3]);
+          mma_16816(d[m], w2.h04, w3.h04, w2.h15, w3.h15, b1.x, b1.y);
+          mma_16816(d[m], w2.h26, w3.h26, w2.h37, w3.h37, b1.z, b1.w);
+        }
+      }
+      epilogue(gi, d);
     }
   }
   const int blk = tc_red_block(NS);
@@ -290,11 +354,22 @@ __device__ __forceinline__ void tc_compute_g(const TcGemvArgs& a, const unsigned
 
 template <bool DUAL>
 __device__ __forceinline__ void tc_compute(const TcGemvArgs& a, const unsigned char* sb, const uint4* Bs,
-                                           const float* Cs, int ntok, int NS, float* red, int warp, int lane) {
-  if (a.G == 64)
-    tc_compute_g<DUAL, 2>(a, sb, Bs, Cs, ntok, NS, red, warp, lane);
-  else
-    tc_compute_g<DUAL, 4>(a, sb, Bs, Cs, ntok, NS, red, warp, lane);
+                                           const float* Cs, int ntok, int NS, float* red, int warp, int lane,
+                                           const float* Xs = nullptr) {
+  if (a.zp) {
+    if (a.G == 32)
+      tc_compute_g<DUAL, 1, true>(a, sb, Bs, Cs, Xs, ntok, NS, red, warp, lane);
+    else if (a.G == 64)
+      tc_compute_g<DUAL, 2, true>(a, sb, Bs, Cs, Xs, ntok, NS, red, warp, lane);
+    else
+      tc_compute_g<DUAL, 4, true>(a, sb, Bs, Cs, Xs, ntok, NS, red, warp, lane);
+  } else if (a.G == 32) {
+    tc_compute_g<DUAL, 1, false>(a, sb, Bs, Cs, Xs, ntok, NS, red, warp, lane);
+  } else if (a.G == 64) {
+    tc_compute_g<DUAL, 2, false>(a, sb, Bs, Cs, Xs, ntok, NS, red, warp, lane);
+  } else {
+    tc_compute_g<DUAL, 4, false>(a, sb, Bs, Cs, Xs, ntok, NS, red, warp, lane);
+  }
 }
 
 // Outputs of an item's token tile from the K-part partials, by one warp (the

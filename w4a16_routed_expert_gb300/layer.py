@@ -31,13 +31,14 @@ class MoELayer:
     host_backing: cpu uint8 [E (+1)][record_bytes] (partial residency; pageable
     memory is copied through the library's pinned staging buffers);
     spare_slots / staging_records / cache_policy: partial residency, see
-    moe_layer_config_t.
+    moe_layer_config_t; zero_points: records with zero-point sections;
+    shared_gate: cuda fp32 [H] gate vector of the shared expert, or None.
     """
 
     def __init__(self, *, hidden, intermediate, num_experts, top_k, group_size, renormalize,
                  has_shared=False, max_tokens, router_w, router_bias=None, pool=None,
                  expert_to_slot=None, num_slots=None, host_backing=None, add_residual=False, spare_slots=0,
-                 staging_records=0, cache_policy=0):
+                 staging_records=0, cache_policy=0, zero_points=False, shared_gate=None):
         partial = host_backing is not None
         self.cfg = capi.moe_layer_config_t(
             hidden=hidden, intermediate=intermediate, num_experts=num_experts, top_k=top_k,
@@ -46,13 +47,14 @@ class MoELayer:
             num_slots=int(num_slots if num_slots is not None else (pool.shape[0] if pool is not None else 0)),
             residency=capi.MOE_RESIDENCY_PARTIAL if partial else capi.MOE_RESIDENCY_FULL,
             add_residual=int(bool(add_residual)), spare_slots=int(spare_slots),
-            staging_records=int(staging_records), cache_policy=int(cache_policy))
+            staging_records=int(staging_records), cache_policy=int(cache_policy),
+            zero_points=int(bool(zero_points)))
         self.weights = capi.moe_layer_weights_t(
             router_w=_ptr(router_w), router_bias=_ptr(router_bias),
             slot_pool=None if partial else _ptr(pool), expert_to_slot=None if partial else _ptr(expert_to_slot),
-            host_backing=_ptr(host_backing) if partial else None)
+            host_backing=_ptr(host_backing) if partial else None, shared_gate=_ptr(shared_gate))
         # keep the borrowed buffers alive for the handle's lifetime
-        self._keep = (router_w, router_bias, pool, expert_to_slot, host_backing)
+        self._keep = (router_w, router_bias, pool, expert_to_slot, host_backing, shared_gate)
         self.hidden, self.top_k, self.num_experts = hidden, top_k, num_experts
         self.handle = capi.moe_layer_create(self.cfg, self.weights)
 
