@@ -96,7 +96,7 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(const DecodeArgs& a, in
   L.cs = L.bs + (uint32_t)a.bs_chunks * ns * 64u;
   L.red = L.cs + (((uint32_t)a.cs_groups * ns * 4u + 15u) & ~15u);
   L.route = L.red + ((2u * (uint32_t)tc_red_words((int)ns) * 4u + 15u) & ~15u);
-  L.total = L.route + (5u * Tk + 8u * E + 74u) * 4u;
+  L.total = L.route + (5u * Tk + 8u * E + 77u) * 4u;  // (+3: alignment of the finish scratch)
   return L;
 }
 
@@ -135,7 +135,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   int32_t* s_sstart = s_sexp + E + 1;                              // [E+1]
   int32_t* s_scount = s_sstart + E + 1;                            // [E+1]
   int32_t* s_nseg = s_scount + E + 1;                              // [1] (+3 pad)
-  int32_t* s_scratch = s_nseg + 4;                                 // [Tk + 3E + 66]
+  // [Tk + 3E + 66], 16-byte aligned (the routing finish reads it 128 bits at a time)
+  int32_t* s_scratch = s_nseg + 4 + ((4u - ((smem_u32(s_nseg + 4) >> 2) & 3u)) & 3u);
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {

@@ -390,7 +390,29 @@ __device__ __forceinline__ void d1_layer(const Decode1Args& a, unsigned char* sm
       *issued = 0;
       fence_mbar_init();
     }
-    // programmatic dependent launch: nothing above touched global memory
+    if (!STACK) {
+      // Inputs that no earlier launch writes (the router rows, the slot map)
+      // and the tile list are requested / built before the wait on the
+      // previous launch, so their latency overlaps its tail.
+      const int rows0 = bid < E ? (E - 1 - bid) / grid + 1 : 0;
+      const int lines = H / 32;  // 128-byte lines of one FP32 router row
+      for (int q = tid; q < rows0 * lines; q += kD1Threads)
+        prefetch_l2(a.r.wr + (size_t)(bid + (q / lines) * grid) * H + (size_t)(q % lines) * 32);
+      if (warp == kD1Producer) {
+        if (lane == 0)
+          for (int cur = g0, t = 0; cur < g1 && t < mug; ++t) {
+            const int sq = cur / gpe;
+            const int pend = min(g1, (sq + 1) * gpe);
+            const int n8 = min(2, pend - cur);
+            tile_s[t] = sq;
+            tile_r0[t] = (cur - sq * gpe) * 8;
+            tile_n[t] = n8 * 8;
+            cur += n8;
+          }
+        for (int e = lane; e < E + a.r.has_shared; e += 32) e2s[e] = __ldg(a.expert_to_slot + e);
+      }
+    }
+    // programmatic dependent launch: nothing above wrote global memory
     pdl_trigger();
     pdl_wait();
     __syncthreads();
@@ -498,27 +520,17 @@ __device__ __forceinline__ void d1_layer(const Decode1Args& a, unsigned char* sm
       if (lane == 0) rpart[i * kLogitParts + warp] = v;
     }
   } else {
-    // epoch bases (read before this CTA arrives), the slot map, the token's
-    // words in fragment order (zero past H)
+    // epoch bases (read before this CTA arrives; the slot map and the tile
+    // list were built before the wait), the token's words in fragment order
+    // (zero past H)
     if (lane == 0) {
       s_base[0] = ld_relaxed(logits_ready);
       s_base[1] = ld_relaxed(gu_done);
-      // the tiles in one pass (walk_tiles' rule)
-      for (int cur = g0, t = 0; cur < g1 && t < mug; ++t) {
-        const int sq = cur / gpe;
-        const int pend = min(g1, (sq + 1) * gpe);
-        const int n8 = min(2, pend - cur);
-        tile_s[t] = sq;
-        tile_r0[t] = (cur - sq * gpe) * 8;
-        tile_n[t] = n8 * 8;
-        cur += n8;
-      }
       if (nu > mug) {
         record_error(a.r.err, MOE_DEV_ERR_BOUNDS);
         *abort_flag = 1;
       }
     }
-    for (int e = lane; e < E + a.r.has_shared; e += 32) e2s[e] = __ldg(a.expert_to_slot + e);
     for (int w = lane; w < nwg; w += 32)
       xb[w] = 8 * w < H ? b_frag(__ldg(reinterpret_cast<const uint4*>(a.r.x) + w)) : make_uint4(0u, 0u, 0u, 0u);
   }
@@ -680,6 +692,8 @@ __device__ __forceinline__ void d1_layer(const Decode1Args& a, unsigned char* sm
     const bool go = __shfl_sync(0xffffffffu, *abort_flag ? 0 : 1, 0);
     const uint64_t pol = l2_policy_evict_first();
     if (go && lane == 0) {
+      // from one lane, tile by tile: the copy engine serves requests in
+      // order, so the first tile lands (and its compute starts) first
       for (int u = 0; u < nu; ++u) {
         const int sq = tile_s[u], r0 = tile_r0[u];
         const uint32_t nb = (uint32_t)tile_n[u] * rowg;

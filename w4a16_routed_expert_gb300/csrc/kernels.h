@@ -53,6 +53,7 @@ struct RouteArgs {
   int32_t* num_seg;     // [1]
   uint32_t* ticket;     // [1], zero between launches
   uint32_t* err;        // [1]
+  unsigned long long* trace;  // nullable: per-CTA phase stamps of the small-batch routing kernel
 };
 
 // Grouped W4A16 GEMM over expert segments (prefill regime, tensor cores).

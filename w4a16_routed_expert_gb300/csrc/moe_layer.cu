@@ -706,6 +706,7 @@ moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_us
   ra.ticket = L->ticket;
   ra.err = L->err;
   const bool small = T <= moe::kSmallRouteMaxT && (size_t)T * c.hidden * 2 <= 200 * 1024;
+  ra.trace = small ? L->trace : nullptr;
   if (!small) ra.nsplit = moe::router_split(T, c.num_experts, c.hidden, L->num_sms);
   if (L->profiling) prof_record(L->ev[0], s);
   L->last_single = false;

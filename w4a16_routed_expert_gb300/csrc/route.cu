@@ -41,7 +41,10 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int e = blockIdx.x;
+  unsigned long long* tr = tid == 0 ? a.trace : nullptr;
+  trace_mark(tr, 0);
   pdl_wait();
+  trace_mark(tr, 1);
   {
     // partials into shared memory laid out as part[t][0][p] (E = 1 view)
     RouteArgs one = a;
@@ -50,6 +53,7 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
     warp_logit_partial(one, 0, warp, s_part);
   }
   __syncthreads();
+  trace_mark(tr, 2);
   if (tid < a.T) {
     float v = 0.f;
 #pragma unroll
@@ -62,14 +66,17 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
   __syncthreads();
   if (tid == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
   __syncthreads();
+  trace_mark(tr, 4);
   if (!s_last) return;
   __threadfence();
 
   // dynamic shared memory: the finish scratch (T*k + 3E + 66 ints), then
-  // the block top-k buffer (T*E + 2T + T*k floats)
+  // the block top-k buffer (block_topk_fbuf_floats)
   int32_t* scratch = reinterpret_cast<int32_t*>(smem);
-  float* fbuf = reinterpret_cast<float*>(scratch + a.T * a.k + 3 * a.E + 66);
-  route_finish_cta<NV>(a, scratch, s_scan, nullptr, nullptr, fbuf);
+  // (the top-k buffer takes 128-bit loads: its start rounded to 16 bytes)
+  float* fbuf = reinterpret_cast<float*>(scratch + ((a.T * a.k + 3 * a.E + 66 + 3) & ~3));
+  route_finish_cta<NV>(a, scratch, s_scan, nullptr, tr, fbuf);
+  trace_mark(tr, 5);
   if (tid == 0) *a.ticket = 0u;
 }
 
@@ -281,8 +288,8 @@ __global__ void __launch_bounds__(kScatterThreads) k_scatter(RouteArgs a) {
 
 template <int NV>
 cudaError_t launch_route_small_nv(const RouteArgs& a, cudaStream_t s, bool pdl) {
-  const size_t fbytes = ((size_t)a.T * a.k + 3 * (size_t)a.E + 66) * sizeof(int) +
-                        ((size_t)a.T * a.E + 2 * (size_t)a.T + (size_t)a.T * a.k) * sizeof(float);
+  const size_t fbytes = (((size_t)a.T * a.k + 3 * (size_t)a.E + 66 + 3) & ~(size_t)3) * sizeof(int) +
+                        (size_t)block_topk_fbuf_floats(a.T, a.E, a.k) * sizeof(float);
   cudaError_t e = ensure_smem(k_route_small<NV>, fbytes);
   if (e != cudaSuccess) return e;
   return launch_ex(k_route_small<NV>, dim3(a.E), dim3(kLogitParts * 32), fbytes, s, pdl, a);

@@ -370,24 +370,30 @@ __device__ __forceinline__ void finish_tiny(const RouteArgs& a, int32_t* s_ids, 
 // Softmax and top-k of all T tokens with every thread of the CTA (E <= 128):
 // the same results, bit for bit, as warp_softmax_topk, with the work spread
 // out. Each logit's rank (the number of logits of its token ahead of it:
-// larger, or equal with a lower id) is counted by 8 lanes over interleaved
-// eighths of the token's logits and summed with shuffles; ranks 0..k-1 are
-// the selection. The softmax maximum and denominator of a token are computed
-// by one warp exactly as in warp_softmax_topk. fbuf: T*E + 2T + T*k floats
-// of shared memory. Writes ids / weights to a.ids, a.w, the user buffers
-// (if any) and s_sel ([T][k], by rank).
+// larger, or equal with a lower id) is counted by one thread against its
+// token's row, read as broadcast 128-bit shared loads (rows padded to a
+// multiple of 4 with -inf, which never ranks ahead); ranks 0..k-1 are the
+// selection. The softmax maximum and denominator of a token are computed by
+// one warp exactly as in warp_softmax_topk. fbuf: T*E4 + 2T + T*k floats of
+// shared memory (E4 = E rounded up to a multiple of 4, block_topk_fbuf_floats).
+// Writes ids / weights to a.ids, a.w, the user buffers (if any) and s_sel
+// ([T][k], by rank).
+__host__ __device__ inline int block_topk_fbuf_floats(int T, int E, int k) {
+  return T * ((E + 3) & ~3) + 2 * T + T * k;
+}
 template <int NV>
 __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const float* part, float* fbuf,
                                                    int32_t* s_sel) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int T = a.T, E = a.E, k = a.k, n = T * E;
-  float* lg = fbuf;       // [T][E]
-  float* mx = lg + n;     // [T]
+  const int T = a.T, E = a.E, k = a.k, E4 = (E + 3) & ~3, n4 = T * E4;
+  float* lg = fbuf;       // [T][E4]
+  float* mx = lg + n4;    // [T]
   float* den = mx + T;    // [T]
   float* sp = den + T;    // [T][k] probabilities by rank
-  for (int i = tid; i < n; i += blockDim.x) {
-    const int t = i / E, e = i - t * E;
-    lg[i] = route_key(part ? logit_from_parts(a, part, t, e) : __ldcg(a.logits + i));
+  for (int i = tid; i < n4; i += blockDim.x) {
+    const int t = i / E4, e = i - t * E4;
+    lg[i] = e < E ? route_key(part ? logit_from_parts(a, part, t, e) : __ldcg(a.logits + (size_t)t * E + e))
+                  : -INFINITY;
   }
   for (int i = tid; i < T * k; i += blockDim.x) {
     s_sel[i] = 0;  // defined even if NaN logits leave a rank unfilled
@@ -400,7 +406,7 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
-      v[i] = (e < E) ? lg[t * E + e] : -INFINITY;
+      v[i] = (e < E) ? lg[t * E4 + e] : -INFINITY;
     }
     float m = -INFINITY;
 #pragma unroll
@@ -417,23 +423,22 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
     }
   }
   __syncthreads();
-  // ranks: a warp takes 4 logits per round, 8 lanes each
-  const int sub = lane & 7;
-  for (int base = warp * 4; base < n; base += nwarps * 4) {
-    const int i = base + (lane >> 3);
-    const bool valid = i < n;
-    const int t = valid ? i / E : 0, e = valid ? i - t * E : 0;
-    const float v = valid ? lg[i] : 0.f;
+  // ranks: one thread per logit
+  for (int i = tid; i < n4; i += blockDim.x) {
+    const int t = i / E4, e = i - t * E4;
+    if (e >= E) continue;
+    const float v = lg[i];
+    const float4* row = reinterpret_cast<const float4*>(lg + t * E4);
     int r = 0;
-    if (valid)
-      for (int e2 = sub; e2 < E; e2 += 8) {
-        const float o = lg[t * E + e2];
-        r += (o > v || (o == v && e2 < e)) ? 1 : 0;
-      }
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
-    r += __shfl_xor_sync(0xffffffffu, r, 2);
-    r += __shfl_xor_sync(0xffffffffu, r, 4);
-    if (valid && sub == 0 && r < k) {
+    for (int q = 0; q < E4 / 4; ++q) {
+      const float4 o = row[q];
+      const int e0 = 4 * q;
+      r += (o.x > v || (o.x == v && e0 + 0 < e)) ? 1 : 0;
+      r += (o.y > v || (o.y == v && e0 + 1 < e)) ? 1 : 0;
+      r += (o.z > v || (o.z == v && e0 + 2 < e)) ? 1 : 0;
+      r += (o.w > v || (o.w == v && e0 + 3 < e)) ? 1 : 0;
+    }
+    if (r < k) {
       s_sel[t * k + r] = e;
       sp[t * k + r] = expf(v - mx[t]) / den[t];
     }
@@ -456,6 +461,7 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
 
 // Top-k for all T tokens, the permutation and the segment list, computed by
 // one CTA (all its threads). scratch: >= T*k + 3*E + 66 ints of shared
+// memory, 16-byte aligned
 // memory; s_scan: 33 ints of shared memory; fbuf (optional, used when
 // E <= 128): T*E + 2T + T*k floats of shared memory for the block-wide
 // top-k.
@@ -485,32 +491,49 @@ __device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* sc
     if (tid == 0) trace_mark(tr, 3);
     finish_tiny(a, s_ids, s_sorted);
   } else if constexpr (!TINY_ONLY) {
-    int* s_counts = s_ids + T * k;
+    // the counting sort by direct placement: the sorted position of pair f
+    // is the number of pairs with a lower expert id plus those with the
+    // same id and a lower flat index (stable); counts and offsets of an
+    // expert likewise by counting. The pairs are read as broadcast 128-bit
+    // shared loads (scratch padded to a multiple of 4 with an id past E).
+    const int n = T * k, n4 = (n + 3) & ~3;
+    int* s_counts = s_ids + n4;
     int* s_off = s_counts + E;
-    int* s_cur = s_off + E + 1;
     cta_softmax_topk<NV>(a, part, fbuf, s_ids);
-    for (int i = tid; i < E; i += blockDim.x) s_counts[i] = 0;
+    for (int f = n + tid; f < n4; f += blockDim.x) s_ids[f] = 0x7fffffff;
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
-    for (int f = tid; f < T * k; f += blockDim.x) atomicAdd(&s_counts[s_ids[f]], 1);
-    __syncthreads();
-    for (int i = tid; i < E; i += blockDim.x) {
-      s_off[i] = s_counts[i];
-      a.counts[i] = s_counts[i];
+    const int4* ids4 = reinterpret_cast<const int4*>(s_ids);
+    for (int f = tid; f < n; f += blockDim.x) {
+      const int e = s_ids[f];
+      int pos = 0;
+      for (int q = 0; q < n4 / 4; ++q) {
+        const int4 o = ids4[q];
+        const int f0 = 4 * q;
+        pos += (o.x < e || (o.x == e && f0 + 0 < f)) ? 1 : 0;
+        pos += (o.y < e || (o.y == e && f0 + 1 < f)) ? 1 : 0;
+        pos += (o.z < e || (o.z == e && f0 + 2 < f)) ? 1 : 0;
+        pos += (o.w < e || (o.w == e && f0 + 3 < f)) ? 1 : 0;
+      }
+      a.perm[pos] = f;
+      a.inv_perm[f] = pos;
+    }
+    for (int e = tid; e <= E; e += blockDim.x) {
+      int below = 0, at = 0;
+      for (int q = 0; q < n4 / 4; ++q) {
+        const int4 o = ids4[q];
+        below += (o.x < e ? 1 : 0) + (o.y < e ? 1 : 0) + (o.z < e ? 1 : 0) + (o.w < e ? 1 : 0);
+        at += (o.x == e ? 1 : 0) + (o.y == e ? 1 : 0) + (o.z == e ? 1 : 0) + (o.w == e ? 1 : 0);
+      }
+      a.offsets[e] = below;
+      s_off[e] = below;
+      if (e < E) {
+        a.counts[e] = at;
+        s_counts[e] = at;
+      }
     }
     __syncthreads();
-    block_exclusive_scan(s_off, E, s_scan);
-    for (int i = tid; i < E; i += blockDim.x) {
-      s_cur[i] = s_off[i];
-      a.offsets[i] = s_off[i];
-    }
-    if (tid == 0) {
-      s_off[E] = T * k;
-      a.offsets[E] = T * k;
-    }
-    __syncthreads();
-    if (warp == 0) warp_stable_scatter(a, s_ids, 0, T * k, s_cur);
-    if (warp == 1) warp_segments(a, s_counts, s_off);
+    if (warp == 0) warp_segments(a, s_counts, s_off);
     __syncthreads();
   }
 }
