@@ -61,14 +61,19 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
     a.logits[(size_t)tid * a.E + e] = v + (a.bias ? __ldg(a.bias + e) : 0.f);
   }
 
-  // the last CTA to finish its logits runs the rest of the routing
-  __threadfence();
+  // the last CTA to finish its logits runs the rest of the routing: the
+  // threads that wrote a logit fence it before the ticket (release); the
+  // ticket's taker fences after it (acquire) and the block barrier orders
+  // the finish's L2 reads after that
+  if (tid < a.T) __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
+  if (tid == 0) {
+    s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1);
+    __threadfence();
+  }
   __syncthreads();
   trace_mark(tr, 4);
   if (!s_last) return;
-  __threadfence();
 
   // dynamic shared memory: the finish scratch (T*k + 3E + 66 ints), then
   // the block top-k buffer (block_topk_fbuf_floats)
