@@ -19,7 +19,8 @@
 //      all E, the top k by (logit descending, id ascending) in two stages
 //      (the best min(k, 32) of each group of 32 ids, then the ranks among
 //      those candidates), the weights and the sorted positions of the k
-//      experts; CTA 0 publishes the routing;
+//      experts; CTA 0 publishes the routing once its output rows are
+//      written (it is read only after the launch);
 //   3. loads: work comes in units of 16 rows. The CTA's gate/up units (a
 //      contiguous range of the (selected expert, intermediate row) space)
 //      and, for every selected expert, its down rows (a contiguous range of
@@ -620,13 +621,19 @@ __device__ __forceinline__ void d1_layer(const Decode1Args& a, unsigned char* sm
   // copies without another block-wide step; many: the whole CTA.
   const bool warp_stage2 = ncand <= 64;
   if (!warp_stage2) {
+    const float4* k4 = reinterpret_cast<const float4*>(cand_key);
+    const int4* i4 = reinterpret_cast<const int4*>(cand_id);
     for (int c = tid; c < ncand; c += kD1Threads) {
       const float v = cand_key[c];
       const int id = cand_id[c];
       int r = 0;
-      for (int c2 = 0; c2 < ncand; ++c2) {
-        const float ov = cand_key[c2];
-        r += (ov > v || (ov == v && cand_id[c2] < id)) ? 1 : 0;
+      for (int q4 = 0; q4 < ncand4 / 4; ++q4) {
+        const float4 ov = k4[q4];
+        const int4 oi = i4[q4];
+        r += (ov.x > v || (ov.x == v && oi.x < id)) ? 1 : 0;
+        r += (ov.y > v || (ov.y == v && oi.y < id)) ? 1 : 0;
+        r += (ov.z > v || (ov.z == v && oi.z < id)) ? 1 : 0;
+        r += (ov.w > v || (ov.w == v && oi.w < id)) ? 1 : 0;
       }
       if (r < k) {
         sel_id[r] = id;
@@ -738,33 +745,6 @@ __device__ __forceinline__ void d1_layer(const Decode1Args& a, unsigned char* sm
     if (lane < k) sel_w[lane] = a.r.renorm ? my_p / psel : my_p;
     __syncwarp();
     if (lane == 0) trace_mark(trp, 7);
-    if (bid == 0 && go) {
-      // publish the routing (moe_layer_routing, the user's ids / weights)
-      if (lane < k) {
-        const float wv = sel_w[lane];
-        a.r.ids[lane] = my_id;
-        a.r.w[lane] = wv;
-        if (a.r.ids_user) a.r.ids_user[lane] = my_id;
-        if (a.r.w_user) a.r.w_user[lane] = wv;
-        a.r.perm[pos] = lane;
-        a.r.inv_perm[lane] = pos;
-      }
-      for (int e = lane; e <= E; e += 32) {
-        int below = 0, hit = 0;
-        for (int j = 0; j < k; ++j) {
-          below += sel_id[j] < e ? 1 : 0;
-          hit += sel_id[j] == e ? 1 : 0;
-        }
-        a.r.offsets[e] = below;
-        if (e < E) a.r.counts[e] = hit;
-      }
-      if (lane < nseg) {
-        a.r.seg_expert[lane] = seg_expert[lane];
-        a.r.seg_start[lane] = lane;
-        a.r.seg_count[lane] = 1;
-      }
-      if (lane == 0) *a.r.num_seg = nseg;
-    }
   } else {
     // consumers: parked (no issue slots taken) until the gate/up copies are
     // issued, then the scale rows by plain loads
@@ -978,6 +958,35 @@ __device__ __forceinline__ void d1_layer(const Decode1Args& a, unsigned char* sm
     }
   }
   trace_mark(tr, 24);
+  if (bid == 0 && warp == kD1Producer && !*abort_flag) {
+    // publish the routing (moe_layer_routing, the user's ids / weights):
+    // only read after the launch, so off the critical path
+    if (lane < k) {
+      const int id = sel_id[lane], pr = pos_of_rank[lane];
+      const float wv = sel_w[lane];
+      a.r.ids[lane] = id;
+      a.r.w[lane] = wv;
+      if (a.r.ids_user) a.r.ids_user[lane] = id;
+      if (a.r.w_user) a.r.w_user[lane] = wv;
+      a.r.perm[pr] = lane;
+      a.r.inv_perm[lane] = pr;
+    }
+    for (int e = lane; e <= E; e += 32) {
+      int below = 0, hit = 0;
+      for (int j = 0; j < k; ++j) {
+        below += sel_id[j] < e ? 1 : 0;
+        hit += sel_id[j] == e ? 1 : 0;
+      }
+      a.r.offsets[e] = below;
+      if (e < E) a.r.counts[e] = hit;
+    }
+    if (lane < nseg) {
+      a.r.seg_expert[lane] = seg_expert[lane];
+      a.r.seg_start[lane] = lane;
+      a.r.seg_count[lane] = 1;
+    }
+    if (lane == 0) *a.r.num_seg = nseg;
+  }
   if constexpr (STACK) {
     if (a.wr_next) {
       // the next layer's partial logits over these rows; the count releases
