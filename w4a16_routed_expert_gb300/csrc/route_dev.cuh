@@ -383,7 +383,7 @@ __host__ __device__ inline int block_topk_fbuf_floats(int T, int E, int k) {
 }
 template <int NV>
 __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const float* part, float* fbuf,
-                                                   int32_t* s_sel) {
+                                                   int32_t* s_sel, unsigned long long* tr = nullptr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int T = a.T, E = a.E, k = a.k, E4 = (E + 3) & ~3, n4 = T * E4;
   float* lg = fbuf;       // [T][E4]
@@ -400,6 +400,7 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
     sp[i] = 0.f;
   }
   __syncthreads();
+  if (tid == 0) trace_mark(tr, 6);
   // maximum and denominator, one warp per token (as warp_softmax_topk)
   for (int t = warp; t < T; t += nwarps) {
     float v[NV];
@@ -423,6 +424,7 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
     }
   }
   __syncthreads();
+  if (tid == 0) trace_mark(tr, 7);
   // ranks: one thread per logit
   for (int i = tid; i < n4; i += blockDim.x) {
     const int t = i / E4, e = i - t * E4;
@@ -444,6 +446,7 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
     }
   }
   __syncthreads();
+  if (tid == 0) trace_mark(tr, 8);
   // routing weights: the selected probabilities summed in rank order
   for (int o = tid; o < T * k; o += blockDim.x) {
     const int t = o / k;
@@ -469,9 +472,9 @@ __device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const flo
 // fbuf must be given when NV <= 4.
 template <int NV>
 __device__ __forceinline__ void cta_softmax_topk(const RouteArgs& a, const float* part, float* fbuf,
-                                                 int32_t* s_ids) {
+                                                 int32_t* s_ids, unsigned long long* tr = nullptr) {
   if constexpr (NV <= 4) {
-    block_softmax_topk<NV>(a, part, fbuf, s_ids);
+    block_softmax_topk<NV>(a, part, fbuf, s_ids, tr);
   } else {
     const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     for (int t = warp; t < a.T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * a.k, part);
@@ -499,7 +502,7 @@ __device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* sc
     const int n = T * k, n4 = (n + 3) & ~3;
     int* s_counts = s_ids + n4;
     int* s_off = s_counts + E;
-    cta_softmax_topk<NV>(a, part, fbuf, s_ids);
+    cta_softmax_topk<NV>(a, part, fbuf, s_ids, tr);
     for (int f = n + tid; f < n4; f += blockDim.x) s_ids[f] = 0x7fffffff;
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
