@@ -208,11 +208,14 @@ moe_status_t moe_layer_create(const moe_layer_config_t* config, const moe_layer_
 moe_status_t moe_layer_forward(moe_layer_t* layer, const void* x, int32_t T, void* out,
                                int32_t* topk_ids, float* topk_w, void* stream);
 
-/* Same computation for callers whose tokens live in host memory: copies x
- * (host FP16 [T][H]) to a device staging buffer, runs the forward and copies
- * out / ids / weights back into host buffers (ids, weights may be NULL).
- * Asynchronous on `stream`; page-locked host buffers make the copies
- * overlap-capable. Synchronise the stream before reading the results. */
+/* Same computation for callers whose tokens live in host memory (x host
+ * FP16 [T][H]; out, ids, weights host buffers; ids, weights may be NULL).
+ * Up to 16 tokens, when every buffer given is page-locked and mapped into
+ * the device's address space (cudaHostAlloc / pinned torch tensors on this
+ * platform), the kernels read x and write the results in place over the
+ * host link, with no staging copies. Otherwise x is copied to a device
+ * staging buffer, the forward runs, and out / ids / weights are copied back.
+ * Asynchronous on `stream`; synchronise it before reading the results. */
 moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* x_host, int32_t T, void* out_host,
                                     int32_t* topk_ids_host, float* topk_w_host, void* stream);
 
@@ -260,8 +263,9 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* prof
  * exit, 12 first down wait entered, 13 its counter seen, 14 its activations
  * staged; then for the CTA's first 8 work items, item i's bytes landed
  * (16 + 2i) and item i computed (17 + 2i), as seen by consumer warp 0.
- * Synchronises the device and copies min(max_stamps, 32 * CTAs) stamps,
- * CTA-major, into host memory; *n_stamps receives the count. */
+ * Synchronises the device and copies min(max_stamps, 32 * 1024) stamps
+ * (32 per CTA for CTAs 0..1023, CTA-major; CTAs the last launch did not
+ * have keep older stamps) into host memory; *n_stamps receives the count. */
 moe_status_t moe_layer_get_trace(moe_layer_t* layer, uint64_t* stamps, int32_t max_stamps, int32_t* n_stamps);
 
 /* Wait counters of the tensor-core GEMM path: when the handle was created

@@ -231,20 +231,29 @@ def test_repeatable_bit_for_bit_and_pdl_independent(monkeypatch):
         assert np.array_equal(a[key], b[key]) and np.array_equal(a[key], c[key]), key
 
 
-def test_forward_host_buffers_match_device_forward():
+@pytest.mark.parametrize("T,pinned", [(1, "all"), (4, "all"), (16, "all"), (24, "all"), (4, "none"), (1, "x-only")])
+def test_forward_host_buffers_match_device_forward(T, pinned):
+    # mapped (page-locked) buffers up to 16 tokens are read / written in
+    # place by the kernels; pageable ones, a mix, or more tokens go through
+    # the staging copies: the same bits every way
     shape = synth.OLMOE
     lay = synth.make_layer(shape, seed=13)
-    x = synth.make_tokens(shape.hidden, 4, seed=13)
-    ml = GH.upload(lay, max_tokens=4)
+    x = synth.make_tokens(shape.hidden, T, seed=13)
+    ml = GH.upload(lay, max_tokens=T)
     dev = GH.run(ml, x)
-    xh = torch.from_numpy(x).pin_memory()
-    oh = torch.empty_like(xh).pin_memory()
-    ih = torch.empty((4, shape.top_k), dtype=torch.int32).pin_memory()
-    wh = torch.empty((4, shape.top_k), dtype=torch.float32).pin_memory()
-    ml.forward_host(xh, oh, ih, wh)
-    ml.sync()
-    assert np.array_equal(oh.float().numpy(), dev["out"])
-    assert np.array_equal(ih.numpy(), dev["ids"]) and np.array_equal(wh.numpy(), dev["w"])
+
+    def buf(t, pin):
+        return t.pin_memory() if pin else t
+
+    xh = buf(torch.from_numpy(x), pinned in ("all", "x-only"))
+    oh = buf(torch.full(xh.shape, float("nan"), dtype=torch.float16), pinned == "all")
+    ih = buf(torch.full((T, shape.top_k), -1, dtype=torch.int32), pinned == "all")
+    wh = buf(torch.full((T, shape.top_k), float("nan"), dtype=torch.float32), pinned == "all")
+    for _ in range(2):
+        ml.forward_host(xh, oh, ih, wh)
+        ml.sync()
+        assert np.array_equal(oh.float().numpy(), dev["out"])
+        assert np.array_equal(ih.numpy(), dev["ids"]) and np.array_equal(wh.numpy(), dev["w"])
     ml.close()
 
 

@@ -18,6 +18,19 @@
 namespace {
 
 thread_local std::string g_last_error;
+constexpr int kTraceCtas = 1024;  // CTAs the phase-trace buffer holds stamps for
+constexpr int kInPlaceHostMaxT = 16;  // forward_host reads / writes mapped host buffers in place up to this T
+
+// Device address of a page-locked, mapped host buffer (nullptr for any
+// other memory).
+void* mapped_device_ptr(const void* p) {
+  cudaPointerAttributes a = {};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
 
 moe_status_t fail(moe_status_t st, const char* fmt, ...) {
   char buf[512];
@@ -118,7 +131,7 @@ size_t workspace_bytes(const moe_layer_config_t& c) {
   b += align256(T * k * 4) * 2;         // ids/w staging
   b += align256(2048 * 4);              // megakernel counters
   b += align256(64 * 4);                // batch-1 decode epoch counters
-  b += align256(1024 * moe::kTraceStamps * 8);  // phase trace (up to 1024 CTAs)
+  b += align256(kTraceCtas * moe::kTraceStamps * 8);  // phase trace
   b += align256(2 * 1024 * moe::kGemmStats * 8);  // GEMM wait counters (two launches)
   return b;
 }
@@ -707,6 +720,9 @@ moe_status_t enqueue_route(moe_layer* L, const __half* x, int T, int32_t* ids_us
   ra.err = L->err;
   const bool small = T <= moe::kSmallRouteMaxT && (size_t)T * c.hidden * 2 <= 200 * 1024;
   ra.trace = small ? L->trace : nullptr;
+  // (tracing only: the routing CTAs that do not finish leave their finish
+  // stamps at zero)
+  if (ra.trace) cudaMemsetAsync(L->trace, 0, (size_t)std::min(c.num_experts, kTraceCtas) * moe::kTraceStamps * 8, s);
   if (!small) ra.nsplit = moe::router_split(T, c.num_experts, c.hidden, L->num_sms);
   if (L->profiling) prof_record(L->ev[0], s);
   L->last_single = false;
@@ -820,6 +836,17 @@ moe_status_t moe_layer_forward_host(moe_layer_t* layer, const void* x_host, int3
   if (T == 0) return MOE_OK;
   if (!x_host || !out_host) return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must not be NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T <= kInPlaceHostMaxT) {
+    // page-locked host buffers with a device address (mapped): the kernels
+    // read x and write the results in place over the host link, no staging
+    // copies; any other buffer takes the staging path below
+    const void* xd = mapped_device_ptr(x_host);
+    void* od = mapped_device_ptr(out_host);
+    void* idd = topk_ids_host ? mapped_device_ptr(topk_ids_host) : nullptr;
+    void* wd = topk_w_host ? mapped_device_ptr(topk_w_host) : nullptr;
+    if (xd && od && (!topk_ids_host || idd) && (!topk_w_host || wd))
+      return moe_layer_forward(layer, xd, T, od, static_cast<int32_t*>(idd), static_cast<float*>(wd), stream);
+  }
   const size_t xb = (size_t)T * layer->cfg.hidden * 2, kb = (size_t)T * layer->cfg.top_k * 4;
   cudaError_t e = cudaMemcpyAsync(layer->x_stage, x_host, xb, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "x host->device");
@@ -903,7 +930,7 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* p) {
 moe_status_t moe_layer_get_trace(moe_layer_t* layer, uint64_t* stamps, int32_t max_stamps, int32_t* n_stamps) {
   if (!layer || !stamps || !n_stamps) return fail(MOE_ERR_INVALID_ARG, "layer, stamps and n_stamps must not be NULL");
   if (!layer->trace) return fail(MOE_ERR_INVALID_ARG, "tracing is off (set MOE_TRACE=1 before create)");
-  const int n = std::min(max_stamps, layer->num_sms * moe::kTraceStamps);
+  const int n = std::min(max_stamps, kTraceCtas * moe::kTraceStamps);
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(stamps, layer->trace, (size_t)n * 8, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(e, "trace read");
