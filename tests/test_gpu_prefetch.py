@@ -167,3 +167,34 @@ def test_a_failed_prefetch_is_reported_once_and_leaves_the_cache_consistent(monk
     GH.compare(lay, x, g)
     assert m.stats().faulted == 0
     m.close()
+
+
+def test_prefetch_through_the_staging_ring_of_a_pageable_backing():
+    # a pageable host copy goes through a small ring of pinned staging
+    # buffers, shared by the forwards and the prefetch thread (which the next
+    # forward waits for): results bit-identical to a pinned backing
+    shape = synth.LayerShape(512, 384, 24, 3, 128, True)
+    lays = [synth.make_layer(shape, seed=synth.stack_layer_seed(35, l)) for l in range(3)]
+    dev = torch.device("cuda")
+
+    def make(lay, pinned):
+        host = torch.from_numpy(lay.records[lay.expert_to_slot]).contiguous()
+        if pinned:
+            host = host.pin_memory()
+        return MoELayer(hidden=shape.hidden, intermediate=shape.intermediate, num_experts=shape.num_experts,
+                        top_k=shape.top_k, group_size=shape.group_size, renormalize=shape.renormalize,
+                        max_tokens=4, router_w=torch.from_numpy(lay.router_w).to(dev), num_slots=6, spare_slots=2,
+                        host_backing=host, staging_records=2, add_residual=True)
+
+    x0 = torch.from_numpy(synth.make_tokens(shape.hidden, 4, seed=35)).cuda()
+    pageable = [make(l, False) for l in lays]
+    pinned = [make(l, True) for l in lays]
+    a = _run_stack(pageable, x0, 4, prefetch=True)
+    b = _run_stack(pinned, x0, 4, prefetch=False)
+    for step in range(4):
+        for l in range(3):
+            assert np.array_equal(a[step][l], b[step][l]), (step, l)
+    st = pageable[1].stats()
+    assert st.staged_copies > 0 and st.prefetch_calls == 4 and st.faulted == 0
+    for m in pageable + pinned:
+        m.close()
