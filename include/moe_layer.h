@@ -254,9 +254,8 @@ moe_status_t moe_layer_get_profile(moe_layer_t* layer, moe_layer_profile_t* prof
  * end of the layer before), 2 the partial logits and the input loaded.
  * Small-batch routing kernel of the multi-kernel path (one CTA per
  * expert): 0 entry, 1 past the dependency, 2 the expert's logit partials
- * done, 4 its ticket taken, and in the CTA that finishes the routing 6
- * logits staged, 7 softmax statistics done, 8 ranks done, 3 top-k done,
- * 5 routing done. Small-batch decode kernel (2..16 tokens): 0 entry, 1 own
+ * done, 4 its ticket taken, and in the CTA that finishes the routing 3
+ * top-k done, 5 routing done. Small-batch decode kernel (2..16 tokens): 0 entry, 1 own
  * logit partials written, 2 all partials seen, 3 top-k done, 4 routing
  * done, 5 first gate/up item started, 6 last gate/up item done, 7 first down
  * item started, 8 consumers done, 9 finisher done, 10 all warps done, 11

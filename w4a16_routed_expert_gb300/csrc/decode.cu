@@ -96,7 +96,8 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(const DecodeArgs& a, in
   L.cs = L.bs + (uint32_t)a.bs_chunks * ns * 64u;
   L.red = L.cs + (((uint32_t)a.cs_groups * ns * 4u + 15u) & ~15u);
   L.route = L.red + ((2u * (uint32_t)tc_red_words((int)ns) * 4u + 15u) & ~15u);
-  L.total = L.route + (5u * Tk + 8u * E + 77u) * 4u;  // (+3: alignment of the finish scratch)
+  // (+3: alignment of the finish scratch)
+  L.total = L.route + (4u * Tk + 5u * E + 11u + (uint32_t)route_finish_scratch_ints(a.r.T, a.r.E, a.r.k)) * 4u;
   return L;
 }
 
@@ -106,7 +107,6 @@ __host__ __device__ inline DecodeSmem decode_smem_layout(const DecodeArgs& a, in
 template <int NV, int TMAX>
 __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int s_scan[33];
   DecodeHdr* hdr = reinterpret_cast<DecodeHdr*>(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.stages;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   int32_t* s_sstart = s_sexp + E + 1;                              // [E+1]
   int32_t* s_scount = s_sstart + E + 1;                            // [E+1]
   int32_t* s_nseg = s_scount + E + 1;                              // [1] (+3 pad)
-  // [Tk + 3E + 66], 16-byte aligned (the routing finish reads it 128 bits at a time)
+  // route_finish_scratch_ints(T, E, k), 16-byte aligned
   int32_t* s_scratch = s_nseg + 4 + ((4u - ((smem_u32(s_nseg + 4) >> 2) & 3u)) & 3u);
 
   if (tid == 0) {
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
     L.seg_count = s_scount;
     L.num_seg = s_nseg;
     // the ring is idle until routing is done: block top-k buffer
-    route_finish_cta<NV, TMAX == 1>(L, s_scratch, s_scan, a.r.logit_part, tr, reinterpret_cast<float*>(ring));
+    route_finish_cta<NV, TMAX == 1>(L, s_scratch, a.r.logit_part, tr);
     __syncthreads();
     trace_mark(tr, 4);
     nseg = *s_nseg;
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
   const int ng_it = (int)((long long)(blockIdx.x + 1) * tot_g / gridDim.x) - fg;
   const int nd_it = (int)((long long)(blockIdx.x + 1) * tot_d / gridDim.x) - fd;
   const int n_it = *abort_flag ? 0 : ng_it + nd_it;
-  const int combine_cap = Tk + 3 * E + 66;      // the routing scratch, free after routing
+  const int combine_cap = route_finish_scratch_ints(T, E, k);  // the routing scratch, free after routing
   const uint32_t gu_target = (uint32_t)nrb_g;  // gate/up items per segment
   const uint32_t dn_target = (uint32_t)nseg;   // down items per row block
 

@@ -37,7 +37,6 @@ template <int NV>
 __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ __align__(16) float s_part[kSmallRouteMaxT * kLogitParts];
-  __shared__ int s_scan[33];
   __shared__ int s_last;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int e = blockIdx.x;
@@ -75,12 +74,9 @@ __global__ void __launch_bounds__(kLogitParts * 32) k_route_small(RouteArgs a) {
   trace_mark(tr, 4);
   if (!s_last) return;
 
-  // dynamic shared memory: the finish scratch (T*k + 3E + 66 ints), then
-  // the block top-k buffer (block_topk_fbuf_floats)
+  // dynamic shared memory: the finish scratch (route_finish_scratch_ints)
   int32_t* scratch = reinterpret_cast<int32_t*>(smem);
-  // (the top-k buffer takes 128-bit loads: its start rounded to 16 bytes)
-  float* fbuf = reinterpret_cast<float*>(scratch + ((a.T * a.k + 3 * a.E + 66 + 3) & ~3));
-  route_finish_cta<NV>(a, scratch, s_scan, nullptr, tr, fbuf);
+  route_finish_cta<NV>(a, scratch, nullptr, tr);
   trace_mark(tr, 5);
   if (tid == 0) *a.ticket = 0u;
 }
@@ -293,8 +289,7 @@ __global__ void __launch_bounds__(kScatterThreads) k_scatter(RouteArgs a) {
 
 template <int NV>
 cudaError_t launch_route_small_nv(const RouteArgs& a, cudaStream_t s, bool pdl) {
-  const size_t fbytes = (((size_t)a.T * a.k + 3 * (size_t)a.E + 66 + 3) & ~(size_t)3) * sizeof(int) +
-                        (size_t)block_topk_fbuf_floats(a.T, a.E, a.k) * sizeof(float);
+  const size_t fbytes = (size_t)route_finish_scratch_ints(a.T, a.E, a.k) * sizeof(int);
   cudaError_t e = ensure_smem(k_route_small<NV>, fbytes);
   if (e != cudaSuccess) return e;
   return launch_ex(k_route_small<NV>, dim3(a.E), dim3(kLogitParts * 32), fbytes, s, pdl, a);

@@ -136,6 +136,55 @@ __device__ __forceinline__ float logit_from_planes(const RouteArgs& a, int t, in
 // that routes the same logits derives the same selection.
 __device__ __forceinline__ float route_key(float v) { return v != v ? -INFINITY : v; }
 
+// Bitonic sort of the warp's 32 NV (key, id) pairs, best first: larger key
+// first, lower id first among equal keys (ids distinct, so the order is
+// total). Position NV * lane + i is register i of the lane; pairs at
+// distance d < NV are exchanged within a lane, the others with lane ^ (d / NV).
+// A pair of a block of `size` positions is put in order when the block's
+// index bit `size` is 0, in reverse otherwise.
+template <int NV>
+__device__ __forceinline__ void warp_bitonic_best_first(float (&key)[NV], int (&id)[NV]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32 * NV; size <<= 1) {
+#pragma unroll
+    for (int d = size >> 1; d > 0; d >>= 1) {
+      if (d < NV) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          if (i & d) continue;
+          const int j = i | d;
+          const bool fwd = ((NV * lane + i) & size) == 0;
+          const bool j_ahead = key[j] > key[i] || (key[j] == key[i] && id[j] < id[i]);
+          if (fwd == j_ahead) {
+            const float tk = key[i];
+            key[i] = key[j];
+            key[j] = tk;
+            const int ti = id[i];
+            id[i] = id[j];
+            id[j] = ti;
+          }
+        }
+      } else {
+        const int ld = d / NV;
+        const bool lower = (lane & ld) == 0;
+        const bool fwd = ((NV * lane) & size) == 0;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          const float ok = __shfl_xor_sync(0xffffffffu, key[i], ld);
+          const int oi = __shfl_xor_sync(0xffffffffu, id[i], ld);
+          const bool other_ahead = ok > key[i] || (ok == key[i] && oi < id[i]);
+          // the lower position of a forward pair keeps the better element
+          if ((lower == fwd) == other_ahead) {
+            key[i] = ok;
+            id[i] = oi;
+          }
+        }
+      }
+    }
+  }
+}
+
 // One warp: softmax over the E logits of token t and selection of the top k
 // (largest logit first, lower id first among equal logits). NV = values held
 // per lane (E <= 32 * NV). Writes ids / weights to the workspace, the user
@@ -172,41 +221,21 @@ __device__ __forceinline__ void warp_softmax_topk(const RouteArgs& a, int t, int
   float my_p = 0.f, psel = 0.f;
   int my_id = 0;
   if constexpr (NV <= 4) {
-    // Rank selection (E <= 128): the rank of a logit is the number of logits
-    // ahead of it (larger, or equal with a lower id); the top k are ranks
-    // 0..k-1. Every comparison is independent, so the warp has no serial
-    // chain of k reductions.
-    int rank[NV];
+    // Sort selection (E <= 128): the warp's 32 NV (logit, id) pairs sorted
+    // best first by a bitonic network in registers; rank j then sits in
+    // lane j / NV, register j % NV, and lane j < k takes it.
+    int id[NV];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) rank[i] = 0;
-#pragma unroll 4
-    for (int o = 0; o < 32; ++o) {
-#pragma unroll
-      for (int i2 = 0; i2 < NV; ++i2) {
-        const float ov = __shfl_sync(0xffffffffu, v[i2], o);
-        const int oe = o + 32 * i2;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          const int e = lane + 32 * i;
-          rank[i] += (ov > v[i] || (ov == v[i] && oe < e)) ? 1 : 0;
-        }
-      }
-    }
-    // lane j takes the logit of rank j: walk the selected set (known to every
-    // lane through ballots) and pick the holder whose rank is j
+    for (int i = 0; i < NV; ++i) id[i] = lane + 32 * i;
+    warp_bitonic_best_first<NV>(v, id);
     float my_v = -INFINITY;
 #pragma unroll
-    for (int i2 = 0; i2 < NV; ++i2) {
-      uint32_t sel = __ballot_sync(0xffffffffu, lane + 32 * i2 < E && rank[i2] < k);
-      while (sel) {
-        const int src = __ffs(sel) - 1;
-        sel &= sel - 1;
-        const int r = __shfl_sync(0xffffffffu, rank[i2], src);
-        const float sv = __shfl_sync(0xffffffffu, v[i2], src);
-        if (r == lane) {
-          my_id = src + 32 * i2;
-          my_v = sv;
-        }
+    for (int i = 0; i < NV; ++i) {
+      const float sv = __shfl_sync(0xffffffffu, v[i], lane / NV);
+      const int si = __shfl_sync(0xffffffffu, id[i], lane / NV);
+      if (lane % NV == i) {
+        my_v = sv;
+        my_id = si;
       }
     }
     my_p = expf(my_v - m) / ssum;
@@ -367,176 +396,76 @@ __device__ __forceinline__ void finish_tiny(const RouteArgs& a, int32_t* s_ids, 
   for (int e = tid; e < a.E; e += blockDim.x) a.counts[e] = s_ids[32 + e + 1] - s_ids[32 + e];
 }
 
-// Softmax and top-k of all T tokens with every thread of the CTA (E <= 128):
-// the same results, bit for bit, as warp_softmax_topk, with the work spread
-// out. Each logit's rank (the number of logits of its token ahead of it:
-// larger, or equal with a lower id) is counted by one thread against its
-// token's row, read as broadcast 128-bit shared loads (rows padded to a
-// multiple of 4 with -inf, which never ranks ahead); ranks 0..k-1 are the
-// selection. The softmax maximum and denominator of a token are computed by
-// one warp exactly as in warp_softmax_topk. fbuf: T*E4 + 2T + T*k floats of
-// shared memory (E4 = E rounded up to a multiple of 4, block_topk_fbuf_floats).
-// Writes ids / weights to a.ids, a.w, the user buffers (if any) and s_sel
-// ([T][k], by rank).
-__host__ __device__ inline int block_topk_fbuf_floats(int T, int E, int k) {
-  return T * ((E + 3) & ~3) + 2 * T + T * k;
-}
+// Top-k for all T tokens, the permutation and the segment list, computed by
+// one CTA (all its threads), one warp per token for the top-k.
+// scratch: route_finish_scratch_ints(T, E, k) ints of shared memory.
+// TINY_ONLY: the caller guarantees T * k <= 32 (only that path is compiled).
 template <int NV>
-__device__ __forceinline__ void block_softmax_topk(const RouteArgs& a, const float* part, float* fbuf,
-                                                   int32_t* s_sel, unsigned long long* tr = nullptr) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int T = a.T, E = a.E, k = a.k, E4 = (E + 3) & ~3, n4 = T * E4;
-  float* lg = fbuf;       // [T][E4]
-  float* mx = lg + n4;    // [T]
-  float* den = mx + T;    // [T]
-  float* sp = den + T;    // [T][k] probabilities by rank
-  for (int i = tid; i < n4; i += blockDim.x) {
-    const int t = i / E4, e = i - t * E4;
-    lg[i] = e < E ? route_key(part ? logit_from_parts(a, part, t, e) : __ldcg(a.logits + (size_t)t * E + e))
-                  : -INFINITY;
-  }
-  for (int i = tid; i < T * k; i += blockDim.x) {
-    s_sel[i] = 0;  // defined even if NaN logits leave a rank unfilled
-    sp[i] = 0.f;
-  }
-  __syncthreads();
-  if (tid == 0) trace_mark(tr, 6);
-  // maximum and denominator, one warp per token (as warp_softmax_topk)
-  for (int t = warp; t < T; t += nwarps) {
-    float v[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < E) ? lg[t * E4 + e] : -INFINITY;
-    }
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) m = fmaxf(m, v[i]);
-    m = warp_max(m);
-    float ssum = 0.f;
-#pragma unroll
-    for (int i = 0; i < NV; ++i)
-      if (lane + 32 * i < E) ssum += expf(v[i] - m);
-    ssum = warp_sum(ssum);
-    if (lane == 0) {
-      mx[t] = m;
-      den[t] = ssum;
-    }
-  }
-  __syncthreads();
-  if (tid == 0) trace_mark(tr, 7);
-  // ranks: one thread per logit
-  for (int i = tid; i < n4; i += blockDim.x) {
-    const int t = i / E4, e = i - t * E4;
-    if (e >= E) continue;
-    const float v = lg[i];
-    const float4* row = reinterpret_cast<const float4*>(lg + t * E4);
-    int r = 0;
-    for (int q = 0; q < E4 / 4; ++q) {
-      const float4 o = row[q];
-      const int e0 = 4 * q;
-      r += (o.x > v || (o.x == v && e0 + 0 < e)) ? 1 : 0;
-      r += (o.y > v || (o.y == v && e0 + 1 < e)) ? 1 : 0;
-      r += (o.z > v || (o.z == v && e0 + 2 < e)) ? 1 : 0;
-      r += (o.w > v || (o.w == v && e0 + 3 < e)) ? 1 : 0;
-    }
-    if (r < k) {
-      s_sel[t * k + r] = e;
-      sp[t * k + r] = expf(v - mx[t]) / den[t];
-    }
-  }
-  __syncthreads();
-  if (tid == 0) trace_mark(tr, 8);
-  // routing weights: the selected probabilities summed in rank order
-  for (int o = tid; o < T * k; o += blockDim.x) {
-    const int t = o / k;
-    float psel = 0.f;
-    for (int j = 0; j < k; ++j) psel += sp[t * k + j];
-    const float p = sp[o];
-    const float wv = a.renorm ? p / psel : p;
-    const int id = s_sel[o];
-    a.ids[o] = id;
-    a.w[o] = wv;
-    if (a.ids_user) a.ids_user[o] = id;
-    if (a.w_user) a.w_user[o] = wv;
-  }
+__device__ __forceinline__ void cta_softmax_topk(const RouteArgs& a, const float* part, int32_t* s_ids) {
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int t = warp; t < a.T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * a.k, part);
 }
 
-// Top-k for all T tokens, the permutation and the segment list, computed by
-// one CTA (all its threads). scratch: >= T*k + 3*E + 66 ints of shared
-// memory, 16-byte aligned
-// memory; s_scan: 33 ints of shared memory; fbuf (optional, used when
-// E <= 128): T*E + 2T + T*k floats of shared memory for the block-wide
-// top-k.
-// TINY_ONLY: the caller guarantees T * k <= 32 (only that path is compiled).
-// fbuf must be given when NV <= 4.
-template <int NV>
-__device__ __forceinline__ void cta_softmax_topk(const RouteArgs& a, const float* part, float* fbuf,
-                                                 int32_t* s_ids, unsigned long long* tr = nullptr) {
-  if constexpr (NV <= 4) {
-    block_softmax_topk<NV>(a, part, fbuf, s_ids, tr);
-  } else {
-    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    for (int t = warp; t < a.T; t += nwarps) warp_softmax_topk<NV>(a, t, s_ids + t * a.k, part);
-  }
-}
+__host__ __device__ inline int route_finish_scratch_ints(int T, int E, int k) { return T * k + 3 * E + 66; }
 
 template <int NV, bool TINY_ONLY = false>
-__device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* scratch, int* s_scan,
-                                                 const float* part, unsigned long long* tr, float* fbuf) {
-  const int tid = threadIdx.x, warp = tid >> 5;
+__device__ __forceinline__ void route_finish_cta(const RouteArgs& a, int32_t* scratch, const float* part,
+                                                 unsigned long long* tr) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = a.T, E = a.E, k = a.k;
   int32_t* s_ids = scratch;
   if (TINY_ONLY || T * k <= 32) {
     int32_t* s_sorted = s_ids + 32 + E + 1;
-    cta_softmax_topk<NV>(a, part, fbuf, s_ids);
+    cta_softmax_topk<NV>(a, part, s_ids);
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
     finish_tiny(a, s_ids, s_sorted);
   } else if constexpr (!TINY_ONLY) {
-    // the counting sort by direct placement: the sorted position of pair f
-    // is the number of pairs with a lower expert id plus those with the
-    // same id and a lower flat index (stable); counts and offsets of an
-    // expert likewise by counting. The pairs are read as broadcast 128-bit
-    // shared loads (scratch padded to a multiple of 4 with an id past E).
-    const int n = T * k, n4 = (n + 3) & ~3;
-    int* s_counts = s_ids + n4;
-    int* s_off = s_counts + E;
-    cta_softmax_topk<NV>(a, part, fbuf, s_ids, tr);
-    for (int f = n + tid; f < n4; f += blockDim.x) s_ids[f] = 0x7fffffff;
+    // the counting sort: counts by shared-memory atomic adds (integers: the
+    // order of the adds does not matter), then one warp scans them into
+    // offsets and places the pairs in flat order, 32 at a time (stable)
+    const int n = T * k;
+    int* s_counts = s_ids + n;    // [E]
+    int* s_off = s_counts + E;    // [E + 1]
+    int* s_cur = s_off + E + 1;   // [E] placement cursors
+    for (int e = tid; e < E; e += blockDim.x) s_counts[e] = 0;
+    cta_softmax_topk<NV>(a, part, s_ids);
     __syncthreads();
     if (tid == 0) trace_mark(tr, 3);
-    const int4* ids4 = reinterpret_cast<const int4*>(s_ids);
-    for (int f = tid; f < n; f += blockDim.x) {
-      const int e = s_ids[f];
-      int pos = 0;
-      for (int q = 0; q < n4 / 4; ++q) {
-        const int4 o = ids4[q];
-        const int f0 = 4 * q;
-        pos += (o.x < e || (o.x == e && f0 + 0 < f)) ? 1 : 0;
-        pos += (o.y < e || (o.y == e && f0 + 1 < f)) ? 1 : 0;
-        pos += (o.z < e || (o.z == e && f0 + 2 < f)) ? 1 : 0;
-        pos += (o.w < e || (o.w == e && f0 + 3 < f)) ? 1 : 0;
-      }
-      a.perm[pos] = f;
-      a.inv_perm[f] = pos;
-    }
-    for (int e = tid; e <= E; e += blockDim.x) {
-      int below = 0, at = 0;
-      for (int q = 0; q < n4 / 4; ++q) {
-        const int4 o = ids4[q];
-        below += (o.x < e ? 1 : 0) + (o.y < e ? 1 : 0) + (o.z < e ? 1 : 0) + (o.w < e ? 1 : 0);
-        at += (o.x == e ? 1 : 0) + (o.y == e ? 1 : 0) + (o.z == e ? 1 : 0) + (o.w == e ? 1 : 0);
-      }
-      a.offsets[e] = below;
-      s_off[e] = below;
-      if (e < E) {
-        a.counts[e] = at;
-        s_counts[e] = at;
-      }
-    }
+    for (int f = tid; f < n; f += blockDim.x) atomicAdd(&s_counts[s_ids[f]], 1);
     __syncthreads();
-    if (warp == 0) warp_segments(a, s_counts, s_off);
+    if (warp == 0) {
+      // lane l scans the experts [l * per, (l + 1) * per)
+      const int per = (E + 31) / 32, e0 = lane * per;
+      int sum = 0;
+      for (int i = 0; i < per; ++i)
+        if (e0 + i < E) sum += s_counts[e0 + i];
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - sum;
+      for (int i = 0; i < per; ++i) {
+        const int e = e0 + i;
+        if (e < E) {
+          const int c = s_counts[e];
+          s_off[e] = run;
+          s_cur[e] = run;
+          a.offsets[e] = run;
+          a.counts[e] = c;
+          run += c;
+        }
+      }
+      if (lane == 31) {
+        s_off[E] = incl;
+        a.offsets[E] = incl;
+      }
+      __syncwarp();
+      warp_stable_scatter(a, s_ids, 0, n, s_cur);
+      warp_segments(a, s_counts, s_off);
+    }
     __syncthreads();
   }
 }
