@@ -270,9 +270,10 @@ moe_status_t moe_layer_get_trace(moe_layer_t* layer, uint64_t* stamps, int32_t m
 /* Wait counters of the tensor-core GEMM path: when the handle was created
  * with MOE_GEMM_STATS=1, each CTA of the last gate/up and down GEMM records
  * 9 cycle counts: producer waiting for a free code stage and a free token
- * stage; MMA thread waiting for a free accumulator, a full A stage and a
- * full token stage; dequantiser warp 0 waiting for codes and for a free A
- * stage; epilogue warp 0 waiting for an accumulator; the CTA's total. Layout
+ * stage; MMA thread waiting for a free accumulator and a full A stage;
+ * dequantiser warp 0 waiting for a landed token stage, for codes and for a
+ * free A stage; epilogue warp 0 waiting for an accumulator; the CTA's
+ * total. Layout
  * [launch (gate/up, down)][CTA][9]. Synchronises the device and copies
  * min(max_values, 2 * 9 * CTAs) counts; *n_values receives the count. */
 moe_status_t moe_layer_get_gemm_stats(moe_layer_t* layer, uint64_t* values, int32_t max_values, int32_t* n_values);

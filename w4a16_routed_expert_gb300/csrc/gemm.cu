@@ -2,32 +2,40 @@
 //
 // Horizon RunMap report, "What is implemented": the INT4 experts stay compact
 // in GPU memory and run with FP16 activations; here a weight tile is expanded
-// to FP16 only inside shared memory, for the MMAs that consume it.
+// to FP16 only on chip (in tensor memory), for the MMAs that consume it.
 //
-// Tile = 128 MMA rows x 256 tokens of one expert segment. The weights are
-// the MMA's A operand (M = 128) and the tokens its B operand (N = 256), so
-// each dequantised weight row serves 256 tokens; the accumulator's TMEM lane
+// Tile = 128 MMA rows x 192 tokens of one expert segment. The weights are
+// the MMA's A operand (M = 128) and the tokens its B operand (N = 192), so
+// each dequantised weight row serves 192 tokens; the accumulator's TMEM lane
 // is the output unit, its column the token. Gate/up tiles interleave the two
 // matrices in M: row 2u is gate unit i0+u, row 2u+1 is up unit i0+u (64 units
 // per tile), so SwiGLU pairs sit in adjacent lanes and meet with one shuffle.
 //
+// The A operand is read from tensor memory (tcgen05.mma with [a-tmem]): the
+// dequantisers store each FP16 row to its TMEM lane, so shared memory carries
+// only the token tiles (TMA write + MMA read) and the INT4 codes. Tensor
+// memory holds two accumulator buffers (2 x 192 columns) and four A stages
+// (4 x 32 columns).
+//
 // Warp roles of a persistent CTA (one per SM):
-//   warp 0      TMA producer: INT4 code tiles (3-D tensor map over the slot
-//               pool: bytes x rows x slot; one 128-byte-wide swizzled box
-//               covers four K steps) and token tiles (2-D 256-row boxes of
-//               the expert-sorted activations: x gathered in sorted order
-//               for gate/up, h for down). A 2-D box of 32 KB streams at ~45
-//               bytes per SM-cycle from L2 on this part, small boxes cost
-//               about as much each, so every K step is one large box.
+//   warp 0      TMA producer of the token tiles (2-D 192-row boxes of the
+//               expert-sorted activations: x gathered in sorted order for
+//               gate/up, h for down). A 2-D box streams at ~45 bytes per
+//               SM-cycle from L2 on this part and small boxes cost about as
+//               much each, so every K step is one large box.
 //   warp 1      TMEM allocation and the single MMA-issuing thread
-//   warps 2-9   dequantisers: codes -> (q - 8) * s in FP16, written in the
-//               128-byte-swizzled K-major layout the MMA reads
-//   warps 10-13 epilogue: TMEM -> registers; gate/up: h = silu(g) * u -> FP16
+//   warps 2-9   dequantisers: codes -> (q - z) * s in FP16, one row per
+//               thread, stored to the A stage in tensor memory
+//   warps 10-17 epilogue: TMEM -> registers; gate/up: h = silu(g) * u -> FP16
 //               h rows; down: FP32 partial rows at the pair's flat index
-// Rings: codes (TMA -> dequant), A (dequant -> MMA), B (TMA -> MMA), and two
-// TMEM accumulator buffers (MMA -> epilogue), each with full/empty mbarriers.
-// Every wait is bounded; a wait that gives up records an error, the CTA
-// drains its in-flight copies and MMAs, frees TMEM and exits.
+//   warp 18     TMA producer of the INT4 code tiles (3-D tensor map over the
+//               slot pool: bytes x rows x slot; one 128-byte-wide swizzled
+//               box covers four K steps)
+// Rings: codes (TMA -> dequant), A (dequant -> MMA, tensor memory), B (TMA ->
+// MMA), and two TMEM accumulator buffers (MMA -> epilogue), each with
+// full/empty mbarriers. Every wait is bounded; a wait that gives up records
+// an error, the CTA drains its in-flight copies and MMAs, frees TMEM and
+// exits.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -41,12 +49,12 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;  // MMA rows per tile (DUAL: 64 gate + 64 up, interleaved)
-constexpr int BN = 256;  // tokens per tile
+constexpr int BN = 192;  // tokens per tile
 constexpr int BK = 64;   // K per pipeline step (128 bytes of FP16)
 constexpr int kCodeK = 4;  // K steps per code tile: 128 bytes of codes per row, one swizzled TMA box
 constexpr int kCodeStages = 4;
-constexpr int kAStages = 3;
-constexpr int kBStages = 3;
+constexpr int kAStages = 4;  // FP16 weight tiles in tensor memory
+constexpr int kBStages = 4;
 constexpr int kDequantWarps = 8;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each half of the columns
 constexpr int kWarpProducer = 0;
@@ -59,11 +67,9 @@ constexpr int kMaxSeg = 1025;
 
 template <bool DUAL>
 struct Smem {
-  static constexpr uint32_t a_tile = BM * BK * 2;      // 16 KB
-  static constexpr uint32_t b_tile = BN * BK * 2;      // 32 KB
+  static constexpr uint32_t b_tile = BN * BK * 2;      // 24 KB
   static constexpr uint32_t code_tile = BM * kCodeK * BK / 2;  // 16 KB (DUAL: 64 gate rows then 64 up rows)
-  static constexpr uint32_t off_a = 0;
-  static constexpr uint32_t off_b = off_a + kAStages * a_tile;
+  static constexpr uint32_t off_b = 0;
   static constexpr uint32_t off_codes = off_b + kBStages * b_tile;
   static constexpr uint32_t off_bar = off_codes + kCodeStages * code_tile;
   // codes_full/empty, a_full/empty, b_full/empty, acc_full/empty, drain
@@ -73,9 +79,15 @@ struct Smem {
   static constexpr uint32_t off_epi = off_prefix + ((kMaxSeg + 1) * 4 + 15) / 16 * 16;  // [BN] output rows of a tile
   static constexpr uint32_t bytes = off_epi + BN * 4;
   static constexpr uint32_t alloc = bytes + 1024;  // slack for 1024-byte alignment
+  // tensor memory: two FP32 accumulator buffers of BN columns, then the
+  // FP16 A stages (BK / 2 columns each: two K elements per column)
   static constexpr uint32_t tmem_cols = 512;
-  static constexpr uint32_t acc_stride = BN;        // two accumulator buffers of 256 columns
+  static constexpr uint32_t acc_stride = BN;
+  static constexpr uint32_t a_col0 = 2 * BN;
+  static constexpr uint32_t a_cols = BK / 2;
   static constexpr int units = DUAL ? BM / 2 : BM;  // output units per tile
+  static_assert(a_col0 + kAStages * a_cols <= tmem_cols, "tensor memory over-committed");
+  static_assert(b_tile % 1024 == 0, "token stages must keep the 1024-byte swizzle alignment");
 };
 
 struct Bars {
@@ -310,7 +322,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
-      unsigned long long sw[3] = {0, 0, 0};
+      unsigned long long sw[2] = {0, 0};
       uint32_t g = 0;
       int j = 0;
       bool ok = true;
@@ -322,18 +334,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t d0 = tbase + (uint32_t)ab * L::acc_stride;
         for (int kk = 0; kk < nK; ++kk, ++g) {
           const int sa = g % kAStages, sb = g % kBStages;
-          if (!timed_wait(&B.a_full[sa], (g / kAStages) & 1u, abort_flag, a.err, st_cta ? &sw[1] : nullptr) ||
-              !timed_wait(&B.b_full[sb], (g / kBStages) & 1u, abort_flag, a.err, st_cta ? &sw[2] : nullptr)) {
+          // one wait per K step: the dequantisers arrive on a_full only once
+          // the step's token tile has landed (each waits on b_full first), so
+          // a full A stage means a full token stage too. A wait in this loop
+          // stalls the MMA stream (the issuing thread's queue of MMAs drains
+          // meanwhile), so the loop holds as few as possible.
+          if (!timed_wait(&B.a_full[sa], (g / kAStages) & 1u, abort_flag, a.err, st_cta ? &sw[1] : nullptr)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(smem + L::off_a + (uint32_t)sa * L::a_tile);
+          const uint32_t a0 = tbase + L::a_col0 + (uint32_t)sa * L::a_cols;
           const uint32_t bb = smem_u32(smem + L::off_b + (uint32_t)sb * L::b_tile);
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
             const uint32_t acc = (kk > 0 || k16 > 0) ? 1u : 0u;
-            mma_f16(d0, smem_desc_sw128(a0 + k16 * 32), smem_desc_sw128(bb + k16 * 32), idesc, acc);
+            mma_f16_ts(d0, a0 + k16 * 8, smem_desc_sw128(bb + k16 * 32), idesc, acc);
           }
           misc->mma_issued = 1;
           mma_commit(&B.a_empty[sa]);
@@ -345,16 +361,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (st_cta) {
         st_cta[2] = sw[0];
         st_cta[3] = sw[1];
-        st_cta[4] = sw[2];
       }
     }
   } else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------ dequant
     // Two groups of kDequantWarps / 2 warps take alternate K steps (group
     // par takes the steps kk with kk % 2 == par), so two A stages fill at
-    // once; a thread converts one A row (64 codes) per step.
+    // once; a thread converts one A row (64 codes) per step and stores it
+    // to its TMEM lane, which fixes the row: a warp reaches the lane quarter
+    // warp % 4 only (the four warps of a group cover the four quarters).
     const int par = (warp - kWarpDequant0) / (kDequantWarps / 2);
-    const int r = tid - kWarpDequant0 * 32 - par * (kDequantWarps / 2) * 32;  // A row 0..127
+    const int r = 32 * (warp & 3) + lane;  // A row 0..127 = TMEM lane
+    const uint32_t a_lane = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + L::a_col0;
     // A row r: DUAL -> unit r/2 of the gate (even r) or up (odd r) matrix,
     // codes row r/2 or 64 + r/2 of the stage; single -> row r.
     const int unit = DUAL ? (r >> 1) : r;
@@ -362,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int crow = DUAL ? ((r & 1) ? 64 + (r >> 1) : (r >> 1)) : r;
     const bool rec = st_cta && warp == kWarpDequant0 && lane == 0;
     uint32_t gbase = 0, gc = 0;  // K steps of the previous tiles, code groups (the producer's order)
-    unsigned long long dw[2] = {0, 0};
+    unsigned long long dw[3] = {0, 0, 0};
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const int s = find_segment(prefix, nseg, t);
@@ -421,24 +439,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
+          tc_fence_after();
           // codes of K step kk: 16-byte chunks 2 (kk % kCodeK) and + 1 of the
           // row's 128 bytes, at their 128-byte-swizzle positions
           const int cc = (kk % kCodeK) * 2;
           const uint4 w0 = *reinterpret_cast<const uint4*>(crowp + ((cc ^ (crow & 7)) << 4));
           const uint4 w1 = *reinterpret_cast<const uint4*>(crowp + (((cc + 1) ^ (crow & 7)) << 4));
-          unsigned char* rowp = smem + L::off_a + (uint32_t)sa * L::a_tile + r * (BK * 2);
           const __half2 s_lo = __half2half2(__ushort_as_half((unsigned short)(sv & 0xFFFFu)));
           const __half2 s_hi = __half2half2(__ushort_as_half((unsigned short)(sv >> 16)));
           // 1024 + z: exponent-bias form of the zero point (exact)
           const __half2 b_lo = __half2half2(__ushort_as_half((unsigned short)(0x6400u + (zv & 0xFFFFu))));
           const __half2 b_hi = __half2half2(__ushort_as_half((unsigned short)(0x6400u + (zv >> 16))));
           const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          // columns 4c .. 4c + 3 of the row: the 8 halves of word c in k order
+          uint32_t col[32];
 #pragma unroll
-          for (int c = 0; c < 8; ++c)  // 16-byte chunk c (8 halves) of the 128-byte A row
-            *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) =
-                dequant8(words[c], c < 4 ? s_lo : s_hi, c < 4 ? b_lo : b_hi);
-          fence_proxy_async_smem();
-          __syncwarp();
+          for (int c = 0; c < 8; ++c) {
+            const uint4 q = dequant8(words[c], c < 4 ? s_lo : s_hi, c < 4 ? b_lo : b_hi);
+            col[4 * c + 0] = q.x;
+            col[4 * c + 1] = q.y;
+            col[4 * c + 2] = q.z;
+            col[4 * c + 3] = q.w;
+          }
+          tmem_st32(a_lane + (uint32_t)sa * L::a_cols, col);
+          tmem_st_wait();
+          tc_fence_before();
+          // the step's token tile must have landed before the arrival
+          const int sb = g % kBStages;
+          if (lane == 0)
+            good = timed_wait(&B.b_full[sb], (g / kBStages) & 1u, abort_flag, a.err, rec ? &dw[2] : nullptr);
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
           if (lane == 0) mbar_arrive(&B.a_full[sa]);
         }
         if (!ok) break;
@@ -449,13 +483,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       gbase += (uint32_t)nK;
     }
     if (st_cta && warp == kWarpDequant0 && lane == 0) {
+      st_cta[4] = dw[2];
       st_cta[5] = dw[0];
       st_cta[6] = dw[1];
     }
   } else {
     // ----------------------------------------------------------- epilogue
     // Warp e of the epilogue reads TMEM lanes 32 * (warp % 4) .. + 31 (its
-    // accumulator rows) and columns 128 * (e / 4) .. + 127 (its tokens).
+    // accumulator rows) and columns (BN / 2) * (e / 4) .. + BN / 2 - 1 (its
+    // tokens).
     const int e = warp - kWarpEpi0, et = tid - kWarpEpi0 * 32;
     const int q = warp & 3, ch = e >> 2;
     const int row = 32 * q + lane;
@@ -497,13 +533,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // DUAL: even lanes own gate unit row/2, odd lanes its up value
       const int gunit = m0 + (DUAL ? (row >> 1) : row);
       const bool rvalid = gunit < a.N;
-      const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * L::acc_stride + 128u * ch;
+      const uint32_t tacc = tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)ab * L::acc_stride + (BN / 2) * ch;
 #pragma unroll 1
       for (int cb = 0; cb < BN / 64; ++cb) {
         uint32_t v[32];
         tmem_ld32(tacc + cb * 32, v);
         tmem_ld_wait();
-        const int c0 = 128 * ch + cb * 32;
+        const int c0 = (BN / 2) * ch + cb * 32;
         if (DUAL) {
 #pragma unroll
           for (int c = 0; c < 32; ++c) {

@@ -79,9 +79,9 @@ struct GemmArgs {
   unsigned long long* stats;    // nullable: [gridDim][kGemmStats] cycles spent waiting, per role
 };
 // GEMM wait counters per CTA: producer (codes stage free, token stage free),
-// MMA (accumulator free, A stage full, token stage full), dequantiser warp 0
-// (codes landed, A stage free), epilogue warp 0 (accumulator full), and the
-// CTA's total cycles.
+// MMA (accumulator free, A stage full), dequantiser warp 0 (token stage
+// landed, codes landed, A stage free), epilogue warp 0 (accumulator full),
+// and the CTA's total cycles.
 constexpr int kGemmStats = 9;
 
 // Whole-layer decode megakernel (T <= kSmallRouteMaxT, full residency).
