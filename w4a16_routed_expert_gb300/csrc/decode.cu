@@ -200,7 +200,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) k_decode(const __grid_const
     L.seg_start = s_sstart;
     L.seg_count = s_scount;
     L.num_seg = s_nseg;
-    // the ring is idle until routing is done: block top-k buffer
     route_finish_cta<NV, TMAX == 1>(L, s_scratch, a.r.logit_part, tr);
     __syncthreads();
     trace_mark(tr, 4);
