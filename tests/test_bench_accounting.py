@@ -3,6 +3,7 @@ algorithmic bytes (every selected expert's record read once, the router
 weights, x in and out) and FLOPs (2 H E per token for the router, 6 H I per
 (token, expert) pair for gate/up/down), plus its launch and throughput
 accounting. CPU only."""
+import json
 import os
 import sys
 
@@ -91,3 +92,21 @@ def test_parity_rows_cover_small_batches_and_sample_large_ones():
     assert bench._parity_rows(64).tolist() == list(range(64))
     r = bench._parity_rows(8192)
     assert len(r) == 64 and r[0] == 0 and r[-1] == 8191 and (np.diff(r) > 0).all()
+
+
+def test_traffic_is_reported_only_for_unchanged_sources(tmp_path, monkeypatch):
+    """A recorded DRAM-traffic figure is returned while the kernel's sources
+    hash to the recorded state, and None once any of them changes."""
+    csrc = tmp_path / "w4a16_routed_expert_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in bench.KERNEL_SOURCES["gemm"]:
+        (csrc / f).write_text(f"// {f}\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    files = [f"w4a16_routed_expert_gb300/csrc/{f}" for f in bench.KERNEL_SOURCES["gemm"]]
+    rec = {"w": {"gate_up": {"dram_bytes_per_launch": 123, "source_sha": bench.source_hash(*files)}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
+    assert bench.kernel_traffic("w", "gate_up", True) == 123
+    assert bench.kernel_traffic("w", "down", True) is None
+    (csrc / "tc.cuh").write_text("// changed\n")
+    assert bench.kernel_traffic("w", "gate_up", True) is None
