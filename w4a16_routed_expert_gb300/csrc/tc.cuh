@@ -1,6 +1,6 @@
 // Blackwell tensor-core helpers (sm_100 family): TMA tensor loads, TMEM
-// allocation, tcgen05.mma (kind::f16, FP32 accumulate; A from shared or
-// tensor memory), commit, TMEM loads and stores.
+// allocation, tcgen05.mma (kind::f16, FP32 accumulate, A from tensor
+// memory and B from shared memory), commit, TMEM loads and stores.
 // Thin inline-PTX wrappers; descriptor bit layouts follow the PTX ISA
 // (tcgen05 "Instruction descriptor" and "Shared memory descriptor").
 #pragma once
@@ -28,23 +28,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
       "l"(tm), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
-// Four rows (r0..r3) of a 2-D tensor, columns [c0, c0 + box), into four
-// consecutive box rows at dst.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tm, int c0, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-      "l"(tm), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
-}
-// Generic-proxy writes to shared memory become visible to the async proxy
-// (tensor core operand reads).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TMEM
@@ -80,16 +65,6 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread: A (M rows on the
 // TMEM lanes, K along the columns, two FP16 per 32-bit column, element 2c in
 // the low half of column c) read from tensor memory.
