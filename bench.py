@@ -196,9 +196,9 @@ def algorithmic(shape, T, eu):
 # Sources each measured kernel is built from: a DRAM-traffic figure recorded
 # under profiles/ is reported only while these files are unchanged.
 KERNEL_SOURCES = {
-    "decode": ["decode.cu", "tcgemv_dev.cuh", "route_dev.cuh", "common.cuh", "kernels.h"],
-    "decode1": ["decode1.cu", "tcgemv_dev.cuh", "route_dev.cuh", "common.cuh", "kernels.h"],
-    "gemv": ["gemv.cu", "tcgemv_dev.cuh", "common.cuh", "kernels.h"],
+    "decode": ["decode.cu", "tcgemv_dev.cuh", "route_dev.cuh", "tc.cuh", "common.cuh", "kernels.h"],
+    "decode1": ["decode1.cu", "tcgemv_dev.cuh", "route_dev.cuh", "tc.cuh", "common.cuh", "kernels.h"],
+    "gemv": ["gemv.cu", "tcgemv_dev.cuh", "tc.cuh", "common.cuh", "kernels.h"],
     "gemm": ["gemm.cu", "tc.cuh", "common.cuh", "kernels.h"],
 }
 
